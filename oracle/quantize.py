@@ -1,0 +1,62 @@
+"""Per-(block, KV head) absmax FP8 E4M3 quantisation (oracle; test only).
+
+The page "Paged Attention and KV Cache Fragmentation", section "Quantization
+as a way to stretch paged memory further", motivates FP8 KV caches (half the
+BF16 footprint) and warns that accumulation must stay in full fp32.  It fixes
+neither the scale granularity nor the rounding; this restatement takes the
+plainest reading, one fp32 scale per (physical block, KV head), separately for
+K and V:
+
+    a      = max |x|  over the block's valid tokens and the head dimension
+    scale  = a / 448            (fp32 IEEE division; 1.0 when a == 0)
+    code   = e4m3_rne_satfinite(x / scale)   (fp32 IEEE division per element)
+
+Slots at or beyond the block's valid length are written as code 0 (+0.0).
+Dequantised value = decode(code) * scale.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from . import e4m3
+
+
+def block_scale(x_block_f32: np.ndarray) -> np.float32:
+    """Scale of one (block, head) tile: fp32 absmax / 448, or 1 when all zero."""
+    a = np.float32(np.max(np.abs(x_block_f32))) if x_block_f32.size else np.float32(0)
+    if a == 0:
+        return np.float32(1.0)
+    return np.float32(a) / np.float32(e4m3.E4M3_MAX)
+
+
+def quantize_tile(x_tile_f32: np.ndarray, valid: int):
+    """Quantise one [block_size, d] tile; returns (uint8 codes, fp32 scale)."""
+    x = np.asarray(x_tile_f32, dtype=np.float32)
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    s = block_scale(x[:valid])
+    if valid > 0:
+        q = (x[:valid] / s).astype(np.float32)     # fp32 IEEE divide
+        codes[:valid] = e4m3.encode_fast(q)
+    return codes, s
+
+
+def quantize_blocks(cache_f32: np.ndarray, block_ids, valid_lens):
+    """Quantise listed blocks of a [num_blocks, Hkv, bs, d] cache.
+
+    Returns (codes uint8 [num_blocks, Hkv, bs, d], scales fp32 [num_blocks,
+    Hkv]).  Blocks not listed keep code 0 and scale 1.
+    """
+    nb, hkv, bs, d = cache_f32.shape
+    codes = np.zeros((nb, hkv, bs, d), dtype=np.uint8)
+    scales = np.ones((nb, hkv), dtype=np.float32)
+    for blk, valid in zip(block_ids, valid_lens):
+        for h in range(hkv):
+            c, s = quantize_tile(cache_f32[blk, h], int(valid))
+            codes[blk, h] = c
+            scales[blk, h] = s
+    return codes, scales
+
+
+def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """fp64 values decode(code) * scale for a whole [nb, Hkv, bs, d] cache."""
+    return e4m3.decode(codes) * scales.astype(np.float64)[:, :, None, None]

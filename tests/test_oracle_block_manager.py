@@ -1,0 +1,131 @@
+"""Pins for the oracle's block-manager model.
+
+* LIFO order and all-or-nothing allocation, written out by hand;
+* conservation: free + distinct live blocks == pool size, and every live
+  block's refcount equals the number of tables holding it, under random
+  seeded op sequences;
+* errors (double free, bad ids, out of blocks) leave the state unchanged;
+* copy-on-write fires exactly when a shared block is partially filled;
+* the footprint formula reproduces the page's 70B / 128K numbers.
+"""
+import copy
+import os
+
+import numpy as np
+
+from oracle import block_manager as BM
+from oracle import footprint
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "kv_footprint_70b_128k.txt")
+
+
+def test_lifo_order_by_hand():
+    m = BM.BlockManagerModel(5)
+    assert m.alloc(3) == (BM.OK, [0, 1, 2])
+    assert m.free([1]) == BM.OK
+    assert m.alloc(1) == (BM.OK, [1])
+    assert m.free([2, 0]) == BM.OK
+    assert m.alloc(3) == (BM.OK, [0, 2, 3])
+    assert m.num_free() == 1
+
+
+def test_all_or_nothing_and_errors():
+    m = BM.BlockManagerModel(4)
+    st, ids = m.alloc(3)
+    snap = copy.deepcopy(m.__dict__)
+    assert m.alloc(2) == (BM.OUT_OF_BLOCKS, None)
+    assert m.free([0, 0]) == BM.BAD_BLOCK_ID          # more frees than refs
+    assert m.free([7]) == BM.BAD_BLOCK_ID
+    assert m.fork([3]) == BM.BAD_BLOCK_ID             # 3 is free
+    assert m.alloc(-1) == (BM.INVALID_ARG, None)
+    assert m.__dict__ == snap
+    assert m.fork([0]) == BM.OK and m.free([0, 0]) == BM.OK
+    assert m.free([0]) == BM.BAD_BLOCK_ID
+
+
+def test_append_allocates_only_on_block_boundaries():
+    m = BM.BlockManagerModel(10)
+    table = []
+    st, slots, pairs = m.append_slots(table, 0, 5, 4, 8)
+    assert st == BM.OK and table == [0, 1] and slots == [0, 1, 2, 3, 4]
+    st, slots, pairs = m.append_slots(table, 5, 3, 4, 8)
+    assert table == [0, 1] and slots == [5, 6, 7] and pairs == []
+    st, slots, pairs = m.append_slots(table, 8, 1, 4, 8)
+    assert table == [0, 1, 2] and slots == [8]
+    assert m.append_slots(table, 9, 40, 4, 8)[0] == BM.INVALID_ARG
+
+
+def test_copy_on_write_of_shared_partial_tail():
+    m = BM.BlockManagerModel(8)
+    parent = []
+    m.append_slots(parent, 0, 6, 4, 4)                  # blocks [0, 1], 6 tokens
+    child = list(parent)
+    assert m.fork(child) == BM.OK
+    st, slots, pairs = m.append_slots(child, 6, 1, 4, 4)
+    assert st == BM.OK and pairs == [(1, 2, 2)]
+    assert child == [0, 2] and parent == [0, 1] and slots == [2 * 4 + 2]
+    assert m.get_refcount(1) == (BM.OK, 1) and m.get_refcount(0) == (BM.OK, 2)
+    # the last holder appends in place: no copy
+    st, slots, pairs = m.append_slots(parent, 6, 1, 4, 4)
+    assert pairs == [] and slots == [1 * 4 + 2]
+    # a full shared block needs no copy: the next token opens a new block
+    p2 = []
+    m.append_slots(p2, 0, 4, 4, 4)
+    m.fork(p2)
+    st, slots, pairs = m.append_slots(list(p2), 4, 1, 4, 4)
+    assert pairs == []
+
+
+def test_out_of_blocks_append_changes_nothing():
+    m = BM.BlockManagerModel(3)
+    t = []
+    m.append_slots(t, 0, 8, 4, 4)
+    m.fork(t)
+    snap = copy.deepcopy(m.__dict__)
+    t2 = list(t)
+    assert m.append_slots(t2, 8, 5, 4, 4)[0] == BM.OUT_OF_BLOCKS
+    assert m.__dict__ == snap and t2 == t
+
+
+def test_conservation_under_random_ops():
+    rng = np.random.default_rng(0)
+    N, bs = 64, 4
+    m = BM.BlockManagerModel(N)
+    seqs = {}
+    for step in range(3000):
+        op = rng.integers(0, 4)
+        if op == 0 or not seqs:                      # new or grow
+            sid = int(rng.integers(0, 12))
+            t, n = seqs.get(sid, ([], 0))
+            k = int(rng.integers(1, 9))
+            st, _, _ = m.append_slots(t, n, k, bs, 32)
+            if st == BM.OK:
+                seqs[sid] = (t, n + k)
+        elif op == 1:                                # fork
+            sid = list(seqs)[int(rng.integers(0, len(seqs)))]
+            t, n = seqs[sid]
+            new = 100 + step
+            if m.fork(t) == BM.OK:
+                seqs[new] = (list(t), n)
+        else:                                        # finish
+            sid = list(seqs)[int(rng.integers(0, len(seqs)))]
+            t, n = seqs.pop(sid)
+            assert m.free(t) == BM.OK
+        holders = {}
+        for t, _ in seqs.values():
+            for b in t:
+                holders[b] = holders.get(b, 0) + 1
+        assert m.num_free() + len(holders) == N
+        for b in range(N):
+            assert m.refcount[b] == holders.get(b, 0)
+
+
+def test_footprint_matches_page_numbers():
+    for line in open(GOLDEN):
+        if line.startswith("#") or not line.strip():
+            continue
+        L, H, d, T, s2, gb = line.split()
+        b = int(T) * footprint.kv_bytes_per_token(int(L), int(H), int(d), 1) * int(s2) // 2
+        assert round(b / 1e9, 1) == float(gb)
+    # one layer of the 70B / 128K request, bf16: exactly 2 * 8 * 128 * 131072 * 2
+    assert footprint.decode_step_kv_bytes([131072], 8, 128, 2) == 536870912
