@@ -1,0 +1,522 @@
+"""Benchmark of the paged decode hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl native|reference]
+
+One step = one decode layer-step of the whole hot path on one batch:
+pa_cache_write of the step's new K/V (one appended token per sequence),
+pa_decode (paged attention over every cached token) and its split-K merge.
+The host block manager has already placed the appended tokens (its cost is
+reported separately).  Inputs are seeded synthetic tensors shaped like the
+workload, resident in HBM; consecutive steps rotate over several
+independent layer pools so that each step streams its KV from DRAM rather
+than from the 129 MB L2.
+
+The JSON line reports algorithmic KV-read GB/s (sum over sequences of
+n * Hkv * d * 2 * bytes, the per-token footprint formula with L = 1) per
+step, sequences/s, the decode kernel's roofline against the measured HBM
+copy bandwidth, an end-to-end figure through the public API with host
+buffers, and the fp64 CPU oracle timed on a bounded sample.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU
+(the path needs no collective); value = bytes of all ranks / slowest rank.
+``--impl reference`` times the fp64 CPU oracle on the same workload instead.
+"""
+from __future__ import annotations
+
+import os
+
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import hashlib
+import json
+import math
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-decode KV-read HBM GB/s (% of GB300 peak) and seqs/s per layer-step"
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- setup ---
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "pa_device.cuh", "libpa.cu"):
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_228_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    p = os.path.join(ROOT, "profiles", "decode_dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(workload)
+    if not e or e.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed loop runs."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        if not self.lines:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ---
+def make_pools(w, n_pools, device):
+    from paged_kv_cache_228_gb300 import workloads as W
+    shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    pools = []
+    for i in range(n_pools):
+        k = W.normal_bf16(shape, w.seed * 100 + 2 * i, device, w.outlier_prob, w.outlier_scale)
+        v = W.normal_bf16(shape, w.seed * 100 + 2 * i + 1, device, w.outlier_prob,
+                          w.outlier_scale)
+        pools.append((k, v))
+    return pools
+
+
+def step_inputs(w, device):
+    """Block manager (native) places the pre-step tokens and the appended
+    ones; returns tables, lens, slots and the host-manager time per append."""
+    from paged_kv_cache_228_gb300 import pa
+    from paged_kv_cache_228_gb300 import workloads as W
+    maxb = w.max_blocks_per_seq
+    alloc, tables, lens = pa.replay_script(W.build_script(w), w.num_seqs, w.block_size, maxb,
+                                           w.pool_blocks)
+    t0 = time.perf_counter()
+    slots = []
+    for b in range(w.num_seqs):
+        st, s, _ = alloc.append_slots(tables[b], lens[b], 1, w.block_size, maxb)
+        assert st == pa.PA_OK
+        slots += s
+    host_us = (time.perf_counter() - t0) * 1e6
+    tab = torch.full((w.num_seqs, maxb), -1, dtype=torch.int32)
+    for b, t in enumerate(tables):
+        tab[b, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    return (tables, tab.to(device), torch.tensor(w.seq_lens, dtype=torch.int32, device=device),
+            torch.tensor(slots, dtype=torch.int64, device=device), host_us)
+
+
+def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
+    """Algorithmic KV bytes of one layer-step: per-token footprint
+    2 * H_kv * d_h * s (one layer) for every cached token, plus, for FP8,
+    the K and V scales of every (block, KV head) a sequence touches."""
+    total = 0
+    for n in w.seq_lens:
+        total += n * 2 * w.num_kv_heads * w.head_dim * bytes_per_scalar
+        if scale_bytes:
+            total += 2 * (-(-n // w.block_size)) * w.num_kv_heads * scale_bytes
+    return total
+
+
+# ----------------------------------------------------------- native arm ---
+def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None):
+    from paged_kv_cache_228_gb300 import pa
+    from paged_kv_cache_228_gb300 import workloads as W
+    per_pool = w.pool_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
+    if n_pools is None:
+        n_pools = max(1, min(8, math.ceil(4 * L2_BYTES / per_pool)))
+    pools = make_pools(w, n_pools, device)
+    tables, tab, lens, slots, host_us = step_inputs(w, device)
+    q = W.normal_bf16((w.num_seqs, w.num_q_heads, w.head_dim), w.seed * 100 + 50, device)
+    kn = W.normal_bf16((w.num_seqs, w.num_kv_heads, w.head_dim), w.seed * 100 + 51, device)
+    vn = W.normal_bf16((w.num_seqs, w.num_kv_heads, w.head_dim), w.seed * 100 + 52, device)
+    out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                      device=device)
+    ws = torch.empty(max(16, pa.pa_decode_workspace_size(
+        w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim)), dtype=torch.uint8,
+        device=device)
+    scales = [(None, None)] * n_pools
+    if fp8:
+        qpools, scales = [], []
+        ids = torch.arange(w.pool_blocks, dtype=torch.int32, device=device)
+        valid = torch.full((w.pool_blocks,), w.block_size, dtype=torch.int32, device=device)
+        for k, v in pools:
+            kq = torch.empty(k.shape, dtype=torch.uint8, device=device)
+            vq = torch.empty_like(kq)
+            ks = torch.empty((w.pool_blocks, w.num_kv_heads), device=device)
+            vs = torch.empty_like(ks)
+            pa.pa_quantize_fp8(k, v, ids, valid, kq, vq, ks, vs)
+            qpools.append((kq, vq))
+            scales.append((ks, vs))
+        del pools
+        pools = qpools
+    stream = torch.cuda.current_stream()
+    pa.pa_get_device_error()
+
+    def step(i, ev=None):
+        k, v = pools[i % n_pools]
+        ks, vs = scales[i % n_pools]
+        if not fp8:
+            pa.pa_cache_write(kn, vn, slots, k, v, stream=stream)
+        if ev is not None:
+            ev[0].record(stream)
+        pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks, v_scale=vs,
+                     stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler = sample_clocks() if sample_clocks else None
+    if sampler:
+        time.sleep(0.3)  # let nvidia-smi start sampling
+    t_start.record(stream)
+    for i in range(steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.stop()
+    if torch.distributed.is_initialized():
+        torch.distributed.barrier()
+    total_ms = t_start.elapsed_time(t_end)
+    dec_ms = [a.elapsed_time(b) for a, b in evs]
+    err = pa.pa_get_device_error()
+    if err:
+        raise RuntimeError(f"device error word 0x{err:x} during the benchmark")
+
+    # CUDA-graph replay of one step per pool (launch overhead amortised)
+    graph_ms = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        s2 = torch.cuda.Stream()
+        s2.wait_stream(stream)
+        with torch.cuda.stream(s2):
+            with torch.cuda.graph(g, stream=s2):
+                for i in range(n_pools):
+                    k, v = pools[i]
+                    ks, vs = scales[i]
+                    if not fp8:
+                        pa.pa_cache_write(kn, vn, slots, k, v, stream=s2)
+                    pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks,
+                                 v_scale=vs, stream=s2)
+        stream.wait_stream(s2)
+        reps = max(1, steps // n_pools)
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(reps):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_ms = a.elapsed_time(b) / (reps * n_pools)
+    except Exception as e:  # graph capture is an extra figure only
+        graph_ms = f"unavailable: {type(e).__name__}: {e}"
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(w, pools[0], scales[0], tab, lens, slots, q, kn, vn, ws, fp8, stream,
+                  max(20, min(steps, 2000)))
+    return {
+        "ms_per_step": total_ms / steps,
+        "decode_ms_mean": statistics.mean(dec_ms),
+        "decode_ms_median": statistics.median(dec_ms),
+        "graph_ms_per_step": graph_ms,
+        "host_append_us": host_us,
+        "n_pools": n_pools,
+        "pool_bytes": per_pool // (2 if fp8 else 1),
+        "clocks": sampler.summary() if sampler else None,
+        "e2e": e2e,
+        "launches_per_step": (1 if fp8 else 2) + 1,
+    }
+
+
+def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps):
+    """Per step: pinned host -> device copies of q, new K/V, slots, block
+    tables and lengths; cache write + decode; device -> host copy of out."""
+    from paged_kv_cache_228_gb300 import pa
+    h = {n: t.cpu().pin_memory() for n, t in
+         dict(q=q, kn=kn, vn=vn, slots=slots, tab=tab, lens=lens).items()}
+    d = {n: torch.empty_like(t) for n, t in dict(q=q, kn=kn, vn=vn, slots=slots, tab=tab,
+                                                  lens=lens).items()}
+    out_h = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
+                        pin_memory=True)
+    out_d = torch.empty(out_h.shape, dtype=torch.bfloat16, device=q.device)
+    k, v = pool
+    ks, vs = scale
+    h2d = sum(t.numel() * t.element_size() for t in h.values())
+    d2h = out_h.numel() * out_h.element_size()
+
+    def one():
+        for n in h:
+            d[n].copy_(h[n], non_blocking=True)
+        if not fp8:
+            pa.pa_cache_write(d["kn"], d["vn"], d["slots"], k, v, stream=stream)
+        pa.pa_decode(d["q"], k, v, d["tab"], d["lens"], w.scale, out_d, ws, k_scale=ks,
+                     v_scale=vs, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(5):
+        one()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        one()
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    return {"ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------ oracle arm ---
+def oracle_sample(w, device, budget_s):
+    """Time the fp64 oracle (as it stands) on whole (sequence, KV head)
+    segments of this workload for about ``budget_s`` seconds; returns
+    (GB/s, segments, seconds)."""
+    from oracle import paged_attention as OPA
+    from paged_kv_cache_228_gb300 import workloads as W
+    tables, _, _, _, _ = step_inputs(w, "cpu")
+    shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    done_bytes, done, t_used = 0, 0, 0.0
+    G = w.group
+    for b in range(w.num_seqs):
+        # only this sequence's blocks are materialised on the host
+        kb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b, device)
+        vb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b + 500, device)
+        kk = kb.float().cpu().numpy()
+        vv = vb.float().cpu().numpy()
+        qq = W.normal_bf16((w.num_q_heads, w.head_dim), w.seed * 1000 + b + 900,
+                           device).double().cpu().numpy()
+        local = np.arange(len(tables[b]))
+        for gk in range(w.num_kv_heads):
+            t0 = time.perf_counter()
+            kc = OPA.gather_sequence(kk[:, gk:gk + 1], local, w.seq_lens[b], w.block_size)[:, 0]
+            vc = OPA.gather_sequence(vv[:, gk:gk + 1], local, w.seq_lens[b], w.block_size)[:, 0]
+            for h in range(gk * G, (gk + 1) * G):
+                OPA.attend(qq[h], kc, vc, w.scale)
+            t_used += time.perf_counter() - t0
+            done += 1
+            done_bytes += w.seq_lens[b] * w.head_dim * 2 * 2
+            if t_used >= budget_s:
+                return done_bytes / t_used / 1e9, done, t_used
+    return done_bytes / max(t_used, 1e-9) / 1e9, done, t_used
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    vals = []
+    segs = 0
+    for i in range(args.warmup + args.steps):
+        v, n, _ = oracle_sample(w, "cpu", budget)
+        if i >= args.warmup:
+            vals.append(v)
+            segs = n
+    value = statistics.mean(vals)
+    cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": f"{segs} whole (sequence, KV head) segments of {w.name} per step, "
+                     f"fp64 numpy, single-threaded BLAS"}
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name}, "cpu_baseline": cpu,
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+# ------------------------------------------------------------------ main ---
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="llama3.1-8b")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    from paged_kv_cache_228_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]()
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    device = f"cuda:{local}" if ws > 1 else "cuda"
+    from paged_kv_cache_228_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if ws > 1:
+        torch.distributed.barrier()
+    from paged_kv_cache_228_gb300 import pa
+    pa.lib()
+
+    gpu_index = local
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        try:
+            gpu_index = int(vis.split(",")[local])
+        except ValueError:
+            pass
+    res = run_native(w, args.steps, args.warmup, device,
+                     sample_clocks=(lambda: ClockSampler(gpu_index)) if rank == 0 else None)
+    nbytes = kv_bytes(w)
+    step_s = res["ms_per_step"] / 1e3
+    if ws > 1:
+        t = torch.tensor([step_s], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_s = float(t.item())
+    value = nbytes * ws / step_s / 1e9
+    peak, peak_kind = peaks()
+    dec_s = res["decode_ms_mean"] / 1e3
+    achieved = nbytes / dec_s / 1e9
+    secondary = {}
+    if rank == 0 and not args.no_secondary and args.workload != "llama3.1-70b-128k":
+        wl = W.llama31_70b_128k()
+        for fp8 in (False, True):
+            r = run_native(wl, max(20, args.steps // 50), max(3, args.warmup // 10), device,
+                           fp8=fp8, n_pools=1)
+            nb = kv_bytes(wl, 1 if fp8 else 2, 4 if fp8 else 0)
+            secondary["llama3.1-70b-128k_" + ("fp8" if fp8 else "bf16")] = {
+                "kv_bytes_per_step": nb,
+                "us_per_step": r["ms_per_step"] * 1e3,
+                "GB_per_s": nb / (r["ms_per_step"] / 1e3) / 1e9,
+                "decode_us": r["decode_ms_mean"] * 1e3,
+                "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
+                "hbm_frac_of_measured": nb / (r["decode_ms_mean"] / 1e3) / 1e9 / peak,
+                "seqs_per_s": wl.num_seqs / (r["ms_per_step"] / 1e3),
+                "graph_us_per_step": (r["graph_ms_per_step"] * 1e3
+                                      if isinstance(r["graph_ms_per_step"], float) else
+                                      r["graph_ms_per_step"]),
+            }
+    cpu = None
+    if rank == 0:
+        v, segs, secs = oracle_sample(w, "cpu", args.cpu_budget)
+        cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{segs} whole (sequence, KV head) segments of {w.name} "
+                         f"({secs:.1f} s), fp64 numpy, single-threaded BLAS"}
+    e2e = res["e2e"]
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V, Q; scattered blocks)",
+            "config": {
+                "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+                "block_size": w.block_size, "kv_bytes_per_step": nbytes,
+                "mean_seq_len": sum(w.seq_lens) / w.num_seqs,
+                "l2": f"inputs larger than L2: {res['n_pools']} rotating layer pools of "
+                      f"{res['pool_bytes'] / 1e9:.2f} GB",
+                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "step": "pa_cache_write + pa_decode (+ split merge), eager launches",
+            },
+            "seqs_per_s": w.num_seqs * ws / step_s,
+            "us_per_step": step_s * 1e6,
+            "hbm_frac": value / ws / peak,
+            "graph_us_per_step": (res["graph_ms_per_step"] * 1e3
+                                  if isinstance(res["graph_ms_per_step"], float)
+                                  else res["graph_ms_per_step"]),
+            "host_block_manager_us_per_append": res["host_append_us"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+                         "kernel": "paged_decode_kernel<128,bf16> + merge (per launch pair)",
+                         "peak_source": peak_kind},
+            "cpu_baseline": cpu,
+            "e2e": {"value": nbytes / (e2e["ms_per_step"] / 1e3) / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                    "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                    "ms_per_step": e2e["ms_per_step"]},
+            "gpu_launches": res["launches_per_step"] * args.steps,
+            "clocks": res["clocks"],
+            "secondary": secondary,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * pa.h -- C ABI of libpa, a paged KV cache and paged decode attention
+ * library for NVIDIA GB300 (sm_103a).
+ *
+ * The method (three web pages on KV cache fragmentation and PagedAttention):
+ *   - "KV cache fragmentation" (field guide), section "Definition": the KV
+ *     cache is cut into small fixed-size pages; each request owns a logical
+ *     sequence of pages that may sit anywhere in physical memory, reached
+ *     through a small indirection table, and the attention kernel walks that
+ *     table.
+ *   - "Paged Attention and KV Cache Fragmentation", section "How
+ *     PagedAttention maps an OS concept onto GPU memory": fixed-size blocks
+ *     holding a set number of key/value vectors per head; a block table per
+ *     request mapping logical positions to physical blocks; blocks allocated
+ *     only as a sequence grows and freed when it finishes; requests with a
+ *     shared prefix point at the same physical blocks.
+ *   - same page, section "Quantization as a way to stretch paged memory
+ *     further": FP8 KV caches with full fp32 accumulation.
+ *
+ * Conventions (all entry points):
+ *   - Every function returns a pa_status; nothing throws or aborts.
+ *   - Arguments are validated on the host before anything is enqueued; on a
+ *     failed check the call returns PA_ERR_INVALID_ARG (or
+ *     PA_ERR_UNSUPPORTED for a valid but unimplemented shape) and has no
+ *     side effects.
+ *   - Device entry points take caller-owned DEVICE pointers, enqueue work on
+ *     `stream` (a cudaStream_t passed as void*; NULL = legacy default stream)
+ *     and return without synchronising.  A launch failure returns
+ *     PA_ERR_CUDA.  Device pointers must be 16-byte aligned.
+ *   - Data-dependent errors found on the device (a block id outside the
+ *     pool, a slot outside the pool, a sequence longer than its table) never
+ *     fault: the offending access is skipped (reads become zeros) and a bit
+ *     is set in a per-device error word read by pa_get_device_error().
+ *   - The library allocates no device memory in any entry point except that
+ *     the CUDA runtime lazily creates its context.  The only host memory it
+ *     owns is the opaque pa_allocator.
+ *   - Layouts are dense, row-major (last index fastest):
+ *       k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *                          bf16 (PA_KV_BF16) or E4M3 bytes (PA_KV_FP8_E4M3)
+ *       k_scale, v_scale : float [num_blocks][num_kv_heads] (FP8 only)
+ *       block_tables     : int32 [num_seqs][max_blocks_per_seq]; entries at
+ *                          or past ceil(seq_len / block_size) are never read
+ *                          (pad them with -1)
+ *       seq_lens         : int32 [num_seqs], lengths including the token
+ *                          appended by this step
+ *       q, out           : bf16 [num_seqs][num_q_heads][head_dim]
+ *     Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pa_status {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* bad pointer, size, shape or alignment       */
+  PA_ERR_OUT_OF_BLOCKS = 2, /* allocator: not enough free blocks           */
+  PA_ERR_BAD_BLOCK_ID = 3,  /* allocator: id outside the pool or not live  */
+  PA_ERR_CUDA = 4,          /* a CUDA runtime call failed                  */
+  PA_ERR_UNSUPPORTED = 5,   /* valid request, shape not implemented        */
+  PA_ERR_WORKSPACE = 6      /* workspace missing or smaller than required  */
+} pa_status;
+
+typedef enum pa_kv_dtype {
+  PA_KV_BF16 = 0,
+  PA_KV_FP8_E4M3 = 1
+} pa_kv_dtype;
+
+/* Bits of the per-device error word (pa_get_device_error). */
+#define PA_DEVERR_BAD_BLOCK_ID 0x1u /* table entry outside [0, num_blocks)  */
+#define PA_DEVERR_BAD_SEQ_LEN  0x2u /* seq_len < 0 or > table capacity      */
+#define PA_DEVERR_BAD_SLOT     0x4u /* slot >= num_blocks * block_size      */
+#define PA_DEVERR_BAD_PAIR     0x8u /* copy pair id/length outside the pool */
+#define PA_DEVERR_TIMEOUT      0x10u /* a pipeline wait hit its bound       */
+#define PA_DEVERR_LAUNCH       0x20u /* internal launch-layout check failed */
+
+/* Version of this ABI; bumped on any incompatible change. */
+int32_t pa_abi_version(void);
+
+/* Static, human-readable name of a status code. */
+const char* pa_status_string(pa_status status);
+
+/* Read and clear the current device's error word (bits PA_DEVERR_*).
+ * Synchronises the current device.  `err` (host) receives the bits. */
+pa_status pa_get_device_error(uint32_t* err);
+
+/* ------------------------------------------------------------------ cache
+ * pa_cache_write -- scatter this step's new K/V into the cache.
+ * "Paged Attention and KV Cache Fragmentation", section "How PagedAttention
+ * maps an OS concept onto GPU memory": new tokens land in the block the
+ * table names for their position.  For each token t < num_tokens with
+ * s = slot_mapping[t] >= 0:
+ *     k_cache[s / block_size][h][s % block_size][:] = k_new[t][h][:]
+ *     v_cache[s / block_size][h][s % block_size][:] = v_new[t][h][:]
+ * for every KV head h, copied bit for bit.  Negative slots are skipped.
+ *   k_new, v_new   device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping   device int64 [num_tokens]
+ *   k_cache/v_cache device bf16 pools (layout above)
+ * Slots >= num_blocks * block_size are skipped and flag
+ * PA_DEVERR_BAD_SLOT.  Two tokens naming the same slot give an unspecified
+ * winner.  kv_dtype must be PA_KV_BF16 (FP8 append: PA_ERR_UNSUPPORTED).
+ * head_dim must be a multiple of 8. */
+pa_status pa_cache_write(const void* k_new, const void* v_new,
+                         const int64_t* slot_mapping, int32_t num_tokens,
+                         void* k_cache, void* v_cache, int32_t num_blocks,
+                         int32_t num_kv_heads, int32_t block_size,
+                         int32_t head_dim, pa_kv_dtype kv_dtype, void* stream);
+
+/* pa_copy_blocks -- copy-on-write of shared partial blocks.
+ * "Paged Attention and KV Cache Fragmentation", section "How PagedAttention
+ * maps an OS concept onto GPU memory": sequences sharing physical blocks
+ * diverge only where their content differs.  For each pair p:
+ *     (src, dst, n) = pairs[3p], pairs[3p+1], pairs[3p+2]
+ *     cache[dst][h][0:n][:] = cache[src][h][0:n][:]  for all heads, K and V
+ * and, for FP8 caches, k_scale[dst][h] = k_scale[src][h] (likewise v).
+ *   pairs          device int32 [num_pairs][3] (pa_seq_append_slots output)
+ *   k_scale/v_scale device float pools or NULL (must be non-NULL for FP8)
+ * Pairs with an id outside the pool or n outside [0, block_size] are
+ * skipped and flag PA_DEVERR_BAD_PAIR.  Pairs must not overlap (no dst may
+ * be another pair's src). */
+pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale,
+                         float* v_scale, const int32_t* pairs,
+                         int32_t num_pairs, int32_t num_blocks,
+                         int32_t num_kv_heads, int32_t block_size,
+                         int32_t head_dim, pa_kv_dtype kv_dtype, void* stream);
+
+/* pa_quantize_fp8 -- build FP8 E4M3 cache blocks from bf16 blocks.
+ * "Paged Attention and KV Cache Fragmentation", section "Quantization as a
+ * way to stretch paged memory further" (FP8 halves the KV footprint).  For
+ * each listed block b = block_ids[i] with n = valid_lens[i] valid tokens,
+ * each KV head h, separately for K and V:
+ *     a     = max |x| over tokens [0, n) and the head dimension (fp32)
+ *     scale = a / 448 (IEEE fp32 division), or 1 when a == 0
+ *     dst[b][h][t][:] = e4m3_rne_satfinite(src[b][h][t][:] / scale), t < n
+ *     dst[b][h][t][:] = 0 (code +0), n <= t < block_size
+ *     scale_out[b][h] = scale
+ *   k_src, v_src    device bf16 pools; k_dst, v_dst device uint8 pools
+ *   block_ids, valid_lens device int32 [num_ids]
+ * Ids outside the pool or n outside [0, block_size] are skipped and flag
+ * PA_DEVERR_BAD_BLOCK_ID. */
+pa_status pa_quantize_fp8(const void* k_src, const void* v_src,
+                          const int32_t* block_ids, const int32_t* valid_lens,
+                          int32_t num_ids, uint8_t* k_dst, uint8_t* v_dst,
+                          float* k_scale, float* v_scale, int32_t num_blocks,
+                          int32_t num_kv_heads, int32_t block_size,
+                          int32_t head_dim, void* stream);
+
+/* ----------------------------------------------------------------- decode
+ * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
+ * this shape with `num_splits` work partitions (0 = the automatic choice
+ * for the current device).  Writes the size to *bytes (host). */
+pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                   int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t num_splits, size_t* bytes);
+
+/* pa_decode -- single-token paged decode attention.
+ * "KV cache fragmentation" (field guide), section "Definition" (the kernel
+ * walks the page table) and "Paged Attention and KV Cache Fragmentation",
+ * section "How PagedAttention maps an OS concept onto GPU memory" (a request
+ * sees its cache as one continuous sequence).  For every sequence b and
+ * query head h, with g = h / (num_q_heads / num_kv_heads) and
+ * n = seq_lens[b]:
+ *     K_b[t] = k_cache[block_tables[b][t / block_size]][g][t % block_size]
+ *     s_t    = scale * <q[b][h], K_b[t]>,           0 <= t < n
+ *     out[b][h] = sum_t softmax(s)_t * V_b[t]       (bf16 result)
+ * with fp32 accumulation throughout.  FP8 caches dequantise as
+ * decode(code) * k_scale[block][g] (likewise V).  A sequence with n == 0
+ * yields zeros.  Long contexts are split over up to `num_splits` persistent
+ * work partitions (0 = automatic) whose partial results are merged with a
+ * log-sum-exp reduction; the split points depend only on seq_lens, so the
+ * result does not depend on which physical blocks the tables name.
+ *   q            device bf16 [num_seqs][num_q_heads][head_dim]
+ *   k_cache, v_cache device pools of kv_dtype; num_blocks = pool blocks
+ *   k_scale, v_scale device float [num_blocks][num_kv_heads] (FP8) or NULL
+ *   block_tables device int32 [num_seqs][max_blocks_per_seq]
+ *   seq_lens     device int32 [num_seqs]
+ *   out          device bf16 [num_seqs][num_q_heads][head_dim]
+ *   workspace    device buffer of >= pa_decode_workspace_size() bytes
+ *                (contents need no initialisation; may be NULL if the size
+ *                is 0)
+ * Supported: head_dim in {64, 128}; 1 <= num_q_heads / num_kv_heads <= 8;
+ * block_size a power of two in [8, 256].  Table entries outside the pool
+ * read as zeros and flag PA_DEVERR_BAD_BLOCK_ID; seq_lens outside
+ * [0, max_blocks_per_seq * block_size] are clamped and flag
+ * PA_DEVERR_BAD_SEQ_LEN. */
+pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale,
+                    pa_kv_dtype kv_dtype, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                    int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale,
+                    void* out, void* workspace, size_t workspace_bytes,
+                    int32_t num_splits, void* stream);
+
+/* ------------------------------------------------------- block manager
+ * Host-only block allocator ("Paged Attention and KV Cache Fragmentation",
+ * section "How PagedAttention maps an OS concept onto GPU memory"; shared
+ * prefixes and forks: "KV cache fragmentation", section "Why it matters").
+ * A LIFO free list (a fresh allocator hands out 0, 1, 2, ...) and one
+ * refcount per block.  Every call is all-or-nothing: on any error no state
+ * changes.  No device memory is touched.  The handle is not thread-safe. */
+typedef struct pa_allocator pa_allocator;
+
+/* Create an allocator over blocks [0, num_blocks); *out receives it. */
+pa_status pa_allocator_create(int32_t num_blocks, pa_allocator** out);
+/* Destroy an allocator (NULL is a no-op). */
+void pa_allocator_destroy(pa_allocator* a);
+/* Pop n blocks (refcount 1 each) into ids_out[0..n); OUT_OF_BLOCKS if fewer
+ * than n are free. */
+pa_status pa_block_alloc(pa_allocator* a, int32_t n, int32_t* ids_out);
+/* Drop one reference per listed id (ids may repeat); blocks reaching zero
+ * are pushed on the free list in list order.  BAD_BLOCK_ID if an id is
+ * outside the pool or listed more often than it is referenced. */
+pa_status pa_block_free(pa_allocator* a, const int32_t* ids, int32_t n);
+/* Add one reference per listed id (a forked sequence shares the blocks).
+ * BAD_BLOCK_ID if an id is outside the pool or free. */
+pa_status pa_block_fork(pa_allocator* a, const int32_t* ids, int32_t n);
+/* Current refcount of one block. */
+pa_status pa_block_refcount(const pa_allocator* a, int32_t id, int32_t* rc);
+/* Number of free blocks (-1 for a NULL handle). */
+int32_t pa_block_num_free(const pa_allocator* a);
+
+/* pa_seq_append_slots -- grow one sequence from `len` to `len + n` tokens.
+ * table (host int32 [max_blocks]) holds the sequence's block ids; entries
+ * [0, ceil(len / block_size)) must be live.  If the last held block is
+ * partially filled and shared (refcount > 1), it is first replaced by a
+ * fresh block and one copy request (src, dst, len % block_size) is written
+ * to cow_pair_out[0..3) with *num_cow = 1 (else *num_cow = 0); the caller
+ * runs pa_copy_blocks on it before writing the new tokens.  Then a block is
+ * allocated for every block boundary the new tokens cross, and
+ * slots_out[i] = table[p / block_size] * block_size + p % block_size for
+ * p = len + i.  INVALID_ARG if ceil((len + n) / block_size) > max_blocks;
+ * OUT_OF_BLOCKS if the free list cannot cover the copy and the growth. */
+pa_status pa_seq_append_slots(pa_allocator* a, int32_t* table,
+                              int32_t max_blocks, int32_t len, int32_t n,
+                              int32_t block_size, int64_t* slots_out,
+                              int32_t* cow_pair_out, int32_t* num_cow);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

@@ -49,7 +49,21 @@ def quantize_blocks(cache_f32: np.ndarray, block_ids, valid_lens):
     nb, hkv, bs, d = cache_f32.shape
     codes = np.zeros((nb, hkv, bs, d), dtype=np.uint8)
     scales = np.ones((nb, hkv), dtype=np.float32)
+    block_ids = np.asarray(block_ids, dtype=np.int64)
+    valid_lens = np.asarray(valid_lens, dtype=np.int64)
+    # Whole blocks: the same arithmetic as quantize_tile, batched over
+    # blocks and heads (one absmax per (block, head), one divide per value).
+    full = block_ids[valid_lens == bs]
+    if full.size:
+        x = np.asarray(cache_f32[full], dtype=np.float32)
+        a = np.max(np.abs(x), axis=(2, 3)).astype(np.float32)
+        s = np.where(a == 0, np.float32(1.0),
+                     a / np.float32(e4m3.E4M3_MAX)).astype(np.float32)
+        codes[full] = e4m3.encode_fast((x / s[:, :, None, None]).astype(np.float32))
+        scales[full] = s
     for blk, valid in zip(block_ids, valid_lens):
+        if valid == bs:
+            continue
         for h in range(hkv):
             c, s = quantize_tile(cache_f32[blk, h], int(valid))
             codes[blk, h] = c

@@ -1,0 +1,152 @@
+// Cache maintenance kernels: scatter append, copy-on-write block copy and
+// per-(block, head) FP8 quantisation.  All are bandwidth-trivial next to the
+// decode step (they touch only the new tokens, the copied blocks or the
+// quantised blocks) and are written as plain 16-byte vectorised copies.
+#pragma once
+
+#include "pa_device.cuh"
+
+namespace pa {
+
+// --------------------------------------------------------- cache write ---
+// "Paged Attention and KV Cache Fragmentation", section "How PagedAttention
+// maps an OS concept onto GPU memory": each new token's K/V goes to the
+// slot its block table names.  One thread per 16-byte chunk; consecutive
+// threads cover one (token, head) row, K rows then V rows.
+__global__ void __launch_bounds__(256)
+    cache_write_kernel(const uint4* __restrict__ k_new,
+                       const uint4* __restrict__ v_new,
+                       const int64_t* __restrict__ slots, int32_t num_tokens,
+                       uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       int64_t num_slots, int32_t num_kv_heads,
+                       int32_t block_size, int32_t chunks_per_row) {
+  const int64_t per_token = 2LL * num_kv_heads * chunks_per_row;
+  const int64_t total = per_token * num_tokens;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+       i < total; i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t t = i / per_token;
+    int64_t r = i - t * per_token;
+    const int kv = static_cast<int>(r / (static_cast<int64_t>(num_kv_heads) * chunks_per_row));
+    r -= static_cast<int64_t>(kv) * num_kv_heads * chunks_per_row;
+    const int32_t h = static_cast<int32_t>(r / chunks_per_row);
+    const int32_t c = static_cast<int32_t>(r - static_cast<int64_t>(h) * chunks_per_row);
+    const int64_t s = slots[t];
+    if (s < 0) continue;
+    if (s >= num_slots) {
+      if (kv == 0 && h == 0 && c == 0) flag_error(PA_DEVERR_BAD_SLOT);
+      continue;
+    }
+    const int64_t blk = s / block_size, off = s - blk * block_size;
+    const int64_t src = (t * num_kv_heads + h) * chunks_per_row + c;
+    const int64_t dst = ((blk * num_kv_heads + h) * block_size + off) * chunks_per_row + c;
+    if (kv == 0)
+      k_cache[dst] = k_new[src];
+    else
+      v_cache[dst] = v_new[src];
+  }
+}
+
+// ---------------------------------------------------------- block copy ---
+// Copy-on-write of a shared partial block (same page, the shared-prefix
+// paragraph): grid (pairs, heads, K/V); each CTA copies the first n rows of
+// one head of one block.
+__global__ void __launch_bounds__(256)
+    copy_blocks_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                       float* __restrict__ k_scale, float* __restrict__ v_scale,
+                       const int32_t* __restrict__ pairs, int32_t num_blocks,
+                       int32_t num_kv_heads, int32_t block_size,
+                       int32_t chunks_per_row) {
+  const int32_t pr = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
+  const int32_t src = pairs[3 * pr], dst = pairs[3 * pr + 1], n = pairs[3 * pr + 2];
+  if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || n < 0 ||
+      n > block_size) {
+    if (threadIdx.x == 0 && h == 0 && kv == 0) flag_error(PA_DEVERR_BAD_PAIR);
+    return;
+  }
+  uint4* cache = kv == 0 ? k_cache : v_cache;
+  const int64_t row = static_cast<int64_t>(block_size) * chunks_per_row;
+  const uint4* s = cache + (static_cast<int64_t>(src) * num_kv_heads + h) * row;
+  uint4* d = cache + (static_cast<int64_t>(dst) * num_kv_heads + h) * row;
+  const int32_t cnt = n * chunks_per_row;
+  for (int32_t i = threadIdx.x; i < cnt; i += blockDim.x) d[i] = s[i];
+  float* sc = kv == 0 ? k_scale : v_scale;
+  if (sc != nullptr && threadIdx.x == 0)
+    sc[static_cast<int64_t>(dst) * num_kv_heads + h] =
+        sc[static_cast<int64_t>(src) * num_kv_heads + h];
+}
+
+// ------------------------------------------------------- FP8 quantise ---
+// "Paged Attention and KV Cache Fragmentation", section "Quantization as a
+// way to stretch paged memory further".  One CTA per (listed block, head,
+// K/V): absmax over the valid rows, scale = absmax / 448 (IEEE division),
+// codes = e4m3_rne_satfinite(x / scale) (IEEE division per element), rows
+// past the valid length written as +0.
+__global__ void __launch_bounds__(256)
+    quantize_fp8_kernel(const uint4* __restrict__ k_src,
+                        const uint4* __restrict__ v_src,
+                        const int32_t* __restrict__ block_ids,
+                        const int32_t* __restrict__ valid_lens,
+                        uint2* __restrict__ k_dst, uint2* __restrict__ v_dst,
+                        float* __restrict__ k_scale, float* __restrict__ v_scale,
+                        int32_t num_blocks, int32_t num_kv_heads,
+                        int32_t block_size, int32_t head_dim) {
+  const int32_t i = blockIdx.x, h = blockIdx.y, kv = blockIdx.z;
+  const int32_t blk = block_ids[i], n = valid_lens[i];
+  if (blk < 0 || blk >= num_blocks || n < 0 || n > block_size) {
+    if (threadIdx.x == 0 && h == 0 && kv == 0) flag_error(PA_DEVERR_BAD_BLOCK_ID);
+    return;
+  }
+  const int32_t vec_per_row = head_dim / 8;  // 8 elements per 16 bytes
+  const int64_t tile = (static_cast<int64_t>(blk) * num_kv_heads + h) *
+                       static_cast<int64_t>(block_size) * vec_per_row;
+  const uint4* src = (kv == 0 ? k_src : v_src) + tile;
+  uint2* dst = (kv == 0 ? k_dst : v_dst) + tile;
+  const int32_t nvec = block_size * vec_per_row;
+  const int32_t nvalid = n * vec_per_row;
+
+  float amax = 0.f;
+  for (int32_t j = threadIdx.x; j < nvalid; j += blockDim.x) {
+    const uint4 w = src[j];
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 f = unpack_bf16x2(ws[q]);
+      amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  __shared__ float red[8];
+  __shared__ float s_scale;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = amax;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float a = 0.f;
+    for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) a = fmaxf(a, red[w]);
+    const float scale = a == 0.f ? 1.f : __fdiv_rn(a, 448.f);
+    s_scale = scale;
+    (kv == 0 ? k_scale : v_scale)[static_cast<int64_t>(blk) * num_kv_heads + h] = scale;
+  }
+  __syncthreads();
+  const float scale = s_scale;
+  for (int32_t j = threadIdx.x; j < nvec; j += blockDim.x) {
+    uint2 out = make_uint2(0u, 0u);
+    if (j < nvalid) {
+      const uint4 w = src[j];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+      uint32_t codes[2] = {0u, 0u};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float2 f = unpack_bf16x2(ws[q]);
+        const uint32_t c0 = __nv_cvt_float_to_fp8(__fdiv_rn(f.x, scale), __NV_SATFINITE, __NV_E4M3);
+        const uint32_t c1 = __nv_cvt_float_to_fp8(__fdiv_rn(f.y, scale), __NV_SATFINITE, __NV_E4M3);
+        codes[q >> 1] |= (c0 | (c1 << 8)) << ((q & 1) * 16);
+      }
+      out = make_uint2(codes[0], codes[1]);
+    }
+    dst[j] = out;
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,420 @@
+// libpa: C ABI entry points (declared in include/pa.h).  Host-side argument
+// validation, TMA descriptor encoding and kernel launches; the kernels live
+// in decode.cuh and cache_ops.cuh, the host block manager in
+// block_manager.cpp.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <climits>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "cache_ops.cuh"
+#include "decode.cuh"
+#include "pa.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+inline bool aligned16(const void* p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+inline bool pow2_in(int32_t x, int32_t lo, int32_t hi) {
+  return x >= lo && x <= hi && (x & (x - 1)) == 0;
+}
+
+inline int ilog2(int32_t x) {
+  int l = 0;
+  while ((1 << l) < x) ++l;
+  return l;
+}
+
+struct DeviceInfo {
+  bool init = false;
+  int sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mu;
+
+pa_status device_sms(int* sms, int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_dev[dev].init) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    g_dev[dev].sms = n;
+    g_dev[dev].init = true;
+  }
+  *sms = g_dev[dev].sms;
+  if (dev_out) *dev_out = dev;
+  return PA_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// dependency on libcuda).
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// 2D map over a row-major [rows][inner] array; box = [box_inner, box_rows].
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
+               uint64_t inner, uint64_t rows, uint64_t row_bytes,
+               uint32_t box_inner, uint32_t box_rows, CUtensorMapSwizzle sw) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Decode launch plan for one (head_dim, dtype) instantiation.
+constexpr int kTargetCtasPerSm = 6;
+constexpr size_t kSmemPerSm = 228 * 1024;
+constexpr size_t kSmemReservedPerCta = 1024;
+
+template <int D, bool FP8>
+struct Plan {
+  using L = Smem<D, FP8>;
+  static int stages() {
+    const size_t per_cta = kSmemPerSm / kTargetCtasPerSm - kSmemReservedPerCta;
+    const size_t fixed = L::kHeaderBytes + 2 * L::kQBytes;
+    int s = static_cast<int>((per_cta - fixed) / L::kStageBytes);
+    if (s < 2) s = 2;
+    if (s > L::kMaxStages) s = L::kMaxStages;
+    return s;
+  }
+  static size_t smem_bytes(int s) {
+    return L::kHeaderBytes + 2 * L::kQBytes + static_cast<size_t>(s) * L::kStageBytes;
+  }
+};
+
+template <int D, bool FP8>
+pa_status decode_ctas_per_sm(int dev, int stages, int* out) {
+  static int cached[kMaxDevices] = {0};
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (cached[dev] == 0) {
+    const size_t smem = Plan<D, FP8>::smem_bytes(stages);
+    if (cudaFuncSetAttribute(paged_decode_kernel<D, FP8>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &n, paged_decode_kernel<D, FP8>, 64, smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (n < 1) return PA_ERR_UNSUPPORTED;
+    cached[dev] = n;
+  }
+  *out = cached[dev];
+  return PA_OK;
+}
+
+size_t workspace_bytes_for(int64_t pieces, int32_t head_dim) {
+  return static_cast<size_t>(pieces) * kMaxG *
+         (static_cast<size_t>(head_dim) * sizeof(float) + sizeof(float2));
+}
+
+template <int D, bool FP8>
+pa_status launch_decode(const DecodeParams& prm_in, const void* q,
+                        const void* k_cache, const void* v_cache,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t num_splits, cudaStream_t stream) {
+  using L = Smem<D, FP8>;
+  int sms = 0, dev = 0;
+  pa_status st = device_sms(&sms, &dev);
+  if (st != PA_OK) return st;
+  const int stages = Plan<D, FP8>::stages();
+  int per_sm = 0;
+  st = decode_ctas_per_sm<D, FP8>(dev, stages, &per_sm);
+  if (st != PA_OK) return st;
+  const int32_t P = num_splits > 0 ? num_splits : sms * per_sm;
+  const int64_t segs = static_cast<int64_t>(prm_in.num_seqs) * prm_in.num_kv_heads;
+  const size_t need = P > 1 ? workspace_bytes_for(P + segs, D) : 0;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+
+  DecodeParams prm = prm_in;
+  prm.num_ctas = P;
+  prm.stages = stages;
+  if (need > 0) {
+    const int64_t pieces = P + segs;
+    prm.ws_o = static_cast<float*>(workspace);
+    prm.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                          static_cast<size_t>(pieces) * kMaxG * D * sizeof(float));
+  } else {
+    prm.ws_o = nullptr;
+    prm.ws_ml = nullptr;
+  }
+
+  CUtensorMap tq, tk, tv;
+  const uint64_t qrows = static_cast<uint64_t>(prm.num_seqs) * prm.num_q_heads;
+  if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, D, qrows, D * 2, 64, 8,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return PA_ERR_CUDA;
+  const uint32_t box_rows = prm.block_size < kTile ? prm.block_size : kTile;
+  const uint64_t rows = static_cast<uint64_t>(prm.rows_total);
+  if (FP8) {
+    const CUtensorMapSwizzle sw = D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (!encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_cache, D, rows, D, D, box_rows, sw) ||
+        !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_cache, D, rows, D, D, box_rows, sw))
+      return PA_ERR_CUDA;
+  } else {
+    if (!encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, D, rows, D * 2, 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, D, rows, D * 2, 64, box_rows,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return PA_ERR_CUDA;
+  }
+  const size_t smem = Plan<D, FP8>::smem_bytes(stages);
+  (void)L::kStageBytes;
+  paged_decode_kernel<D, FP8><<<P, 64, smem, stream>>>(tq, tk, tv, prm);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (segs > 0) {
+    paged_decode_merge_kernel<D><<<static_cast<unsigned>(segs), 256, 0, stream>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int32_t pa_abi_version(void) { return 1; }
+
+extern "C" const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_OUT_OF_BLOCKS: return "PA_ERR_OUT_OF_BLOCKS";
+    case PA_ERR_BAD_BLOCK_ID: return "PA_ERR_BAD_BLOCK_ID";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+extern "C" pa_status pa_get_device_error(uint32_t* err) {
+  if (err == nullptr) return PA_ERR_INVALID_ARG;
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero)) != cudaSuccess) return PA_ERR_CUDA;
+  *err = v;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_cache_write(const void* k_new, const void* v_new,
+                                    const int64_t* slot_mapping, int32_t num_tokens,
+                                    void* k_cache, void* v_cache, int32_t num_blocks,
+                                    int32_t num_kv_heads, int32_t block_size,
+                                    int32_t head_dim, pa_kv_dtype kv_dtype, void* stream) {
+  if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 ||
+      head_dim <= 0 || head_dim % 8 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (kv_dtype == PA_KV_FP8_E4M3) return PA_ERR_UNSUPPORTED;
+  if (kv_dtype != PA_KV_BF16) return PA_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_INVALID_ARG;
+  int sms = 0;
+  pa_status st = device_sms(&sms, nullptr);
+  if (st != PA_OK) return st;
+  const int32_t cpr = head_dim / 8;
+  const int64_t total = 2LL * num_tokens * num_kv_heads * cpr;
+  int64_t grid = (total + 255) / 256;
+  if (grid > static_cast<int64_t>(sms) * 16) grid = static_cast<int64_t>(sms) * 16;
+  cache_write_kernel<<<static_cast<unsigned>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
+      num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      static_cast<int64_t>(num_blocks) * block_size, num_kv_heads, block_size, cpr);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale,
+                                    float* v_scale, const int32_t* pairs, int32_t num_pairs,
+                                    int32_t num_blocks, int32_t num_kv_heads,
+                                    int32_t block_size, int32_t head_dim,
+                                    pa_kv_dtype kv_dtype, void* stream) {
+  if (num_pairs < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  int esz;
+  if (kv_dtype == PA_KV_BF16) {
+    esz = 2;
+  } else if (kv_dtype == PA_KV_FP8_E4M3) {
+    esz = 1;
+    if (num_pairs > 0 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  } else {
+    return PA_ERR_INVALID_ARG;
+  }
+  if ((head_dim * esz) % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (num_pairs == 0) return PA_OK;
+  if (!k_cache || !v_cache || !pairs || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(num_pairs), static_cast<unsigned>(num_kv_heads), 2);
+  copy_blocks_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+      kv_dtype == PA_KV_FP8_E4M3 ? k_scale : nullptr,
+      kv_dtype == PA_KV_FP8_E4M3 ? v_scale : nullptr, pairs, num_blocks, num_kv_heads,
+      block_size, head_dim * esz / 16);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_quantize_fp8(const void* k_src, const void* v_src,
+                                     const int32_t* block_ids, const int32_t* valid_lens,
+                                     int32_t num_ids, uint8_t* k_dst, uint8_t* v_dst,
+                                     float* k_scale, float* v_scale, int32_t num_blocks,
+                                     int32_t num_kv_heads, int32_t block_size,
+                                     int32_t head_dim, void* stream) {
+  if (num_ids < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 ||
+      head_dim <= 0 || head_dim % 16 != 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_ids == 0) return PA_OK;
+  if (!k_src || !v_src || !block_ids || !valid_lens || !k_dst || !v_dst || !k_scale || !v_scale)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_src) || !aligned16(v_src) || !aligned16(k_dst) || !aligned16(v_dst))
+    return PA_ERR_INVALID_ARG;
+  if (num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+  dim3 grid(static_cast<unsigned>(num_ids), static_cast<unsigned>(num_kv_heads), 2);
+  quantize_fp8_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_src), static_cast<const uint4*>(v_src), block_ids,
+      valid_lens, reinterpret_cast<uint2*>(k_dst), reinterpret_cast<uint2*>(v_dst), k_scale,
+      v_scale, num_blocks, num_kv_heads, block_size, head_dim);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+namespace {
+
+pa_status auto_ctas(int32_t head_dim, pa_kv_dtype dt, int32_t* out) {
+  int sms = 0, dev = 0;
+  pa_status st = device_sms(&sms, &dev);
+  if (st != PA_OK) return st;
+  int per = 0;
+  if (dt == PA_KV_BF16 && head_dim == 128)
+    st = decode_ctas_per_sm<128, false>(dev, Plan<128, false>::stages(), &per);
+  else if (dt == PA_KV_BF16 && head_dim == 64)
+    st = decode_ctas_per_sm<64, false>(dev, Plan<64, false>::stages(), &per);
+  else if (dt == PA_KV_FP8_E4M3 && head_dim == 128)
+    st = decode_ctas_per_sm<128, true>(dev, Plan<128, true>::stages(), &per);
+  else if (dt == PA_KV_FP8_E4M3 && head_dim == 64)
+    st = decode_ctas_per_sm<64, true>(dev, Plan<64, true>::stages(), &per);
+  else
+    return PA_ERR_UNSUPPORTED;
+  if (st != PA_OK) return st;
+  *out = sms * per;
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                              int32_t num_kv_heads, int32_t head_dim,
+                                              int32_t num_splits, size_t* bytes) {
+  if (bytes == nullptr || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      num_splits < 0)
+    return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  int32_t P = num_splits;
+  if (P == 0) {
+    // The automatic partition count is the same for both cache dtypes'
+    // worst case; take the larger.
+    int32_t a = 0, b = 0;
+    pa_status st = auto_ctas(head_dim, PA_KV_BF16, &a);
+    if (st != PA_OK) return st;
+    st = auto_ctas(head_dim, PA_KV_FP8_E4M3, &b);
+    if (st != PA_OK) return st;
+    P = a > b ? a : b;
+  }
+  *bytes = P > 1 ? workspace_bytes_for(P + static_cast<int64_t>(num_seqs) * num_kv_heads,
+                                       head_dim)
+                 : 0;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               pa_kv_dtype kv_dtype, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t num_splits, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq < 0 || num_splits < 0 || !(scale == scale) ||
+      num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (kv_dtype != PA_KV_BF16 && kv_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (group > kMaxG) return PA_ERR_UNSUPPORTED;
+  if (!pow2_in(block_size, 8, 256)) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
+  const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
+  if (rows > INT_MAX - 64) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(num_seqs) * num_q_heads > INT_MAX - 64) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX - 64)
+    return PA_ERR_UNSUPPORTED;
+
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.block_size = block_size;
+  p.log2_bs = ilog2(block_size);
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.rows_total = static_cast<int32_t>(rows);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (kv_dtype == PA_KV_BF16) {
+    if (head_dim == 128)
+      return launch_decode<128, false>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+    return launch_decode<64, false>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+  }
+  if (head_dim == 128)
+    return launch_decode<128, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+  return launch_decode<64, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+}

@@ -1,0 +1,291 @@
+"""Python binding of libpa (argument marshalling only).
+
+Every function here forwards to the C ABI declared in ``include/pa.h`` under
+the same name; torch tensors are used only as device (or host) memory and
+their current CUDA stream.  No computation of the method happens in Python:
+if ``libpa.so`` is missing, importing the functions raises instead of
+falling back to anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa.so")
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_OUT_OF_BLOCKS, PA_ERR_BAD_BLOCK_ID = 0, 1, 2, 3
+PA_ERR_CUDA, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE = 4, 5, 6
+PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+
+DEVERR_BAD_BLOCK_ID, DEVERR_BAD_SEQ_LEN, DEVERR_BAD_SLOT = 0x1, 0x2, 0x4
+DEVERR_BAD_PAIR, DEVERR_TIMEOUT, DEVERR_LAUNCH = 0x8, 0x10, 0x20
+
+_lib = None
+
+_c_int = ctypes.c_int32
+_c_ptr = ctypes.c_void_p
+_c_size = ctypes.c_size_t
+
+# name -> (restype, argtypes); must match include/pa.h
+SIGNATURES = {
+    "pa_abi_version": (_c_int, []),
+    "pa_status_string": (ctypes.c_char_p, [_c_int]),
+    "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_uint32)]),
+    "pa_cache_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
+                                _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_copy_blocks": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int,
+                                _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_quantize_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                                 _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_decode_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                          ctypes.POINTER(_c_size)]),
+    "pa_decode": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
+                           _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                           ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int, _c_ptr]),
+    "pa_allocator_create": (_c_int, [_c_int, ctypes.POINTER(_c_ptr)]),
+    "pa_allocator_destroy": (None, [_c_ptr]),
+    "pa_block_alloc": (_c_int, [_c_ptr, _c_int, _c_ptr]),
+    "pa_block_free": (_c_int, [_c_ptr, _c_ptr, _c_int]),
+    "pa_block_fork": (_c_int, [_c_ptr, _c_ptr, _c_int]),
+    "pa_block_refcount": (_c_int, [_c_ptr, _c_int, ctypes.POINTER(_c_int)]),
+    "pa_block_num_free": (_c_int, [_c_ptr]),
+    "pa_seq_append_slots": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
+                                     _c_ptr, _c_ptr, ctypes.POINTER(_c_int)]),
+}
+
+
+class PAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpa; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m paged_kv_cache_228_gb300.build` (there is no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(status).decode()
+
+
+def _check(fn: str, status: int):
+    if status != PA_OK:
+        raise PAError(fn, status)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, dtype, name, ndim=None):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {ndim} dims, got {t.dim()}")
+
+
+def _kv_dtype(cache):
+    if cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if cache.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return PA_KV_FP8_E4M3
+    raise TypeError(f"unsupported cache dtype {cache.dtype}")
+
+
+# ------------------------------------------------------------------ misc ---
+def pa_abi_version() -> int:
+    return int(lib().pa_abi_version())
+
+
+def pa_get_device_error() -> int:
+    v = ctypes.c_uint32(0)
+    _check("pa_get_device_error", lib().pa_get_device_error(ctypes.byref(v)))
+    return int(v.value)
+
+
+# ----------------------------------------------------------------- cache ---
+def pa_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
+    """Scatter k_new/v_new [T, Hkv, d] into the pools at slot_mapping[T]."""
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    nb, hkv, bs, d = k_cache.shape
+    _need(k_new, k_cache.dtype, "k_new", 3)
+    _need(v_new, k_cache.dtype, "v_new", 3)
+    _check("pa_cache_write", lib().pa_cache_write(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache),
+        _ptr(v_cache), nb, hkv, bs, d, _kv_dtype(k_cache), _stream(stream)))
+
+
+def pa_copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):
+    """Copy-on-write: pairs int32 [P, 3] rows (src, dst, valid slots)."""
+    _need(pairs, torch.int32, "pairs", 2)
+    nb, hkv, bs, d = k_cache.shape
+    _check("pa_copy_blocks", lib().pa_copy_blocks(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(pairs),
+        pairs.shape[0], nb, hkv, bs, d, _kv_dtype(k_cache), _stream(stream)))
+
+
+def pa_quantize_fp8(k_src, v_src, block_ids, valid_lens, k_dst, v_dst, k_scale,
+                    v_scale, stream=None):
+    """Quantise listed bf16 blocks to E4M3 with per-(block, head) scales."""
+    _need(block_ids, torch.int32, "block_ids", 1)
+    _need(valid_lens, torch.int32, "valid_lens", 1)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    nb, hkv, bs, d = k_src.shape
+    _check("pa_quantize_fp8", lib().pa_quantize_fp8(
+        _ptr(k_src), _ptr(v_src), _ptr(block_ids), _ptr(valid_lens), block_ids.shape[0],
+        _ptr(k_dst), _ptr(v_dst), _ptr(k_scale), _ptr(v_scale), nb, hkv, bs, d,
+        _stream(stream)))
+
+
+# ---------------------------------------------------------------- decode ---
+def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                             num_splits=0) -> int:
+    n = ctypes.c_size_t(0)
+    _check("pa_decode_workspace_size", lib().pa_decode_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, num_splits, ctypes.byref(n)))
+    return int(n.value)
+
+
+def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out, workspace=None,
+              k_scale=None, v_scale=None, num_splits=0, stream=None):
+    """Paged decode attention: out[B, Hq, d] (bf16) from q[B, Hq, d] (bf16)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode", lib().pa_decode(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _kv_dtype(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+        hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits,
+        _stream(stream)))
+
+
+# --------------------------------------------------------- block manager ---
+class Allocator:
+    """Handle over the native host block manager (pa_allocator)."""
+
+    def __init__(self, num_blocks: int):
+        h = ctypes.c_void_p()
+        _check("pa_allocator_create", lib().pa_allocator_create(num_blocks, ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+
+    def close(self):
+        if self._h:
+            lib().pa_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def _ids(ids):
+        arr = (ctypes.c_int32 * max(1, len(ids)))(*ids)
+        return arr, len(ids)
+
+    def alloc(self, n: int):
+        """(status, ids or None)."""
+        buf = (ctypes.c_int32 * max(1, n))()
+        st = lib().pa_block_alloc(self._h, n, buf)
+        return st, (list(buf[:n]) if st == PA_OK else None)
+
+    def free(self, ids) -> int:
+        arr, n = self._ids(ids)
+        return lib().pa_block_free(self._h, arr, n)
+
+    def fork(self, ids) -> int:
+        arr, n = self._ids(ids)
+        return lib().pa_block_fork(self._h, arr, n)
+
+    def refcount(self, bid: int):
+        rc = ctypes.c_int32(0)
+        st = lib().pa_block_refcount(self._h, bid, ctypes.byref(rc))
+        return st, (rc.value if st == PA_OK else None)
+
+    def num_free(self) -> int:
+        return int(lib().pa_block_num_free(self._h))
+
+    def append_slots(self, table: list, length: int, n: int, block_size: int,
+                     max_blocks: int):
+        """Grow a sequence; ``table`` (list) is updated in place on success.
+
+        Returns (status, slots, cow_pairs) like the C call.
+        """
+        tab = (ctypes.c_int32 * max(1, max_blocks))(*([-1] * max(1, max_blocks)))
+        for i, b in enumerate(table[:max_blocks]):
+            tab[i] = b
+        slots = (ctypes.c_int64 * max(1, n))()
+        cow = (ctypes.c_int32 * 3)()
+        ncow = ctypes.c_int32(0)
+        st = lib().pa_seq_append_slots(self._h, tab, max_blocks, length, n, block_size,
+                                       slots, cow, ctypes.byref(ncow))
+        if st != PA_OK:
+            return st, None, None
+        want = -(-(length + n) // block_size)
+        table[:] = list(tab[:want])
+        pairs = [tuple(cow[:3])] if ncow.value else []
+        return st, list(slots[:n]), pairs
+
+
+def replay_script(ops, num_seqs: int, block_size: int, max_blocks: int, num_blocks: int):
+    """Apply a workload op script to a fresh native allocator.
+
+    Returns (allocator, tables, lens); raises on any non-OK status.
+    """
+    a = Allocator(num_blocks)
+    tables = [[] for _ in range(num_seqs)]
+    lens = [0] * num_seqs
+    for op in ops:
+        kind = op[0]
+        if kind == "alloc":
+            st, _ = a.alloc(op[1])
+            _check("pa_block_alloc", st)
+        elif kind == "free_list":
+            _check("pa_block_free", a.free(op[1]))
+        elif kind == "append":
+            _, b, n = op
+            st, _, _ = a.append_slots(tables[b], lens[b], n, block_size, max_blocks)
+            _check("pa_seq_append_slots", st)
+            lens[b] += n
+        elif kind == "fork":
+            _, child, parent, ntok = op
+            ids = tables[parent][:-(-ntok // block_size)]
+            _check("pa_block_fork", a.fork(ids))
+            tables[child] = list(ids)
+            lens[child] = ntok
+        else:
+            raise ValueError(kind)
+    return a, tables, lens

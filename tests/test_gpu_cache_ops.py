@@ -1,0 +1,142 @@
+"""GPU parity of the cache kernels against the oracle, bit for bit.
+
+* pa_cache_write: every config's append step, plus random distinct slots
+  with skipped (negative) slots, for bs in {8, 16, 32} and d in {64, 128};
+* pa_copy_blocks: copy-on-write pairs from a real fork, bf16 and FP8 (with
+  scales);
+* pa_quantize_fp8: codes and scales equal the oracle's quantiser (its own
+  E4M3 encoder), including outlier-heavy and partially valid blocks; a
+  cross-check of a sample of codes against torch's float8_e4m3fn cast.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import paged_attention as OPA
+from oracle import quantize as OQ
+from paged_kv_cache_228_gb300 import pa
+from paged_kv_cache_228_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_cache_228_gb300 import build
+    build.build()
+    pa.pa_get_device_error()  # clear
+
+
+def _bits(t):
+    return t.detach().cpu().view(torch.int16 if t.element_size() == 2 else torch.uint8).numpy()
+
+
+@pytest.mark.parametrize("bs,d,nb,H,T", [(16, 64, 32, 2, 4), (8, 128, 64, 8, 37),
+                                         (32, 128, 40, 8, 128), (16, 128, 300, 8, 256)])
+def test_cache_write_bit_exact(bs, d, nb, H, T):
+    dev = "cuda"
+    kc = W.normal_bf16((nb, H, bs, d), 11, dev)
+    vc = W.normal_bf16((nb, H, bs, d), 12, dev)
+    kn = W.normal_bf16((T, H, d), 13, dev)
+    vn = W.normal_bf16((T, H, d), 14, dev)
+    slots = W.distinct_slots(nb * bs, T, 15)
+    slots[::5] = -1
+    ek, ev = OPA.cache_write(_bits(kn), _bits(vn), slots.numpy(), _bits(kc), _bits(vc))
+    pa.pa_cache_write(kn, vn, slots.to(dev), kc, vc)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(kc), ek)
+    assert np.array_equal(_bits(vc), ev)
+    assert pa.pa_get_device_error() == 0
+
+
+def test_cache_write_bad_slot_is_flagged_and_skipped():
+    dev = "cuda"
+    kc = torch.zeros((4, 2, 16, 64), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    kn = torch.ones((2, 2, 64), dtype=torch.bfloat16, device=dev)
+    slots = torch.tensor([3, 4 * 16 + 5], dtype=torch.int64, device=dev)
+    pa.pa_cache_write(kn, kn, slots, kc, vc)
+    assert pa.pa_get_device_error() & pa.DEVERR_BAD_SLOT
+    assert kc.sum().item() == 2 * 64  # only slot 3 written
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("fp8", [False, True])
+def test_copy_blocks_bit_exact(fp8):
+    dev = "cuda"
+    nb, H, bs, d = 24, 4, 16, 128
+    if fp8:
+        kc = torch.randint(0, 255, (nb, H, bs, d), dtype=torch.uint8, device=dev)
+        vc = torch.randint(0, 255, (nb, H, bs, d), dtype=torch.uint8, device=dev)
+        ks = torch.rand((nb, H), device=dev)
+        vs = torch.rand((nb, H), device=dev)
+    else:
+        kc = W.normal_bf16((nb, H, bs, d), 21, dev)
+        vc = W.normal_bf16((nb, H, bs, d), 22, dev)
+        ks = vs = None
+    # a real fork: parent of 2 * 16 + 5 tokens, three children append one token
+    a = pa.Allocator(nb)
+    parent = []
+    a.append_slots(parent, 0, 37, bs, 8)
+    pairs = []
+    for _ in range(3):
+        child = list(parent)
+        a.fork(child)
+        st, _, pr = a.append_slots(child, 37, 1, bs, 8)
+        pairs += pr
+    assert len(pairs) == 3 and all(p[2] == 5 for p in pairs)
+    ek, ev = OPA.copy_blocks(_bits(kc), _bits(vc), pairs)
+    pa.pa_copy_blocks(kc, vc, torch.tensor(pairs, dtype=torch.int32, device=dev), ks, vs)
+    torch.cuda.synchronize()
+    assert np.array_equal(_bits(kc), ek) and np.array_equal(_bits(vc), ev)
+    if fp8:
+        for s, dd, _ in pairs:
+            assert torch.equal(ks[dd], ks[s]) and torch.equal(vs[dd], vs[s])
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("bs,d", [(16, 128), (8, 64), (32, 128)])
+def test_quantize_fp8_bit_exact(bs, d):
+    dev = "cuda"
+    nb, H = 40, 4
+    k = W.normal_bf16((nb, H, bs, d), 31, dev, outlier_prob=0.01, outlier_scale=20.0)
+    v = W.normal_bf16((nb, H, bs, d), 32, dev, outlier_prob=0.01, outlier_scale=20.0)
+    k[3] = 0  # an all-zero block: scale 1
+    ids = [3, 7, 0, 39, 12, 5]
+    valid = [bs, bs, 1, bs // 2, bs - 1, 0]
+    kq = torch.full((nb, H, bs, d), 0xAB, dtype=torch.uint8, device=dev)
+    vq = torch.full_like(kq, 0xCD)
+    ks = torch.full((nb, H), -1.0, device=dev)
+    vs = torch.full((nb, H), -1.0, device=dev)
+    pa.pa_quantize_fp8(k, v, torch.tensor(ids, dtype=torch.int32, device=dev),
+                       torch.tensor(valid, dtype=torch.int32, device=dev), kq, vq, ks, vs)
+    torch.cuda.synchronize()
+    k32 = k.float().cpu().numpy()
+    v32 = v.float().cpu().numpy()
+    eq, es = OQ.quantize_blocks(k32, ids, valid)
+    fq, fs = OQ.quantize_blocks(v32, ids, valid)
+    for i in ids:
+        assert np.array_equal(kq[i].cpu().numpy(), eq[i]), i
+        assert np.array_equal(vq[i].cpu().numpy(), fq[i]), i
+        assert np.array_equal(ks[i].cpu().numpy(), es[i]), i
+        assert np.array_equal(vs[i].cpu().numpy(), fs[i]), i
+    # untouched blocks keep their contents
+    assert (kq[1] == 0xAB).all() and (ks[1] == -1).all()
+    assert pa.pa_get_device_error() == 0
+
+
+def test_quantize_codes_agree_with_torch_cast():
+    # Library cross-check of the GPU conversion (inside +-448 torch's cast
+    # is RNE like the kernel's satfinite conversion).
+    dev = "cuda"
+    k = W.normal_bf16((8, 2, 16, 128), 41, dev)
+    ids = torch.arange(8, dtype=torch.int32, device=dev)
+    valid = torch.full((8,), 16, dtype=torch.int32, device=dev)
+    kq = torch.empty((8, 2, 16, 128), dtype=torch.uint8, device=dev)
+    ks = torch.empty((8, 2), device=dev)
+    pa.pa_quantize_fp8(k, k, ids, valid, kq, kq.clone(), ks, ks.clone())
+    kc = k.float().cpu()
+    s = kc.abs().amax(dim=(2, 3)) / torch.tensor(448.0)  # fp32 IEEE on the CPU
+    x = kc / s[:, :, None, None]
+    ref = x.to(torch.float8_e4m3fn).view(torch.uint8)
+    assert torch.equal(ref, kq.cpu())

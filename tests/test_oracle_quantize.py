@@ -66,3 +66,16 @@ def test_quantize_blocks_layout():
     c10, s10 = QZ.quantize_tile(cache[1, 0], 3)
     assert np.array_equal(codes[1, 0], c10) and scales[1, 0] == s10
     assert not codes[0].any() and np.all(scales[0] == 1)
+
+
+def test_batched_whole_blocks_equal_per_tile_path():
+    g = np.random.default_rng(6)
+    cache = (g.standard_normal((9, 3, 16, 32)) * np.where(
+        g.random((9, 3, 16, 32)) < 0.01, 20, 1)).astype(np.float32)
+    cache[4, 1] = 0
+    ids = [0, 4, 8, 2]
+    codes, scales = QZ.quantize_blocks(cache, ids, [16] * 4)
+    for b in ids:
+        for h in range(3):
+            c, s = QZ.quantize_tile(cache[b, h], 16)
+            assert np.array_equal(codes[b, h], c) and scales[b, h] == s
