@@ -181,7 +181,8 @@ def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
 
 
 # ----------------------------------------------------------- native arm ---
-def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None):
+def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None,
+               profile_only=False):
     from paged_kv_cache_228_gb300 import pa
     from paged_kv_cache_228_gb300 import workloads as W
     per_pool = w.pool_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
@@ -254,6 +255,8 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     err = pa.pa_get_device_error()
     if err:
         raise RuntimeError(f"device error word 0x{err:x} during the benchmark")
+    if profile_only:
+        return {"ms_per_step": total_ms / steps, "decode_ms_mean": statistics.mean(dec_ms)}
 
     # CUDA-graph replay of one step per pool (launch overhead amortised)
     graph_ms = None
@@ -409,6 +412,11 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--fp8", action="store_true",
+                    help="with --profile: run the FP8 cache path of the workload")
+    ap.add_argument("--profile", action="store_true",
+                    help="only the warm-up and timed steps of the main workload "
+                         "(for ncu captures); prints the step time")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -439,6 +447,13 @@ def main():
             gpu_index = int(vis.split(",")[local])
         except ValueError:
             pass
+    if args.profile:
+        r = run_native(w, args.steps, args.warmup, device, fp8=args.fp8,
+                       n_pools=1 if w.num_seqs * max(w.seq_lens) > 10 ** 6 else None,
+                       profile_only=True)
+        print(json.dumps({"workload": w.name, "ms_per_step": r["ms_per_step"],
+                          "decode_ms_mean": r["decode_ms_mean"]}))
+        return
     res = run_native(w, args.steps, args.warmup, device,
                      sample_clocks=(lambda: ClockSampler(gpu_index)) if rank == 0 else None)
     nbytes = kv_bytes(w)
