@@ -198,6 +198,42 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     void* out, void* workspace, size_t workspace_bytes,
                     int32_t num_splits, void* stream);
 
+/* pa_decode_noalloc -- pa_decode for callers that cannot allocate.
+ * The pages have no counterpart: this is a library-only convenience.
+ * Some callers cannot call cudaMalloc or otherwise obtain device memory:
+ * plugin hosts that forbid allocation inside their execute callback and
+ * provide no workspace, services that fix their whole device-memory budget
+ * at start-up, and thin foreign-function callers with no device allocator.
+ * This entry point takes the same arguments as pa_decode minus the
+ * workspace pointer and size, and uses instead a
+ * library-owned device array of PA_NOALLOC_SCRATCH_BYTES (16 MiB) that every
+ * GPU which loads the library holds until the process exits.
+ *   - It allocates nothing: no cudaMalloc, cudaFree or allocating library
+ *     routine is called.
+ *   - The first call on each device looks up that device's address of the
+ *     array (with the device current); make that first call before any
+ *     stream capture on the device.
+ *   - Requests whose workspace (pa_decode_workspace_size with the same
+ *     num_splits) exceeds PA_NOALLOC_SCRATCH_BYTES are rejected with
+ *     PA_ERR_WORKSPACE and nothing is enqueued.
+ *   - All calls on a device share the one array, which keeps whatever the
+ *     last call left in it.  Nothing in it needs to start at zero: every
+ *     partial result a call reads was written earlier by the same call.
+ *   - Calls whose kernels overlap on the GPU (different streams without
+ *     ordering between them) race on the array; order them on one stream
+ *     or use pa_decode with separate workspaces. */
+#define PA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+pa_status pa_decode_noalloc(const void* q, const void* k_cache,
+                            const void* v_cache, const float* k_scale,
+                            const float* v_scale, pa_kv_dtype kv_dtype,
+                            const int32_t* block_tables,
+                            int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t num_seqs,
+                            int32_t num_q_heads, int32_t num_kv_heads,
+                            int32_t head_dim, int32_t block_size,
+                            int32_t num_blocks, float scale, void* out,
+                            int32_t num_splits, void* stream);
+
 /* ------------------------------------------------------- block manager
  * Host-only block allocator ("Paged Attention and KV Cache Fragmentation",
  * section "How PagedAttention maps an OS concept onto GPU memory"; shared

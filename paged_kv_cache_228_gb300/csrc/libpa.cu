@@ -418,3 +418,52 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
     return launch_decode<128, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
   return launch_decode<64, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
 }
+
+// ------------------------------------------------------------ no-alloc ---
+// Scratch for pa_decode_noalloc: a file-scope device array, so the entry
+// point needs no allocation.  In host code the symbol is only a host-side
+// stand-in; the device address is looked up per device with
+// cudaGetSymbolAddress (with that device current) and cached.
+namespace pa {
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+void* g_noalloc_addr[kMaxDevices] = {nullptr};
+std::mutex g_noalloc_mu;
+
+pa_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PA_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return PA_ERR_CUDA;
+    g_noalloc_addr[dev] = p;
+  }
+  *out = g_noalloc_addr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                       const float* k_scale, const float* v_scale,
+                                       pa_kv_dtype kv_dtype, const int32_t* block_tables,
+                                       int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                       int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim,
+                                       int32_t block_size, int32_t num_blocks, float scale,
+                                       void* out, int32_t num_splits, void* stream) {
+  void* scratch = nullptr;
+  const pa_status st = pa::noalloc_scratch(&scratch);
+  if (st != PA_OK) return st;
+  // pa_decode validates the arguments first and returns PA_ERR_WORKSPACE,
+  // enqueuing nothing, when this shape needs more than the array holds.
+  return pa_decode(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_tables,
+                   max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                   head_dim, block_size, num_blocks, scale, out, scratch,
+                   PA_NOALLOC_SCRATCH_BYTES, num_splits, stream);
+}

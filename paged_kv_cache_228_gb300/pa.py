@@ -45,6 +45,9 @@ SIGNATURES = {
     "pa_decode": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                            _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                            ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int, _c_ptr]),
+    "pa_decode_noalloc": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr,
+                                   _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   _c_int, ctypes.c_float, _c_ptr, _c_int, _c_ptr]),
     "pa_allocator_create": (_c_int, [_c_int, ctypes.POINTER(_c_ptr)]),
     "pa_allocator_destroy": (None, [_c_ptr]),
     "pa_block_alloc": (_c_int, [_c_ptr, _c_int, _c_ptr]),
@@ -188,6 +191,28 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out, workspace
         _kv_dtype(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
         hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits,
         _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def pa_decode_noalloc(q, k_cache, v_cache, block_tables, seq_lens, scale, out,
+                      k_scale=None, v_scale=None, num_splits=0, stream=None):
+    """pa_decode without a workspace argument, for callers that cannot
+    allocate device memory: the library's own 16 MiB device array serves as
+    scratch.  Calls on one device share it, so calls whose kernels overlap
+    (unordered streams) race; requests needing more scratch raise
+    PA_ERR_WORKSPACE."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    _check("pa_decode_noalloc", lib().pa_decode_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+        _kv_dtype(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
+        hq, hkv, d, bs, nb, float(scale), _ptr(out), num_splits, _stream(stream)))
 
 
 # --------------------------------------------------------- block manager ---
