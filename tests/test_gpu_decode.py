@@ -228,6 +228,19 @@ def test_partition_count_within_tolerance(splits):
     assert pa.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("splits", [0, 2000])
+def test_repeated_decode_is_bit_identical(splits):
+    # The reduction order depends only on logical positions and the partition
+    # count, so repeated calls must agree bit for bit; a pipeline race (a tile
+    # read before its copy landed or after the next copy overwrote it) would
+    # show up here as run-to-run differences.
+    case = build_case(W.llama31_8b())
+    outs = [run_step(case, write=False, num_splits=splits) for _ in range(6)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert pa.pa_get_device_error() == 0
+
+
 def test_empty_and_ragged_sequences():
     lens = [0, 1, 15, 16, 17, 0, 33, 255, 256, 257]
     w = W.Workload("ragged", len(lens), 8, 2, 64, 16, seq_lens=[max(1, n) for n in lens],
