@@ -33,10 +33,11 @@
 //     online softmax per head column in fp32 (running max m, sum l)
 //     O^T[d x 8 heads]     += V_tile^T[d x 16] . P^T[16 x 8] (ldmatrix.trans)
 //   P^T's fragment comes from S^T's accumulator by one movmatrix.trans per
-//   8x8 quarter.  FP8 tiles are converted to f16 in registers (exact) with
-//   a d-permutation that makes every fragment one 32-bit shared load; the
-//   per-(block, head) K scale multiplies the scores and the V scale the
-//   per-tile P.V product, so accumulation stays fp32.
+//   8x8 quarter.  FP8 tiles: QK runs on the E4M3 MMA straight from the
+//   cache bytes (the query as a two-term E4M3 split), PV on the f16 MMA
+//   with V converted exactly in registers; the per-(block, head) K scale
+//   multiplies the scores and the V scale the per-tile P.V product, so
+//   accumulation stays fp32.
 #pragma once
 
 #include "pa_device.cuh"
@@ -425,27 +426,24 @@ __device__ __forceinline__ void tile_bf16(const DecodeParams& p, uint32_t kb,
   }
 }
 
-// Address of 32-bit word w of row r in an FP8 tile (rows of D bytes; 128B
-// swizzle for D = 128, 64B swizzle for D = 64).
+// Byte offset of 16-byte chunk `ch` of row r in an FP8 tile (rows of D
+// bytes; 128B swizzle for D = 128, 64B swizzle for D = 64).
 template <int D>
-__device__ __forceinline__ uint32_t fp8_word(uint32_t base, int r, int w) {
-  if (D == 128)
-    return base + r * 128 + ((((w >> 2) ^ (r & 7))) << 4) + ((w & 3) << 2);
-  else
-    return base + r * 64 + ((((w >> 2) ^ ((r >> 1) & 3))) << 4) + ((w & 3) << 2);
+__device__ __forceinline__ uint32_t fp8_chunk(int r, int ch) {
+  if (D == 128) return r * 128 + ((ch ^ (r & 7)) << 4);
+  return r * 64 + ((ch ^ ((r >> 1) & 3)) << 4);
 }
 
-__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
-  return v;
-}
-
-// FP8 tile.  Q^T fragments are f16 with a d-permutation: k-step kk, lane
-// (gq, tq) pairs k {2tq, 2tq+1, 2tq+8, 2tq+9} with d 16kk + 4tq + {0..3}, so
-// each K fragment register pair is one 32-bit shared load.  The V side uses
-// tokens {2tq, 2tq+1, 2tq+8, 2tq+9} (the order movmatrix leaves P in) and
-// an output d-permutation (see the finalisation).
+// FP8 tile.
+// QK on the E4M3 tensor-core MMA (m16n8k32): K fragments come straight from
+// ldmatrix (row = token, 4 consecutive d bytes per register); the query is a
+// two-term E4M3 split q*qs = hi + lo/16 per head (qb[2ks] = hi, qb[2ks+1] =
+// lo of k-step ks), so s = s_hi + s_lo/16 keeps it to 2^-8 relative.
+// PV on the f16 MMA: ldmatrix.trans of the E4M3 V rows gives each lane
+// (tokens 2tq, 2tq+1) x (d 2gq, 2gq+1) of a 16-byte chunk; one byte permute
+// and two exact cvt make the V^T fragments.  Output row gq of m-tile i is
+// d = 16i + 2gq, row gq + 8 is d = 16i + 2gq + 1.  The per-(block, head)
+// V scale multiplies the tile's P.V product in fp32.
 template <int D>
 __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
                                          uint32_t vb, int valid, float4 sc,
@@ -453,24 +451,23 @@ __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
                                          float hm0, float hm1,
                                          SegState<D>& s) {
   const int lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
-  float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+  const int gq = lane >> 2;
+  float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
-  for (int kk = 0; kk < D / 16; ++kk) {
-    const uint32_t w0 = lds32(fp8_word<D>(kb, gq, kk * 4 + tq));
-    const uint32_t w8 = lds32(fp8_word<D>(kb, gq + 8, kk * 4 + tq));
-    const uint32_t a0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0));
-    const uint32_t a2 = e4m3x2_to_f16x2(static_cast<uint16_t>(w0 >> 16));
-    const uint32_t a1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w8));
-    const uint32_t a3 = e4m3x2_to_f16x2(static_cast<uint16_t>(w8 >> 16));
-    if (kk & 1)
-      mma_f16(sb, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
-    else
-      mma_f16(sa, a0, a1, a2, a3, qb[kk][0], qb[kk][1]);
+    for (int ks = 0; ks < D / 32; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kb + fp8_chunk<D>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+      mma_e4m3(sh, a0, a1, a2, a3, qb[2 * ks][0], qb[2 * ks][1]);
+      mma_e4m3(sl, a0, a1, a2, a3, qb[2 * ks + 1][0], qb[2 * ks + 1][1]);
+    }
   }
   // row gq is in the tile's first block, row gq + 8 in its second (bs = 8)
-  float x0 = (sa[0] + sb[0]) * (sc.x * hm0), x1 = (sa[1] + sb[1]) * (sc.x * hm1);
-  float x2 = (sa[2] + sb[2]) * (sc.y * hm0), x3 = (sa[3] + sb[3]) * (sc.y * hm1);
+  float x0 = fmaf(sl[0], 0.0625f, sh[0]) * (sc.x * hm0);
+  float x1 = fmaf(sl[1], 0.0625f, sh[1]) * (sc.x * hm1);
+  float x2 = fmaf(sl[2], 0.0625f, sh[2]) * (sc.y * hm0);
+  float x3 = fmaf(sl[3], 0.0625f, sh[3]) * (sc.y * hm1);
   if (gq >= valid) x0 = x1 = -INFINITY;
   if (gq + 8 >= valid) x2 = x3 = -INFINITY;
   const float vmax = fmaxf(sc.z, sc.w);
@@ -480,35 +477,32 @@ __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
   softmax_tile<true>(x0, x1, x2, x3, s.m, s.l, r0, r1, alpha0, alpha1, pb0, pb1);
   rescale(s, alpha0, alpha1);
   // O^T += vmax * (V8^T . P'^T), P' = p * v_scale(row) / vmax (<= p)
-  const int t2 = 2 * tq;
+  {
+    const int j = lane >> 3;
+    const int r = (lane & 7) + (j & 1) * 8;  // token row
 #pragma unroll
-  for (int pp = 0; pp < D / 32; ++pp) {
-    const int w = pp * 8 + gq;
-    const uint32_t r0w = lds32(fp8_word<D>(vb, t2, w));
-    const uint32_t r1w = lds32(fp8_word<D>(vb, t2 + 1, w));
-    const uint32_t r8w = lds32(fp8_word<D>(vb, t2 + 8, w));
-    const uint32_t r9w = lds32(fp8_word<D>(vb, t2 + 9, w));
-    const uint32_t u0 = __byte_perm(r0w, r1w, 0x5140);
-    const uint32_t u1 = __byte_perm(r0w, r1w, 0x7362);
-    const uint32_t u2 = __byte_perm(r8w, r9w, 0x5140);
-    const uint32_t u3 = __byte_perm(r8w, r9w, 0x7362);
-    const uint32_t xd0 = __byte_perm(u0, u2, 0x5410);  // d = 4w + 0
-    const uint32_t xd1 = __byte_perm(u0, u2, 0x7632);  // d = 4w + 1
-    const uint32_t xd2 = __byte_perm(u1, u3, 0x5410);  // d = 4w + 2
-    const uint32_t xd3 = __byte_perm(u1, u3, 0x7632);  // d = 4w + 3
-    float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_f16(t0, e4m3x2_to_f16x2(static_cast<uint16_t>(xd0)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd1)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd0 >> 16)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd1 >> 16)), pb0, pb1);
-    mma_f16(t1, e4m3x2_to_f16x2(static_cast<uint16_t>(xd2)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd3)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd2 >> 16)),
-            e4m3x2_to_f16x2(static_cast<uint16_t>(xd3 >> 16)), pb0, pb1);
+    for (int pp = 0; pp < D / 32; ++pp) {
+      uint32_t v0, v1, v2, v3;  // (tok 0-7, ch 2pp), (8-15, 2pp), (0-7, 2pp+1), (8-15, 2pp+1)
+      ldsm_x4_t(vb + fp8_chunk<D>(r, 2 * pp + (j >> 1)), v0, v1, v2, v3);
+      // [t d, t d+1, t+1 d, t+1 d+1] -> [t d, t+1 d, t d+1, t+1 d+1]
+      const uint32_t u0 = __byte_perm(v0, 0, 0x3120);
+      const uint32_t u1 = __byte_perm(v1, 0, 0x3120);
+      const uint32_t u2 = __byte_perm(v2, 0, 0x3120);
+      const uint32_t u3 = __byte_perm(v3, 0, 0x3120);
+      float t0[4], t1[4];
+      mma_f16_zero_c(t0, e4m3x2_to_f16x2(static_cast<uint16_t>(u0)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u0 >> 16)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u1)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u1 >> 16)), pb0, pb1);
+      mma_f16_zero_c(t1, e4m3x2_to_f16x2(static_cast<uint16_t>(u2)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u2 >> 16)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u3)),
+                     e4m3x2_to_f16x2(static_cast<uint16_t>(u3 >> 16)), pb0, pb1);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      s.acc[2 * pp][q] = fmaf(vmax, t0[q], s.acc[2 * pp][q]);
-      s.acc[2 * pp + 1][q] = fmaf(vmax, t1[q], s.acc[2 * pp + 1][q]);
+      for (int q = 0; q < 4; ++q) {
+        s.acc[2 * pp][q] = fmaf(vmax, t0[q], s.acc[2 * pp][q]);
+        s.acc[2 * pp + 1][q] = fmaf(vmax, t1[q], s.acc[2 * pp + 1][q]);
+      }
     }
   }
 }
@@ -517,9 +511,8 @@ __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
 template <int D, bool FP8>
 __device__ __forceinline__ int acc_d(int i, int q, int gq) {
   if (!FP8) return 16 * i + gq + ((q >> 1) << 3);
-  // FP8: m-tile pair pp = i / 2 covers d = 32pp + 4gq + {0, 1, 2, 3}:
-  // (i even, rows gq / gq+8) -> +0 / +1, (i odd) -> +2 / +3.
-  return 32 * (i >> 1) + 4 * gq + 2 * (i & 1) + (q >> 1);
+  // FP8: m-tile i covers chunk i; rows gq / gq + 8 are d = 16i + 2gq (+1).
+  return 16 * i + 2 * gq + (q >> 1);
 }
 
 template <int D, bool FP8>
@@ -557,35 +550,57 @@ __device__ __forceinline__ void consumer(const DecodeParams& p, Header* hdr,
                 qb[kk][0], qb[kk][1], qb[kk + 1][0], qb[kk + 1][1]);
       }
     } else {
-      // q[gq][16kk + 4tq .. +3] as f16, scaled per head by a power of two
-      // that puts max|q| in [2^14, 2^15) (exact; undone in the scores).
-      float qv[D / 16][4];
+      // q[gq][32ks + 16h + 4tq .. +3] (h = 0, 1) as a two-term E4M3 split
+      // per head: x = q * qs with the power of two qs putting max|x| in
+      // [128, 256); hi = e4m3(x), lo = e4m3(16 (x - hi)); B fragments
+      // qb[2ks][h] = hi, qb[2ks + 1][h] = lo.  The scores are divided by qs.
+      float qv[D / 32][2][4];
       float amax = 0.f;
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const int byte = (16 * kk + 4 * tq) * 2;          // within the row
-        const int slab = byte >> 7, inrow = byte & 127;
-        const int ch = inrow >> 4;
-        const uint32_t addr = qslot + slab * L::kQSlabBytes + gq * 128 +
-                              ((ch ^ gq) << 4) + (inrow & 15);
-        uint32_t w0, w1;
-        asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];" : "=r"(w0), "=r"(w1) : "r"(addr));
-        const float2 f0 = unpack_bf16x2(w0), f1 = unpack_bf16x2(w1);
-        qv[kk][0] = f0.x; qv[kk][1] = f0.y; qv[kk][2] = f1.x; qv[kk][3] = f1.y;
-        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
-                                 fmaxf(fabsf(f1.x), fabsf(f1.y))));
-      }
+      for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int byte = (32 * ks + 16 * h + 4 * tq) * 2;  // within the row
+          const int slab = byte >> 7, inrow = byte & 127;
+          const int ch = inrow >> 4;
+          const uint32_t addr = qslot + slab * L::kQSlabBytes + gq * 128 +
+                                ((ch ^ gq) << 4) + (inrow & 15);
+          uint32_t w0, w1;
+          asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                       : "=r"(w0), "=r"(w1)
+                       : "r"(addr)
+                       : "memory");
+          const float2 f0 = unpack_bf16x2(w0), f1 = unpack_bf16x2(w1);
+          qv[ks][h][0] = f0.x; qv[ks][h][1] = f0.y; qv[ks][h][2] = f1.x; qv[ks][h][3] = f1.y;
+          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
+                                   fmaxf(fabsf(f1.x), fabsf(f1.y))));
+        }
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
       amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      int e = 0;
-      if (amax > 0.f) (void)frexpf(amax, &e);     // amax in [2^(e-1), 2^e)
-      const float qs = ldexpf(1.f, 15 - e);
+      // amax in [2^(e-1), 2^e) from the exponent field (subnormal or zero
+      // amax clamps to e = -100, which keeps every power of two below normal)
+      int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+      e = max(e, -100);
+      const float qs = __uint_as_float(static_cast<uint32_t>(8 - e + 127) << 23);
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        qb[kk][0] = pack_f16x2(qv[kk][0] * qs, qv[kk][1] * qs);
-        qb[kk][1] = pack_f16x2(qv[kk][2] * qs, qv[kk][3] * qs);
-      }
-      const float inv = ldexpf(p.scale_log2, e - 15);
+      for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          float x[4], r[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) x[k] = qv[ks][h][k] * qs;
+          const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]);
+          const uint32_t h23 = f32x2_to_e4m3x2(x[2], x[3]);
+          const float2 d01 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h01)));
+          const float2 d23 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h23)));
+          r[0] = (x[0] - d01.x) * 16.f;
+          r[1] = (x[1] - d01.y) * 16.f;
+          r[2] = (x[2] - d23.x) * 16.f;
+          r[3] = (x[3] - d23.y) * 16.f;
+          qb[2 * ks][h] = h01 | (h23 << 16);
+          qb[2 * ks + 1][h] = f32x2_to_e4m3x2(r[0], r[1]) | (f32x2_to_e4m3x2(r[2], r[3]) << 16);
+        }
+      const float inv = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(e - 8 + 127) << 23);
       hm0 = __shfl_sync(0xffffffffu, inv, (2 * tq) * 4);
       hm1 = __shfl_sync(0xffffffffu, inv, (2 * tq + 1) * 4);
     }

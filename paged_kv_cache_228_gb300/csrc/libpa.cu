@@ -94,7 +94,7 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
 }
 
 // Decode launch plan for one (head_dim, dtype) instantiation.
-constexpr int kTargetCtasPerSm = 6;
+constexpr int kTargetCtasPerSm = 8;
 constexpr size_t kSmemPerSm = 228 * 1024;
 constexpr size_t kSmemReservedPerCta = 1024;
 
