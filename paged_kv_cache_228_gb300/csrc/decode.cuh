@@ -331,19 +331,29 @@ __device__ __forceinline__ void softmax_tile(float x0, float x1, float x2,
                                              float ratio1, float& alpha0,
                                              float& alpha1, uint32_t& pb0,
                                              uint32_t& pb1) {
-  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+  // Conditional rescaling: the running max only moves when some score of
+  // the tile exceeds it by more than kSlack (log2 units); otherwise the
+  // weights 2^(x - m) stay <= 2^kSlack, exact enough in bf16/f16 and summed
+  // in fp32, and the cross-lane max reduction is skipped.  The first tile of
+  // a segment (m = -inf) always takes the full path.
+  constexpr float kSlack = 8.f;
+  const bool grow = fmaxf(x0, x2) > m[0] + kSlack || fmaxf(x1, x3) > m[1] + kSlack;
+  alpha0 = alpha1 = 1.f;
+  if (__any_sync(0xffffffffu, grow)) {
+    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
-  for (int o = 4; o < 32; o <<= 1) {
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
+    alpha0 = fast_exp2(m[0] - mn0);
+    alpha1 = fast_exp2(m[1] - mn1);
+    m[0] = mn0;
+    m[1] = mn1;
   }
-  const float mn0 = fmaxf(m[0], mx0), mn1 = fmaxf(m[1], mx1);
-  alpha0 = fast_exp2(m[0] - mn0);
-  alpha1 = fast_exp2(m[1] - mn1);
-  m[0] = mn0;
-  m[1] = mn1;
-  const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-  const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+  const float p0 = fast_exp2(x0 - m[0]), p1 = fast_exp2(x1 - m[1]);
+  const float p2 = fast_exp2(x2 - m[0]), p3 = fast_exp2(x3 - m[1]);
   uint32_t P01, P23;
   float2 r01, r23;
   if (F16P) {
@@ -452,26 +462,31 @@ __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
                                          SegState<D>& s) {
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2;
-  float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+  // Four independent accumulator chains (hi/lo x even/odd k-step) keep the
+  // dependent MMA depth at D/64.
+  float sh[2][4] = {}, sl[2][4] = {};
   {
     const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < D / 32; ++ks) {
       uint32_t a0, a1, a2, a3;
       ldsm_x4(kb + fp8_chunk<D>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-      mma_e4m3(sh, a0, a1, a2, a3, qb[2 * ks][0], qb[2 * ks][1]);
-      mma_e4m3(sl, a0, a1, a2, a3, qb[2 * ks + 1][0], qb[2 * ks + 1][1]);
+      mma_e4m3(sh[ks & 1], a0, a1, a2, a3, qb[2 * ks][0], qb[2 * ks][1]);
+      mma_e4m3(sl[ks & 1], a0, a1, a2, a3, qb[2 * ks + 1][0], qb[2 * ks + 1][1]);
     }
   }
   // row gq is in the tile's first block, row gq + 8 in its second (bs = 8)
-  float x0 = fmaf(sl[0], 0.0625f, sh[0]) * (sc.x * hm0);
-  float x1 = fmaf(sl[1], 0.0625f, sh[1]) * (sc.x * hm1);
-  float x2 = fmaf(sl[2], 0.0625f, sh[2]) * (sc.y * hm0);
-  float x3 = fmaf(sl[3], 0.0625f, sh[3]) * (sc.y * hm1);
+  float x[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    x[q] = fmaf(sl[0][q] + sl[1][q], 0.0625f, sh[0][q] + sh[1][q]) *
+           ((q < 2 ? sc.x : sc.y) * ((q & 1) ? hm1 : hm0));
+  float x0 = x[0], x1 = x[1], x2 = x[2], x3 = x[3];
   if (gq >= valid) x0 = x1 = -INFINITY;
   if (gq + 8 >= valid) x2 = x3 = -INFINITY;
   const float vmax = fmaxf(sc.z, sc.w);
-  const float r0 = sc.z / vmax, r1 = sc.w / vmax;
+  // ratios <= 1 of the two blocks' V scales (equal for block_size >= 16)
+  const float r0 = __fdividef(sc.z, vmax), r1 = __fdividef(sc.w, vmax);
   float alpha0, alpha1;
   uint32_t pb0, pb1;
   softmax_tile<true>(x0, x1, x2, x3, s.m, s.l, r0, r1, alpha0, alpha1, pb0, pb1);
