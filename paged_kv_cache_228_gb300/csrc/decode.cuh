@@ -454,72 +454,133 @@ __device__ __forceinline__ uint32_t fp8_chunk(int r, int ch) {
 // and two exact cvt make the V^T fragments.  Output row gq of m-tile i is
 // d = 16i + 2gq, row gq + 8 is d = 16i + 2gq + 1.  The per-(block, head)
 // V scale multiplies the tile's P.V product in fp32.
+
+// Masked scores (log2 units) of one FP8 tile: x = (row gq, head 2tq),
+// (gq, 2tq+1), (gq+8, 2tq), (gq+8, 2tq+1).
+template <int D>
+__device__ __forceinline__ void qk_fp8(uint32_t kb, int valid, float4 sc,
+                                       const uint32_t (&qb)[D / 16][2], float hm0,
+                                       float hm1, float (&x)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int gq = lane >> 2;
+  // Four independent accumulator chains (hi/lo x even/odd k-step) keep the
+  // dependent MMA depth at D/64.
+  float sh[2][4] = {}, sl[2][4] = {};
+  const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+  for (int ks = 0; ks < D / 32; ++ks) {
+    uint32_t a0, a1, a2, a3;
+    ldsm_x4(kb + fp8_chunk<D>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
+    mma_e4m3(sh[ks & 1], a0, a1, a2, a3, qb[2 * ks][0], qb[2 * ks][1]);
+    mma_e4m3(sl[ks & 1], a0, a1, a2, a3, qb[2 * ks + 1][0], qb[2 * ks + 1][1]);
+  }
+  // row gq is in the tile's first block, row gq + 8 in its second (bs = 8)
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    x[q] = fmaf(sl[0][q] + sl[1][q], 0.0625f, sh[0][q] + sh[1][q]) *
+           ((q < 2 ? sc.x : sc.y) * ((q & 1) ? hm1 : hm0));
+  if (gq >= valid) x[0] = x[1] = -INFINITY;
+  if (gq + 8 >= valid) x[2] = x[3] = -INFINITY;
+}
+
+// O^T += vmax * (V8^T . P'^T) for one FP8 tile, P' = p * v_scale(row) / vmax.
+template <int D>
+__device__ __forceinline__ void pv_fp8(uint32_t vb, float vmax, uint32_t pb0,
+                                       uint32_t pb1, SegState<D>& s) {
+  const int lane = threadIdx.x & 31;
+  const int j = lane >> 3;
+  const int r = (lane & 7) + (j & 1) * 8;  // token row
+#pragma unroll
+  for (int pp = 0; pp < D / 32; ++pp) {
+    uint32_t v0, v1, v2, v3;  // (tok 0-7, ch 2pp), (8-15, 2pp), (0-7, 2pp+1), (8-15, 2pp+1)
+    ldsm_x4_t(vb + fp8_chunk<D>(r, 2 * pp + (j >> 1)), v0, v1, v2, v3);
+    // [t d, t d+1, t+1 d, t+1 d+1] -> [t d, t+1 d, t d+1, t+1 d+1]
+    const uint32_t u0 = __byte_perm(v0, 0, 0x3120);
+    const uint32_t u1 = __byte_perm(v1, 0, 0x3120);
+    const uint32_t u2 = __byte_perm(v2, 0, 0x3120);
+    const uint32_t u3 = __byte_perm(v3, 0, 0x3120);
+    float t0[4], t1[4];
+    mma_f16_zero_c(t0, e4m3x2_to_f16x2(static_cast<uint16_t>(u0)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u0 >> 16)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u1)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u1 >> 16)), pb0, pb1);
+    mma_f16_zero_c(t1, e4m3x2_to_f16x2(static_cast<uint16_t>(u2)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u2 >> 16)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u3)),
+                   e4m3x2_to_f16x2(static_cast<uint16_t>(u3 >> 16)), pb0, pb1);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      s.acc[2 * pp][q] = fmaf(vmax, t0[q], s.acc[2 * pp][q]);
+      s.acc[2 * pp + 1][q] = fmaf(vmax, t1[q], s.acc[2 * pp + 1][q]);
+    }
+  }
+}
+
 template <int D>
 __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
                                          uint32_t vb, int valid, float4 sc,
                                          const uint32_t (&qb)[D / 16][2],
                                          float hm0, float hm1,
                                          SegState<D>& s) {
-  const int lane = threadIdx.x & 31;
-  const int gq = lane >> 2;
-  // Four independent accumulator chains (hi/lo x even/odd k-step) keep the
-  // dependent MMA depth at D/64.
-  float sh[2][4] = {}, sl[2][4] = {};
-  {
-    const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int ks = 0; ks < D / 32; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(kb + fp8_chunk<D>(r, 2 * ks + (lane >> 4)), a0, a1, a2, a3);
-      mma_e4m3(sh[ks & 1], a0, a1, a2, a3, qb[2 * ks][0], qb[2 * ks][1]);
-      mma_e4m3(sl[ks & 1], a0, a1, a2, a3, qb[2 * ks + 1][0], qb[2 * ks + 1][1]);
-    }
-  }
-  // row gq is in the tile's first block, row gq + 8 in its second (bs = 8)
   float x[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    x[q] = fmaf(sl[0][q] + sl[1][q], 0.0625f, sh[0][q] + sh[1][q]) *
-           ((q < 2 ? sc.x : sc.y) * ((q & 1) ? hm1 : hm0));
-  float x0 = x[0], x1 = x[1], x2 = x[2], x3 = x[3];
-  if (gq >= valid) x0 = x1 = -INFINITY;
-  if (gq + 8 >= valid) x2 = x3 = -INFINITY;
+  qk_fp8<D>(kb, valid, sc, qb, hm0, hm1, x);
   const float vmax = fmaxf(sc.z, sc.w);
   // ratios <= 1 of the two blocks' V scales (equal for block_size >= 16)
   const float r0 = __fdividef(sc.z, vmax), r1 = __fdividef(sc.w, vmax);
   float alpha0, alpha1;
   uint32_t pb0, pb1;
-  softmax_tile<true>(x0, x1, x2, x3, s.m, s.l, r0, r1, alpha0, alpha1, pb0, pb1);
+  softmax_tile<true>(x[0], x[1], x[2], x[3], s.m, s.l, r0, r1, alpha0, alpha1, pb0, pb1);
   rescale(s, alpha0, alpha1);
-  // O^T += vmax * (V8^T . P'^T), P' = p * v_scale(row) / vmax (<= p)
-  {
-    const int j = lane >> 3;
-    const int r = (lane & 7) + (j & 1) * 8;  // token row
+  pv_fp8<D>(vb, vmax, pb0, pb1, s);
+}
+
+// Two consecutive FP8 tiles of one segment in one step: the QK and PV
+// chains of the two tiles are independent, and one conditional-max check
+// (and, when needed, one cross-lane reduction) covers all 32 tokens.
+template <int D>
+__device__ __forceinline__ void tile_fp8_pair(uint32_t kbA, uint32_t vbA, float4 scA,
+                                              uint32_t kbB, uint32_t vbB, int validB,
+                                              float4 scB,
+                                              const uint32_t (&qb)[D / 16][2],
+                                              float hm0, float hm1, SegState<D>& s) {
+  float xa[4], xb[4];
+  qk_fp8<D>(kbA, kTile, scA, qb, hm0, hm1, xa);
+  qk_fp8<D>(kbB, validB, scB, qb, hm0, hm1, xb);
+  constexpr float kSlack = 8.f;  // as in softmax_tile
+  const float t0 = fmaxf(fmaxf(xa[0], xa[2]), fmaxf(xb[0], xb[2]));
+  const float t1 = fmaxf(fmaxf(xa[1], xa[3]), fmaxf(xb[1], xb[3]));
+  float alpha0 = 1.f, alpha1 = 1.f;
+  if (__any_sync(0xffffffffu, t0 > s.m[0] + kSlack || t1 > s.m[1] + kSlack)) {
+    float mx0 = t0, mx1 = t1;
 #pragma unroll
-    for (int pp = 0; pp < D / 32; ++pp) {
-      uint32_t v0, v1, v2, v3;  // (tok 0-7, ch 2pp), (8-15, 2pp), (0-7, 2pp+1), (8-15, 2pp+1)
-      ldsm_x4_t(vb + fp8_chunk<D>(r, 2 * pp + (j >> 1)), v0, v1, v2, v3);
-      // [t d, t d+1, t+1 d, t+1 d+1] -> [t d, t+1 d, t d+1, t+1 d+1]
-      const uint32_t u0 = __byte_perm(v0, 0, 0x3120);
-      const uint32_t u1 = __byte_perm(v1, 0, 0x3120);
-      const uint32_t u2 = __byte_perm(v2, 0, 0x3120);
-      const uint32_t u3 = __byte_perm(v3, 0, 0x3120);
-      float t0[4], t1[4];
-      mma_f16_zero_c(t0, e4m3x2_to_f16x2(static_cast<uint16_t>(u0)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u0 >> 16)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u1)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u1 >> 16)), pb0, pb1);
-      mma_f16_zero_c(t1, e4m3x2_to_f16x2(static_cast<uint16_t>(u2)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u2 >> 16)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u3)),
-                     e4m3x2_to_f16x2(static_cast<uint16_t>(u3 >> 16)), pb0, pb1);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        s.acc[2 * pp][q] = fmaf(vmax, t0[q], s.acc[2 * pp][q]);
-        s.acc[2 * pp + 1][q] = fmaf(vmax, t1[q], s.acc[2 * pp + 1][q]);
-      }
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
+    const float mn0 = fmaxf(s.m[0], mx0), mn1 = fmaxf(s.m[1], mx1);
+    alpha0 = fast_exp2(s.m[0] - mn0);
+    alpha1 = fast_exp2(s.m[1] - mn1);
+    s.m[0] = mn0;
+    s.m[1] = mn1;
   }
+  float pa[4], pb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    pa[q] = fast_exp2(xa[q] - s.m[q & 1]);
+    pb[q] = fast_exp2(xb[q] - s.m[q & 1]);
+  }
+  s.l[0] = s.l[0] * alpha0 + ((pa[0] + pa[2]) + (pb[0] + pb[2]));
+  s.l[1] = s.l[1] * alpha1 + ((pa[1] + pa[3]) + (pb[1] + pb[3]));
+  const float vmaxA = fmaxf(scA.z, scA.w), vmaxB = fmaxf(scB.z, scB.w);
+  const float ra0 = __fdividef(scA.z, vmaxA), ra1 = __fdividef(scA.w, vmaxA);
+  const float rb0 = __fdividef(scB.z, vmaxB), rb1 = __fdividef(scB.w, vmaxB);
+  const uint32_t pbA0 = movmatrix_t(pack_f16x2(pa[0] * ra0, pa[1] * ra0));
+  const uint32_t pbA1 = movmatrix_t(pack_f16x2(pa[2] * ra1, pa[3] * ra1));
+  const uint32_t pbB0 = movmatrix_t(pack_f16x2(pb[0] * rb0, pb[1] * rb0));
+  const uint32_t pbB1 = movmatrix_t(pack_f16x2(pb[2] * rb1, pb[3] * rb1));
+  rescale(s, alpha0, alpha1);
+  pv_fp8<D>(vbA, vmaxA, pbA0, pbA1, s);
+  pv_fp8<D>(vbB, vmaxB, pbB0, pbB1, s);
 }
 
 // d index of accumulator element (i, q) for lane gq.
@@ -625,6 +686,33 @@ __device__ __forceinline__ void consumer(const DecodeParams& p, Header* hdr,
     seg_reset(s);
     // ---- tiles
     for (int32_t tile = c.tile; tile < seg_end; ++tile) {
+      if (FP8 && tile + 1 < seg_end) {
+        // Two full-or-tail tiles in one step (the first is never a tail).
+        const uint32_t sA = it % p.stages, sB = (it + 1) % p.stages;
+        ok = mbar_wait(smem_addr(&hdr->full[sA]), (it / p.stages) & 1);
+        ok = ok && mbar_wait(smem_addr(&hdr->full[sB]), ((it + 1) / p.stages) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        const uint32_t kbA = ring + sA * L::kStageBytes, kbB = ring + sB * L::kStageBytes;
+        const int validB = min(kTile, c.n - (tile + 1) * kTile);
+        if (validB < kTile) {
+          for (int off = validB * D + lane * 16; off < kTile * D; off += 32 * 16)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(kbB + L::kKVBytes + off), "r"(0)
+                         : "memory");
+          fence_proxy_async_smem();
+          __syncwarp();
+        }
+        tile_fp8_pair<D>(kbA, kbA + L::kKVBytes, hdr->scales[sA], kbB, kbB + L::kKVBytes,
+                         validB, hdr->scales[sB], qb, hm0, hm1, s);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_addr(&hdr->empty[sA]));
+          mbar_arrive(smem_addr(&hdr->empty[sB]));
+        }
+        it += 2;
+        ++tile;
+        continue;
+      }
       const uint32_t stage = it % p.stages;
       ok = mbar_wait(smem_addr(&hdr->full[stage]), (it / p.stages) & 1);
       ok = __all_sync(0xffffffffu, ok);
