@@ -20,12 +20,16 @@
 //   unnormalised partial (o, m, l) that the merge kernel combines by
 //   log-sum-exp.  Split points depend only on seq_lens, so the output does
 //   not depend on which physical blocks the tables name.
-// * CTA = 2 warps.  Warp 0 (producer) reads block-table entries 32 at a
-//   time with one coalesced warp load and issues 2D TMA copies of each
-//   tile's K and V rows (128-byte wide boxes, 128B swizzle) into a ring of
-//   shared-memory stages guarded by mbarriers; it also stages the G query
-//   rows of each new segment.  Warp 1 (consumer) runs the math.  Several
-//   CTAs per SM keep >100 KB of loads in flight per SM.
+// * Copies: 2D TMA boxes of each tile's K and V rows (128 bytes wide, 128B
+//   swizzle; 64B for FP8 d=64) into a ring of shared-memory stages, one
+//   mbarrier per stage, plus the G query rows of each new segment.  Block-
+//   table entries arrive 32 blocks at a time from one coalesced warp load,
+//   the next batch (and its FP8 scales) loaded ahead.
+// * CTA shape per instantiation.  bf16: 2 warps, a copy warp and a math
+//   warp, 8 CTAs per SM -- under full HBM load a TMA issue stalls its
+//   thread for hundreds of cycles, and the copy warp absorbs that.  FP8:
+//   the math per byte is ~2.5x heavier, so every warp computes: 1-warp
+//   CTAs (16 per SM) that top their ring up after each tile.
 // * Math on tensor cores (mma.sync m16n8k16, fp32 accumulate), tokens on M
 //   and the GQA group on N, so one K/V tile feeds every query head of its
 //   group from a single read:
@@ -64,6 +68,14 @@ struct DecodeParams {
 };
 
 // ------------------------------------------------ shared memory layout ---
+// [query slots | stage ring | header].  A bf16 tile is D/64 slabs of 16
+// rows x 128 bytes, an FP8 tile 16 rows x D bytes, both as the TMA's 128B
+// (64B for FP8 d=64) swizzle writes them: the 8 rows of an ldmatrix hit 8
+// different bank groups.  Query slots and stages are multiples of 1024
+// bytes, so every box starts 1024-aligned.
+constexpr int kQSlots = 2;
+constexpr int kMaxStages = 24;
+
 template <int D, bool FP8>
 struct Smem {
   static constexpr int kSlabBytes = FP8 ? kTile * D : kTile * 128;  // one box
@@ -72,18 +84,22 @@ struct Smem {
   static constexpr int kStageBytes = 2 * kKVBytes;
   static constexpr int kQSlabBytes = 8 * 128;           // 8 rows x 64 bf16
   static constexpr int kQBytes = (D / 64) * kQSlabBytes;
-  static constexpr int kHeaderBytes = 1024;  // barriers + per-stage scales
-  static constexpr int kMaxStages = 24;
+  static_assert(kStageBytes % 1024 == 0 && kQBytes % 1024 == 0, "alignment");
 };
 
 struct Header {
-  uint64_t full[24];
-  uint64_t empty[24];
-  uint64_t qfull[2];
-  uint64_t qempty[2];
-  float4 scales[24];  // FP8: (k_scale row g, k_scale row g+8, v_scale ...)
+  uint64_t full[kMaxStages];   // stage landed
+  uint64_t empty[kMaxStages];  // stage read (two-warp CTAs)
+  uint64_t qfull[kQSlots];     // query slot landed
+  uint64_t qempty[kQSlots];    // query slot read (two-warp CTAs)
+  float4 scales[kMaxStages];  // FP8: (k_scale row g, k_scale row g+8, v_scale ...)
 };
-static_assert(sizeof(Header) <= 1024, "header overflow");
+
+template <int D, bool FP8>
+__host__ __device__ constexpr size_t decode_smem_bytes(int stages) {
+  return static_cast<size_t>(kQSlots) * Smem<D, FP8>::kQBytes +
+         static_cast<size_t>(stages) * Smem<D, FP8>::kStageBytes + sizeof(Header);
+}
 
 __device__ __forceinline__ int32_t cdiv16(int32_t n) { return (n + 15) >> 4; }
 
@@ -101,36 +117,46 @@ struct Cursor {
   int32_t b, g, tile, T, n;
 };
 
-// Warp-collective: find the segment holding flat tile u (< W).
+// Warp-collective: find the segment holding flat tile u (< W).  The
+// lengths of 128 sequences are loaded at once.
 __device__ __forceinline__ void locate(const DecodeParams& p, int64_t u,
                                        Cursor& c) {
   const int lane = threadIdx.x & 31;
   int64_t base = 0;
-  for (int32_t b0 = 0; b0 < p.num_seqs; b0 += 32) {
-    const int32_t b = b0 + lane;
-    const int32_t n = b < p.num_seqs ? clamp_len(p, p.seq_lens[b]) : 0;
-    const int64_t w = static_cast<int64_t>(p.num_kv_heads) * cdiv16(n);
-    int64_t incl = w;
+  for (int32_t b00 = 0; b00 < p.num_seqs; b00 += 128) {
+    int32_t nk[4];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+    for (int k = 0; k < 4; ++k) {
+      const int32_t b = b00 + 32 * k + lane;
+      nk[k] = b < p.num_seqs ? clamp_len(p, p.seq_lens[b]) : 0;
     }
-    const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-    if (base + total > u) {
-      const unsigned m = __ballot_sync(0xffffffffu, base + incl > u);
-      const int L = __ffs(m) - 1;
-      const int64_t excl = __shfl_sync(0xffffffffu, incl - w, L);
-      const int32_t nn = __shfl_sync(0xffffffffu, n, L);
-      const int64_t rem = u - (base + excl);
-      c.b = b0 + L;
-      c.n = nn;
-      c.T = cdiv16(nn);
-      c.g = static_cast<int32_t>(rem / c.T);
-      c.tile = static_cast<int32_t>(rem % c.T);
-      return;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int32_t b0 = b00 + 32 * k;
+      const int32_t n = nk[k];
+      const int64_t w = static_cast<int64_t>(p.num_kv_heads) * cdiv16(n);
+      int64_t incl = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
+      if (base + total > u) {
+        const unsigned m = __ballot_sync(0xffffffffu, base + incl > u);
+        const int L = __ffs(m) - 1;
+        const int64_t excl = __shfl_sync(0xffffffffu, incl - w, L);
+        const int32_t nn = __shfl_sync(0xffffffffu, n, L);
+        const int64_t rem = u - (base + excl);
+        c.b = b0 + L;
+        c.n = nn;
+        c.T = cdiv16(nn);
+        c.g = static_cast<int32_t>(rem / c.T);
+        c.tile = static_cast<int32_t>(rem % c.T);
+        return;
+      }
+      base += total;
     }
-    base += total;
   }
   c.b = p.num_seqs;  // unreachable for u < W
   c.g = c.tile = c.T = c.n = 0;
@@ -164,6 +190,7 @@ __device__ __forceinline__ int32_t cta_of(int64_t W, int32_t P, int64_t u) {
 __device__ __forceinline__ int64_t total_tiles(const DecodeParams& p) {
   const int lane = threadIdx.x & 31;
   int64_t w = 0;
+#pragma unroll 4
   for (int32_t b = lane; b < p.num_seqs; b += 32)
     w += cdiv16(clamp_len(p, p.seq_lens[b]));
 #pragma unroll
@@ -171,133 +198,240 @@ __device__ __forceinline__ int64_t total_tiles(const DecodeParams& p) {
   return w * p.num_kv_heads;
 }
 
-// ------------------------------------------------------------ producer ---
-template <int D, bool FP8>
-__device__ __forceinline__ void producer(const DecodeParams& p,
-                                         const CUtensorMap* tm_q,
-                                         const CUtensorMap* tm_k,
-                                         const CUtensorMap* tm_v, Header* hdr,
-                                         uint32_t qbuf, uint32_t ring,
-                                         int64_t lo, int64_t hi) {
-  using L = Smem<D, FP8>;
+// ---------------------------------------------------------- issue side ---
+struct Maps {
+  const CUtensorMap* q;
+  const CUtensorMap* k;
+  const CUtensorMap* v;
+};
+
+struct Bufs {
+  uint32_t q, ring;  // shared addresses of the query slots and the ring
+  Header* hdr;
+};
+
+// Table batch: lane l holds the entry of block (l & (rpt - 1)) of tile
+// tb + l / rpt, rpt = blocks per tile (2 for block_size 8, else 1).
+struct Loader {
+  Cursor c;          // next tile to issue
+  int64_t u;         // its flat index
+  int32_t seg_end;   // end of this CTA's part of c's segment
+  int32_t tb;        // first tile of the table batch held (-1: none)
+  int32_t e;         // this lane's table entry
+  int32_t ne;        // the same for the next batch, loaded ahead
+  float ks, vs;      // FP8: scales of e for head g
+  float nks, nvs;    // FP8: scales of ne, loaded mid-batch
+  uint32_t it;       // tiles issued
+  uint32_t qn;       // query slots filled (segments begun)
+  bool fresh;        // the next tile opens a segment
+};
+
+// log2 of the blocks per 16-token tile
+__device__ __forceinline__ int rpt_log2(const DecodeParams& p) {
+  return p.block_size < kTile ? 1 : 0;
+}
+
+// This lane's table entry in the batch that starts at tile t (-1 past the
+// end of the CTA's part of the segment or of the sequence).
+__device__ __forceinline__ int32_t fetch_entry(const DecodeParams& p, const Loader& ld,
+                                               int32_t t) {
   const int lane = threadIdx.x & 31;
-  Cursor c;
-  locate(p, lo, c);
-  int64_t u = lo;
-  uint32_t it = 0;      // tiles issued
-  uint32_t qcount = 0;  // segments issued
+  const int lr = rpt_log2(p);
+  const int32_t tile = t + (lane >> lr);
+  const int32_t tok = tile * kTile + (lane & ((1 << lr) - 1)) * p.block_size;
+  if (tile >= ld.seg_end || tok >= ld.c.n) return -1;
+  return p.block_tables[static_cast<int64_t>(ld.c.b) * p.max_blocks + (tok >> p.log2_bs)];
+}
+
+// FP8 scales of block x for head g (1 for ids out of range).
+__device__ __forceinline__ void fetch_scales(const DecodeParams& p, int32_t g, int32_t x,
+                                             float& k, float& v) {
+  k = v = 1.f;
+  if (x >= 0 && x < p.num_blocks) {
+    k = p.k_scale[static_cast<int64_t>(x) * p.num_kv_heads + g];
+    v = p.v_scale[static_cast<int64_t>(x) * p.num_kv_heads + g];
+  }
+}
+
+// Warp-collective: make the table entries (and FP8 scales) of tile
+// ld.c.tile available.  The next batch's entries are loaded one batch
+// ahead and their scales half a batch ahead, so only the first batch of a
+// segment waits on memory.
+template <bool FP8>
+__device__ __forceinline__ void advance_table(const DecodeParams& p, Loader& ld) {
+  const int32_t t = ld.c.tile;
+  const int32_t per = 32 >> rpt_log2(p);  // tiles per batch
+  if (ld.tb < 0) {
+    ld.e = fetch_entry(p, ld, t);
+    if (FP8) fetch_scales(p, ld.c.g, ld.e, ld.ks, ld.vs);
+    ld.ne = fetch_entry(p, ld, t + per);
+    ld.tb = t;
+  } else if (t - ld.tb == per) {
+    ld.e = ld.ne;
+    if (FP8) {
+      ld.ks = ld.nks;
+      ld.vs = ld.nvs;
+    }
+    ld.ne = fetch_entry(p, ld, t + per);
+    ld.tb = t;
+  }
+  if (FP8 && t - ld.tb == per / 2) fetch_scales(p, ld.c.g, ld.ne, ld.nks, ld.nvs);
+}
+
+// Lane 0: the query rows of segment c into slot `slot` (8 rows from
+// b*Hq + g*G; rows past the group are ignored, rows past the tensor read
+// zeros).
+template <int D, bool FP8>
+__device__ __forceinline__ void copy_query(const DecodeParams& p, const Maps& tm,
+                                           const Bufs& sb, const Cursor& c, uint32_t slot) {
+  using L = Smem<D, FP8>;
+  const uint32_t bar = smem_addr(&sb.hdr->qfull[slot]);
+  mbar_arrive_expect_tx(bar, L::kQBytes);
+  const int32_t row = c.b * p.num_q_heads + c.g * p.group;
+#pragma unroll
+  for (int sl = 0; sl < D / 64; ++sl)
+    tma_load_2d(sb.q + slot * L::kQBytes + sl * L::kQSlabBytes, tm.q, sl * 64, row, bar);
+}
+
+// Lane 0: K and V rows of tile c.tile into `stage`, one box per block (two
+// for block_size 8).  An invalid block id reads rows past the tensor, which
+// the TMA fills with zeros.
+template <int D, bool FP8>
+__device__ __forceinline__ void copy_tile(const DecodeParams& p, const Maps& tm,
+                                          const Bufs& sb, const Cursor& c, uint32_t stage,
+                                          int32_t b0, int32_t b1) {
+  using L = Smem<D, FP8>;
+  const int32_t tok = c.tile * kTile;
   const int box_rows = p.block_size < kTile ? p.block_size : kTile;
   const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * (FP8 ? D : 128);
-  bool ok = true;
-  while (u < hi && ok) {
-    const int32_t seg_end = static_cast<int32_t>(
-        min(static_cast<int64_t>(c.T), c.tile + (hi - u)));
-    // Query rows of this segment: 8 rows from b*Hq + g*G (rows past the
-    // group are ignored by the consumer; past the tensor they read zeros).
-    if (lane == 0) {
-      const uint32_t slot = qcount & 1;
-      if (qcount >= 2) ok = mbar_wait(smem_addr(&hdr->qempty[slot]), ((qcount >> 1) - 1) & 1);
-      if (ok) {
-        const uint32_t bar = smem_addr(&hdr->qfull[slot]);
-        mbar_arrive_expect_tx(bar, L::kQBytes);
-        const int32_t row = c.b * p.num_q_heads + c.g * p.group;
-#pragma unroll
-        for (int s = 0; s < D / 64; ++s)
-          tma_load_2d(qbuf + slot * L::kQBytes + s * L::kQSlabBytes, tm_q,
-                      s * 64, row, bar);
-      }
+  const int nbox = (p.block_size < kTile && tok + p.block_size < c.n) ? 2 : 1;
+  const uint32_t bar = smem_addr(&sb.hdr->full[stage]);
+  mbar_arrive_expect_tx(bar, 2u * nbox * L::kSlabs * box_bytes);
+  const uint32_t kdst = sb.ring + stage * L::kStageBytes;
+  const uint32_t vdst = kdst + L::kKVBytes;
+  for (int bx = 0; bx < nbox; ++bx) {
+    const int32_t blk = bx == 0 ? b0 : b1;
+    int32_t row;  // row = (blk * Hkv + g) * bs + offset
+    if (blk < 0 || blk >= p.num_blocks) {
+      flag_error(PA_DEVERR_BAD_BLOCK_ID);
+      row = p.rows_total;  // out of the tensor: zero fill
+    } else {
+      const int32_t off = p.block_size >= kTile ? (tok & (p.block_size - 1)) : 0;
+      row = (blk * p.num_kv_heads + c.g) * p.block_size + off;
     }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    ++qcount;
-    const int32_t* trow = p.block_tables + static_cast<int64_t>(c.b) * p.max_blocks;
-    const int32_t kvrow_base = c.g;  // row = (blk * Hkv + g) * bs + offset
-    for (int32_t t0 = c.tile; t0 < seg_end && ok; t0 += 32) {
-      const int32_t nt = min(32, seg_end - t0);
-      // One coalesced load of the table entries of up to 32 tiles.
-      int32_t e0 = -1, e1 = -1;
-      float ks0 = 1.f, ks1 = 1.f, vs0 = 1.f, vs1 = 1.f;
-      if (lane < nt) {
-        const int32_t tok = (t0 + lane) * kTile;
-        if (p.block_size >= kTile) {
-          e0 = trow[tok >> p.log2_bs];
-        } else {
-          e0 = trow[tok >> p.log2_bs];
-          if (tok + p.block_size < c.n) e1 = trow[(tok >> p.log2_bs) + 1];
-        }
-        bool bad = e0 < 0 || e0 >= p.num_blocks;
-        if (p.block_size < kTile && tok + p.block_size < c.n)
-          bad |= e1 < 0 || e1 >= p.num_blocks;
-        if (bad) flag_error(PA_DEVERR_BAD_BLOCK_ID);
-        if (FP8) {
-          if (e0 >= 0 && e0 < p.num_blocks) {
-            ks0 = p.k_scale[static_cast<int64_t>(e0) * p.num_kv_heads + c.g];
-            vs0 = p.v_scale[static_cast<int64_t>(e0) * p.num_kv_heads + c.g];
-          }
-          ks1 = ks0;
-          vs1 = vs0;
-          if (p.block_size < kTile && e1 >= 0 && e1 < p.num_blocks) {
-            ks1 = p.k_scale[static_cast<int64_t>(e1) * p.num_kv_heads + c.g];
-            vs1 = p.v_scale[static_cast<int64_t>(e1) * p.num_kv_heads + c.g];
-          }
-        }
-      }
-      for (int32_t j = 0; j < nt; ++j) {
-        const int32_t b0 = __shfl_sync(0xffffffffu, e0, j);
-        const int32_t b1 = __shfl_sync(0xffffffffu, e1, j);
-        float4 sc;
-        sc.x = __shfl_sync(0xffffffffu, ks0, j);
-        sc.y = __shfl_sync(0xffffffffu, ks1, j);
-        sc.z = __shfl_sync(0xffffffffu, vs0, j);
-        sc.w = __shfl_sync(0xffffffffu, vs1, j);
-        if (lane == 0) {
-          const uint32_t stage = it % p.stages;
-          const uint32_t use = it / p.stages;
-          if (use > 0) ok = mbar_wait(smem_addr(&hdr->empty[stage]), (use - 1) & 1);
-          if (ok) {
-            if (FP8) hdr->scales[stage] = sc;
-            const int32_t tile = t0 + j;
-            const int32_t tok = tile * kTile;
-            const int nbox = (p.block_size < kTile && tok + p.block_size < c.n) ? 2 : 1;
-            const uint32_t bar = smem_addr(&hdr->full[stage]);
-            mbar_arrive_expect_tx(bar, 2u * nbox * L::kSlabs * box_bytes);
-            const uint32_t kdst = ring + stage * L::kStageBytes;
-            const uint32_t vdst = kdst + L::kKVBytes;
-            for (int bx = 0; bx < nbox; ++bx) {
-              const int32_t blk = bx == 0 ? b0 : b1;
-              int32_t row;
-              if (blk < 0 || blk >= p.num_blocks) {
-                row = p.rows_total;  // out of the tensor: TMA fills zeros
-              } else {
-                const int32_t off = p.block_size >= kTile ? (tok & (p.block_size - 1)) : 0;
-                row = (blk * p.num_kv_heads + kvrow_base) * p.block_size + off;
-              }
-              const uint32_t sub = static_cast<uint32_t>(bx) * box_bytes;
+    const uint32_t sub = static_cast<uint32_t>(bx) * box_bytes;
 #pragma unroll
-              for (int s = 0; s < L::kSlabs; ++s) {
-                tma_load_2d(kdst + s * L::kSlabBytes + sub, tm_k, s * 64, row, bar);
-                tma_load_2d(vdst + s * L::kSlabBytes + sub, tm_v, s * 64, row, bar);
-              }
-            }
-          }
-        }
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        ++it;
-        if (!ok) break;
-      }
+    for (int sl = 0; sl < L::kSlabs; ++sl) {
+      tma_load_2d(kdst + sl * L::kSlabBytes + sub, tm.k, sl * 64, row, bar);
+      tma_load_2d(vdst + sl * L::kSlabBytes + sub, tm.v, sl * 64, row, bar);
     }
-    u += seg_end - c.tile;
-    if (u < hi) next_segment(p, c);
   }
-  // Drain: wait until every copy this CTA issued has landed (no TMA may
-  // target shared memory after the CTA exits).  On the normal path the
-  // consumer already waited for all of them.
+}
+
+// Warp-collective: issue the loader's next tile (and, if it opens a
+// segment, the segment's query rows) into the next stage, then advance
+// the loader.  The caller has made sure the stage and query slot are free.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm,
+                                           const Bufs& sb, Loader& ld, int64_t hi) {
+  const int lane = threadIdx.x & 31;
+  if (ld.fresh) {
+    if (lane == 0) copy_query<D, FP8>(p, tm, sb, ld.c, ld.qn % kQSlots);
+    ++ld.qn;
+    ld.fresh = false;
+  }
+  advance_table<FP8>(p, ld);
+  const int lr = rpt_log2(p);
+  const int j = (ld.c.tile - ld.tb) << lr;  // lane of the tile's first block
+  const int32_t b0 = __shfl_sync(0xffffffffu, ld.e, j);
+  const int32_t b1 = __shfl_sync(0xffffffffu, ld.e, (j + lr) & 31);  // bs 8: second block
+  const uint32_t stage = ld.it % p.stages;
+  if (FP8) {
+    float4 sc;
+    sc.x = __shfl_sync(0xffffffffu, ld.ks, j);
+    sc.y = __shfl_sync(0xffffffffu, ld.ks, (j + lr) & 31);
+    sc.z = __shfl_sync(0xffffffffu, ld.vs, j);
+    sc.w = __shfl_sync(0xffffffffu, ld.vs, (j + lr) & 31);
+    // an absent (or unusable) second block takes the first one's scales,
+    // so the V-scale ratios of the tile stay 1
+    if (!(b1 >= 0 && b1 < p.num_blocks)) {
+      sc.y = sc.x;
+      sc.w = sc.z;
+    }
+    // written before the stage's arrive, read after its completion
+    if (lane == 0) sb.hdr->scales[stage] = sc;
+  }
+  if (lane == 0) copy_tile<D, FP8>(p, tm, sb, ld.c, stage, b0, b1);
+  ++ld.it;
+  ++ld.u;
+  if (++ld.c.tile == ld.seg_end && ld.u < hi) {
+    next_segment(p, ld.c);
+    ld.seg_end = static_cast<int32_t>(min(static_cast<int64_t>(ld.c.T), hi - ld.u));
+    ld.tb = -1;
+    ld.fresh = true;
+  }
+}
+
+// Warp-collective: the loader at flat tile lo of a CTA owning [lo, hi).
+__device__ __forceinline__ void loader_init(const DecodeParams& p, int64_t lo, int64_t hi,
+                                            Loader& ld) {
+  locate(p, lo, ld.c);
+  ld.u = lo;
+  ld.seg_end = static_cast<int32_t>(min(static_cast<int64_t>(ld.c.T), ld.c.tile + (hi - lo)));
+  ld.tb = -1;
+  ld.e = ld.ne = -1;
+  ld.ks = ld.vs = ld.nks = ld.nvs = 1.f;
+  ld.it = ld.qn = 0;
+  ld.fresh = true;
+}
+
+__device__ __forceinline__ bool can_issue(const DecodeParams& p, const Loader& ld,
+                                          int64_t hi, uint32_t used, uint32_t qread) {
+  return ld.u < hi && ld.it - used < static_cast<uint32_t>(p.stages) &&
+         (!ld.fresh || ld.qn - qread < static_cast<uint32_t>(kQSlots));
+}
+
+// Single-warp CTA: issue tiles while a stage is free (`used` = tiles
+// consumed) and, for a tile that opens a segment, a query slot is free
+// (`qread` = slots read).  The warp has synchronised after its last reads
+// of the bytes these copies overwrite; the proxy fence orders those reads
+// before the TMA writes.
+template <int D, bool FP8>
+__device__ __forceinline__ void top_up(const DecodeParams& p, const Maps& tm, const Bufs& sb,
+                                       Loader& ld, int64_t hi, uint32_t used, uint32_t qread) {
+  if (!can_issue(p, ld, hi, used, qread)) return;
+  if ((threadIdx.x & 31) == 0) fence_proxy_async_smem();
+  do {
+    issue_tile<D, FP8>(p, tm, sb, ld, hi);
+  } while (can_issue(p, ld, hi, used, qread));
+  __syncwarp();
+}
+
+// Two-warp CTA, copy warp: issue every tile of [lo, hi) as soon as the
+// math warp has released its stage (and query slot).
+template <int D, bool FP8>
+__device__ __forceinline__ void produce(const DecodeParams& p, const Maps& tm, const Bufs& sb,
+                                        Loader& ld, int64_t hi) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t S = p.stages;
+  bool ok = true;
+  while (ld.u < hi) {
+    if (lane == 0) {
+      if (ld.fresh && ld.qn >= kQSlots)
+        ok = mbar_wait(smem_addr(&sb.hdr->qempty[ld.qn % kQSlots]), (ld.qn / kQSlots - 1) & 1);
+      if (ok && ld.it >= S)
+        ok = mbar_wait(smem_addr(&sb.hdr->empty[ld.it % S]), (ld.it / S - 1) & 1);
+    }
+    if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+    issue_tile<D, FP8>(p, tm, sb, ld, hi);
+  }
+  // No copy may target shared memory after the CTA exits.  On the normal
+  // path the math warp has already waited for all of them.
   if (lane == 0) {
-    const uint32_t S = p.stages;
-    const uint32_t first = it > S ? it - S : 0;
-    for (uint32_t k = first; k < it; ++k)
-      mbar_wait(smem_addr(&hdr->full[k % S]), (k / S) & 1, 1u << 16);
-    for (uint32_t k = (qcount > 2 ? qcount - 2 : 0); k < qcount; ++k)
-      mbar_wait(smem_addr(&hdr->qfull[k & 1]), (k >> 1) & 1, 1u << 16);
+    for (uint32_t k = ld.it > S ? ld.it - S : 0; k < ld.it; ++k)
+      mbar_wait(smem_addr(&sb.hdr->full[k % S]), (k / S) & 1, 1u << 16);
+    for (uint32_t k = ld.qn > kQSlots ? ld.qn - kQSlots : 0; k < ld.qn; ++k)
+      mbar_wait(smem_addr(&sb.hdr->qfull[k % kQSlots]), (k / kQSlots) & 1, 1u << 16);
   }
 }
 
@@ -534,55 +668,6 @@ __device__ __forceinline__ void tile_fp8(const DecodeParams& p, uint32_t kb,
   pv_fp8<D>(vb, vmax, pb0, pb1, s);
 }
 
-// Two consecutive FP8 tiles of one segment in one step: the QK and PV
-// chains of the two tiles are independent, and one conditional-max check
-// (and, when needed, one cross-lane reduction) covers all 32 tokens.
-template <int D>
-__device__ __forceinline__ void tile_fp8_pair(uint32_t kbA, uint32_t vbA, float4 scA,
-                                              uint32_t kbB, uint32_t vbB, int validB,
-                                              float4 scB,
-                                              const uint32_t (&qb)[D / 16][2],
-                                              float hm0, float hm1, SegState<D>& s) {
-  float xa[4], xb[4];
-  qk_fp8<D>(kbA, kTile, scA, qb, hm0, hm1, xa);
-  qk_fp8<D>(kbB, validB, scB, qb, hm0, hm1, xb);
-  constexpr float kSlack = 8.f;  // as in softmax_tile
-  const float t0 = fmaxf(fmaxf(xa[0], xa[2]), fmaxf(xb[0], xb[2]));
-  const float t1 = fmaxf(fmaxf(xa[1], xa[3]), fmaxf(xb[1], xb[3]));
-  float alpha0 = 1.f, alpha1 = 1.f;
-  if (__any_sync(0xffffffffu, t0 > s.m[0] + kSlack || t1 > s.m[1] + kSlack)) {
-    float mx0 = t0, mx1 = t1;
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-    }
-    const float mn0 = fmaxf(s.m[0], mx0), mn1 = fmaxf(s.m[1], mx1);
-    alpha0 = fast_exp2(s.m[0] - mn0);
-    alpha1 = fast_exp2(s.m[1] - mn1);
-    s.m[0] = mn0;
-    s.m[1] = mn1;
-  }
-  float pa[4], pb[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    pa[q] = fast_exp2(xa[q] - s.m[q & 1]);
-    pb[q] = fast_exp2(xb[q] - s.m[q & 1]);
-  }
-  s.l[0] = s.l[0] * alpha0 + ((pa[0] + pa[2]) + (pb[0] + pb[2]));
-  s.l[1] = s.l[1] * alpha1 + ((pa[1] + pa[3]) + (pb[1] + pb[3]));
-  const float vmaxA = fmaxf(scA.z, scA.w), vmaxB = fmaxf(scB.z, scB.w);
-  const float ra0 = __fdividef(scA.z, vmaxA), ra1 = __fdividef(scA.w, vmaxA);
-  const float rb0 = __fdividef(scB.z, vmaxB), rb1 = __fdividef(scB.w, vmaxB);
-  const uint32_t pbA0 = movmatrix_t(pack_f16x2(pa[0] * ra0, pa[1] * ra0));
-  const uint32_t pbA1 = movmatrix_t(pack_f16x2(pa[2] * ra1, pa[3] * ra1));
-  const uint32_t pbB0 = movmatrix_t(pack_f16x2(pb[0] * rb0, pb[1] * rb0));
-  const uint32_t pbB1 = movmatrix_t(pack_f16x2(pb[2] * rb1, pb[3] * rb1));
-  rescale(s, alpha0, alpha1);
-  pv_fp8<D>(vbA, vmaxA, pbA0, pbA1, s);
-  pv_fp8<D>(vbB, vmaxB, pbB0, pbB1, s);
-}
-
 // d index of accumulator element (i, q) for lane gq.
 template <int D, bool FP8>
 __device__ __forceinline__ int acc_d(int i, int q, int gq) {
@@ -591,138 +676,174 @@ __device__ __forceinline__ int acc_d(int i, int q, int gq) {
   return 16 * i + 2 * gq + (q >> 1);
 }
 
+// Query fragments (B operand, n = head, k = d) from a query slot, and for
+// FP8 the per-head score multipliers hm0 / hm1 (heads 2tq, 2tq + 1).
 template <int D, bool FP8>
-__device__ __forceinline__ void consumer(const DecodeParams& p, Header* hdr,
-                                         uint32_t qbuf, uint32_t ring,
-                                         int64_t lo, int64_t hi,
-                                         int32_t cta) {
+__device__ __forceinline__ void load_query(const DecodeParams& p, uint32_t qslot,
+                                           uint32_t (&qb)[D / 16][2], float& hm0,
+                                           float& hm1) {
   using L = Smem<D, FP8>;
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  Cursor c;
-  locate(p, lo, c);
+  hm0 = hm1 = p.scale_log2;
+  if (!FP8) {
+#pragma unroll
+    for (int kp = 0; kp < D / 32; ++kp) {
+      const int kk = 2 * kp;
+      const int r = lane & 7;
+      const int ch = (kk & 3) * 2 + (lane >> 3);
+      ldsm_x4(qslot + (kk >> 2) * L::kQSlabBytes + r * 128 + ((ch ^ r) << 4),
+              qb[kk][0], qb[kk][1], qb[kk + 1][0], qb[kk + 1][1]);
+    }
+  } else {
+    // q[gq][32ks + 16h + 4tq .. +3] (h = 0, 1) as a two-term E4M3 split
+    // per head: x = q * qs with the power of two qs putting max|x| in
+    // [128, 256); hi = e4m3(x), lo = e4m3(16 (x - hi)); B fragments
+    // qb[2ks][h] = hi, qb[2ks + 1][h] = lo.  The scores are divided by qs.
+    float qv[D / 32][2][4];
+    float amax = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int byte = (32 * ks + 16 * h + 4 * tq) * 2;  // within the row
+        const int slab = byte >> 7, inrow = byte & 127;
+        const int ch = inrow >> 4;
+        const uint32_t addr = qslot + slab * L::kQSlabBytes + gq * 128 +
+                              ((ch ^ gq) << 4) + (inrow & 15);
+        uint32_t w0, w1;
+        asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                     : "=r"(w0), "=r"(w1)
+                     : "r"(addr)
+                     : "memory");
+        const float2 f0 = unpack_bf16x2(w0), f1 = unpack_bf16x2(w1);
+        qv[ks][h][0] = f0.x; qv[ks][h][1] = f0.y; qv[ks][h][2] = f1.x; qv[ks][h][3] = f1.y;
+        amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
+                                 fmaxf(fabsf(f1.x), fabsf(f1.y))));
+      }
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    // amax in [2^(e-1), 2^e) from the exponent field (subnormal or zero
+    // amax clamps to e = -100, which keeps every power of two below normal)
+    int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+    e = max(e, -100);
+    const float qs = __uint_as_float(static_cast<uint32_t>(8 - e + 127) << 23);
+#pragma unroll
+    for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float x[4], r[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) x[k] = qv[ks][h][k] * qs;
+        const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]);
+        const uint32_t h23 = f32x2_to_e4m3x2(x[2], x[3]);
+        const float2 d01 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h01)));
+        const float2 d23 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h23)));
+        r[0] = (x[0] - d01.x) * 16.f;
+        r[1] = (x[1] - d01.y) * 16.f;
+        r[2] = (x[2] - d23.x) * 16.f;
+        r[3] = (x[3] - d23.y) * 16.f;
+        qb[2 * ks][h] = h01 | (h23 << 16);
+        qb[2 * ks + 1][h] = f32x2_to_e4m3x2(r[0], r[1]) | (f32x2_to_e4m3x2(r[2], r[3]) << 16);
+      }
+    const float inv = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(e - 8 + 127) << 23);
+    hm0 = __shfl_sync(0xffffffffu, inv, (2 * tq) * 4);
+    hm1 = __shfl_sync(0xffffffffu, inv, (2 * tq + 1) * 4);
+  }
+}
+
+// Write a finished piece of segment c: the normalised output when the
+// piece is the whole segment, else the unnormalised partial (o, m, l) at
+// piece index cta + b*Hkv + g.
+template <int D, bool FP8>
+__device__ __forceinline__ void finish_piece(const DecodeParams& p, const SegState<D>& s,
+                                             const Cursor& c, bool whole, int32_t cta) {
+  const int lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  float l0 = s.l[0], l1 = s.l[1];
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  const int h0 = 2 * tq, h1 = 2 * tq + 1;
+  if (whole) {
+    const float i0 = 1.f / l0, i1 = 1.f / l1;
+    __nv_bfloat16* ob = p.out + (static_cast<int64_t>(c.b) * p.num_q_heads +
+                                 c.g * p.group) * D;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int h = (q & 1) ? h1 : h0;
+        if (h < p.group)
+          ob[h * D + acc_d<D, FP8>(i, q, gq)] =
+              __float2bfloat16_rn(s.acc[i][q] * ((q & 1) ? i1 : i0));
+      }
+  } else {
+    const int64_t piece = static_cast<int64_t>(cta) + c.b * p.num_kv_heads + c.g;
+    float* wo = p.ws_o + piece * kMaxG * D;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int h = (q & 1) ? h1 : h0;
+        if (h < p.group) wo[h * D + acc_d<D, FP8>(i, q, gq)] = s.acc[i][q];
+      }
+    if (gq == 0) {
+      if (h0 < p.group) p.ws_ml[piece * kMaxG + h0] = make_float2(s.m[0], l0);
+      if (h1 < p.group) p.ws_ml[piece * kMaxG + h1] = make_float2(s.m[1], l1);
+    }
+  }
+}
+
+// The math warp: every tile of [lo, hi), segment by segment.  Single-warp
+// CTAs (kFused) refill the ring themselves after each tile; two-warp CTAs
+// release stages and query slots to the copy warp.  Returns the tiles and
+// query slots consumed.
+template <int D, bool FP8, bool kFused>
+__device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, const Bufs& sb,
+                                         Loader& ld, Cursor c, int64_t lo, int64_t hi,
+                                         int32_t cta, uint32_t& used, uint32_t& qread) {
+  using L = Smem<D, FP8>;
+  Header* hdr = sb.hdr;
+  const int lane = threadIdx.x & 31;
   int64_t u = lo;
-  uint32_t it = 0, qcount = 0;
+  used = qread = 0;
   bool ok = true;
   SegState<D> s;
   uint32_t qb[D / 16][2];
+  float hm0, hm1;
+  if (kFused) top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
   while (u < hi && ok) {
     const int32_t seg_end = static_cast<int32_t>(
         min(static_cast<int64_t>(c.T), c.tile + (hi - u)));
     const bool whole = c.tile == 0 && seg_end == c.T;
-    // ---- query fragments (B operand, n = head, k = d)
-    const uint32_t qslot = qbuf + (qcount & 1) * L::kQBytes;
-    ok = mbar_wait(smem_addr(&hdr->qfull[qcount & 1]), (qcount >> 1) & 1);
+    const uint32_t qs = qread % kQSlots;
+    ok = mbar_wait(smem_addr(&hdr->qfull[qs]), (qread / kQSlots) & 1);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
-    float hm0 = p.scale_log2, hm1 = p.scale_log2;
-    if (!FP8) {
-#pragma unroll
-      for (int kp = 0; kp < D / 32; ++kp) {
-        const int kk = 2 * kp;
-        const int r = lane & 7;
-        const int ch = (kk & 3) * 2 + (lane >> 3);
-        ldsm_x4(qslot + (kk >> 2) * L::kQSlabBytes + r * 128 + ((ch ^ r) << 4),
-                qb[kk][0], qb[kk][1], qb[kk + 1][0], qb[kk + 1][1]);
-      }
-    } else {
-      // q[gq][32ks + 16h + 4tq .. +3] (h = 0, 1) as a two-term E4M3 split
-      // per head: x = q * qs with the power of two qs putting max|x| in
-      // [128, 256); hi = e4m3(x), lo = e4m3(16 (x - hi)); B fragments
-      // qb[2ks][h] = hi, qb[2ks + 1][h] = lo.  The scores are divided by qs.
-      float qv[D / 32][2][4];
-      float amax = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < D / 32; ++ks)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int byte = (32 * ks + 16 * h + 4 * tq) * 2;  // within the row
-          const int slab = byte >> 7, inrow = byte & 127;
-          const int ch = inrow >> 4;
-          const uint32_t addr = qslot + slab * L::kQSlabBytes + gq * 128 +
-                                ((ch ^ gq) << 4) + (inrow & 15);
-          uint32_t w0, w1;
-          asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
-                       : "=r"(w0), "=r"(w1)
-                       : "r"(addr)
-                       : "memory");
-          const float2 f0 = unpack_bf16x2(w0), f1 = unpack_bf16x2(w1);
-          qv[ks][h][0] = f0.x; qv[ks][h][1] = f0.y; qv[ks][h][2] = f1.x; qv[ks][h][3] = f1.y;
-          amax = fmaxf(amax, fmaxf(fmaxf(fabsf(f0.x), fabsf(f0.y)),
-                                   fmaxf(fabsf(f1.x), fabsf(f1.y))));
-        }
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      // amax in [2^(e-1), 2^e) from the exponent field (subnormal or zero
-      // amax clamps to e = -100, which keeps every power of two below normal)
-      int e = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 126;
-      e = max(e, -100);
-      const float qs = __uint_as_float(static_cast<uint32_t>(8 - e + 127) << 23);
-#pragma unroll
-      for (int ks = 0; ks < D / 32; ++ks)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          float x[4], r[4];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) x[k] = qv[ks][h][k] * qs;
-          const uint32_t h01 = f32x2_to_e4m3x2(x[0], x[1]);
-          const uint32_t h23 = f32x2_to_e4m3x2(x[2], x[3]);
-          const float2 d01 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h01)));
-          const float2 d23 = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(h23)));
-          r[0] = (x[0] - d01.x) * 16.f;
-          r[1] = (x[1] - d01.y) * 16.f;
-          r[2] = (x[2] - d23.x) * 16.f;
-          r[3] = (x[3] - d23.y) * 16.f;
-          qb[2 * ks][h] = h01 | (h23 << 16);
-          qb[2 * ks + 1][h] = f32x2_to_e4m3x2(r[0], r[1]) | (f32x2_to_e4m3x2(r[2], r[3]) << 16);
-        }
-      const float inv = p.scale_log2 * __uint_as_float(static_cast<uint32_t>(e - 8 + 127) << 23);
-      hm0 = __shfl_sync(0xffffffffu, inv, (2 * tq) * 4);
-      hm1 = __shfl_sync(0xffffffffu, inv, (2 * tq + 1) * 4);
-    }
+    load_query<D, FP8>(p, sb.q + qs * L::kQBytes, qb, hm0, hm1);
+    ++qread;
     __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&hdr->qempty[qcount & 1]));
-    ++qcount;
+    if (kFused) {
+      top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
+    } else if (lane == 0) {
+      mbar_arrive(smem_addr(&hdr->qempty[qs]));
+    }
     seg_reset(s);
-    // ---- tiles
     for (int32_t tile = c.tile; tile < seg_end; ++tile) {
-      if (FP8 && tile + 1 < seg_end) {
-        // Two full-or-tail tiles in one step (the first is never a tail).
-        const uint32_t sA = it % p.stages, sB = (it + 1) % p.stages;
-        ok = mbar_wait(smem_addr(&hdr->full[sA]), (it / p.stages) & 1);
-        ok = ok && mbar_wait(smem_addr(&hdr->full[sB]), ((it + 1) / p.stages) & 1);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        const uint32_t kbA = ring + sA * L::kStageBytes, kbB = ring + sB * L::kStageBytes;
-        const int validB = min(kTile, c.n - (tile + 1) * kTile);
-        if (validB < kTile) {
-          for (int off = validB * D + lane * 16; off < kTile * D; off += 32 * 16)
-            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(kbB + L::kKVBytes + off), "r"(0)
-                         : "memory");
-          fence_proxy_async_smem();
-          __syncwarp();
-        }
-        tile_fp8_pair<D>(kbA, kbA + L::kKVBytes, hdr->scales[sA], kbB, kbB + L::kKVBytes,
-                         validB, hdr->scales[sB], qb, hm0, hm1, s);
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_addr(&hdr->empty[sA]));
-          mbar_arrive(smem_addr(&hdr->empty[sB]));
-        }
-        it += 2;
-        ++tile;
-        continue;
-      }
-      const uint32_t stage = it % p.stages;
-      ok = mbar_wait(smem_addr(&hdr->full[stage]), (it / p.stages) & 1);
+      const uint32_t stage = used % p.stages;
+      ok = mbar_wait(smem_addr(&hdr->full[stage]), (used / p.stages) & 1);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      const uint32_t kb = ring + stage * L::kStageBytes;
+      const uint32_t kb = sb.ring + stage * L::kStageBytes;
       const uint32_t vb = kb + L::kKVBytes;
       const int valid = min(kTile, c.n - tile * kTile);
       if (valid < kTile) {
         // Rows past the sequence end hold stale or foreign data: zero the V
         // rows (0 * NaN would poison the MMA); K rows are masked by -inf.
+        // The proxy fence orders these writes before the stage's next copy.
         const int row_bytes = FP8 ? D : 128;
         for (int sl = 0; sl < L::kSlabs; ++sl)
           for (int off = valid * row_bytes + lane * 16; off < kTile * row_bytes; off += 32 * 16)
@@ -736,82 +857,79 @@ __device__ __forceinline__ void consumer(const DecodeParams& p, Header* hdr,
       } else {
         tile_fp8<D>(p, kb, vb, valid, hdr->scales[stage], qb, hm0, hm1, s);
       }
+      ++used;
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&hdr->empty[stage]));
-      ++it;
-    }
-    if (!ok) break;
-    // ---- finalise the piece
-    float l0 = s.l[0], l1 = s.l[1];
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    const int h0 = 2 * tq, h1 = 2 * tq + 1;
-    if (whole) {
-      const float i0 = 1.f / l0, i1 = 1.f / l1;
-      __nv_bfloat16* ob = p.out + (static_cast<int64_t>(c.b) * p.num_q_heads +
-                                   c.g * p.group) * D;
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int h = (q & 1) ? h1 : h0;
-          if (h < p.group)
-            ob[h * D + acc_d<D, FP8>(i, q, gq)] =
-                __float2bfloat16_rn(s.acc[i][q] * ((q & 1) ? i1 : i0));
-        }
-    } else {
-      const int64_t piece = static_cast<int64_t>(cta) + c.b * p.num_kv_heads + c.g;
-      float* wo = p.ws_o + piece * kMaxG * D;
-#pragma unroll
-      for (int i = 0; i < D / 16; ++i)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int h = (q & 1) ? h1 : h0;
-          if (h < p.group) wo[h * D + acc_d<D, FP8>(i, q, gq)] = s.acc[i][q];
-        }
-      if (gq == 0) {
-        if (h0 < p.group) p.ws_ml[piece * kMaxG + h0] = make_float2(s.m[0], l0);
-        if (h1 < p.group) p.ws_ml[piece * kMaxG + h1] = make_float2(s.m[1], l1);
+      if (kFused) {
+        top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
+      } else if (lane == 0) {
+        mbar_arrive(smem_addr(&hdr->empty[stage]));
       }
     }
+    if (!ok) break;
+    finish_piece<D, FP8>(p, s, c, whole, cta);
     u += seg_end - c.tile;
     if (u < hi) next_segment(p, c);
   }
 }
 
+// ------------------------------------------------------------- kernels ---
+// Kernel shape per instantiation, from measurement: bf16 tiles stream at
+// the HBM rate when a copy warp sits beside each math warp (the TMA issue
+// stalls land on the copy warp); FP8's heavier math wants every warp
+// computing, so its CTAs are single warps that issue their own copies.
 template <int D, bool FP8>
-__global__ void __launch_bounds__(64)
-    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
-                        const __grid_constant__ CUtensorMap tm_k,
-                        const __grid_constant__ CUtensorMap tm_v,
-                        const DecodeParams p) {
-  using L = Smem<D, FP8>;
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Header* hdr = reinterpret_cast<Header*>(smem_raw);
-  const uint32_t base = smem_addr(smem_raw);
-  // Swizzled TMA boxes need 1024-byte aligned destinations; the dynamic
-  // shared window is expected to start aligned.  Check rather than assume.
-  if (base & 1023u) {
-    if (threadIdx.x == 0) flag_error(PA_DEVERR_LAUNCH);
-    return;
-  }
-  const uint32_t tiles = base + L::kHeaderBytes;
-  const uint32_t qbuf = tiles;
-  const uint32_t ring = tiles + 2 * L::kQBytes;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
+struct DecodeShape {
+  static constexpr bool kTwoWarps = !FP8;
+  static constexpr int kThreads = kTwoWarps ? 64 : 32;
+};
 
+// Shared-memory carve-up; false if the window is not 1024-aligned (the
+// swizzled TMA boxes need it) or the ring depth is out of range.
+template <int D, bool FP8>
+__device__ __forceinline__ bool carve(const DecodeParams& p, uint8_t* smem_raw, Bufs& sb) {
+  using L = Smem<D, FP8>;
+  const uint32_t base = smem_addr(smem_raw);
+  if ((base & 1023u) || p.stages < 1 || p.stages > kMaxStages) {
+    if (threadIdx.x == 0) flag_error(PA_DEVERR_LAUNCH);
+    return false;
+  }
+  sb.q = base;
+  sb.ring = base + kQSlots * L::kQBytes;
+  sb.hdr = reinterpret_cast<Header*>(smem_raw + kQSlots * L::kQBytes + p.stages * L::kStageBytes);
+  return true;
+}
+
+// This CTA's range [lo, hi) of the flat tile list; false if it has none.
+// With fewer tiles than CTAs only the first W CTAs take part, so that
+// every participating CTA owns at least one tile (the merge relies on it).
+__device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& lo, int64_t& hi) {
+  const int64_t W = total_tiles(p);
+  if (W == 0) return false;
+  const int32_t P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
+  if (static_cast<int32_t>(blockIdx.x) >= P) return false;
+  cta_range(W, P, blockIdx.x, lo, hi);
+  return true;
+}
+
+// Two warps: warp 0 copies, warp 1 computes.
+template <int D, bool FP8>
+__global__ void __launch_bounds__(64, 8)
+    paged_decode_ws_kernel(const __grid_constant__ CUtensorMap tm_q,
+                           const __grid_constant__ CUtensorMap tm_k,
+                           const __grid_constant__ CUtensorMap tm_v,
+                           const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Bufs sb;
+  if (!carve<D, FP8>(p, smem_raw, sb)) return;
+  const Maps tm{&tm_q, &tm_k, &tm_v};
   if (threadIdx.x == 0) {
-    for (int s = 0; s < p.stages; ++s) {
-      mbar_init(smem_addr(&hdr->full[s]), 1);
-      mbar_init(smem_addr(&hdr->empty[s]), 1);
+    for (int st = 0; st < p.stages; ++st) {
+      mbar_init(smem_addr(&sb.hdr->full[st]), 1);
+      mbar_init(smem_addr(&sb.hdr->empty[st]), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(smem_addr(&hdr->qfull[s]), 1);
-      mbar_init(smem_addr(&hdr->qempty[s]), 1);
+    for (int st = 0; st < kQSlots; ++st) {
+      mbar_init(smem_addr(&sb.hdr->qfull[st]), 1);
+      mbar_init(smem_addr(&sb.hdr->qempty[st]), 1);
     }
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
@@ -819,45 +937,89 @@ __global__ void __launch_bounds__(64)
     tma_prefetch_desc(&tm_v);
   }
   __syncthreads();
-
-  int64_t W = total_tiles(p);  // both warps compute it; identical
-  if (W == 0) return;
-  // With fewer tiles than CTAs only the first W CTAs take part, so that
-  // every participating CTA owns at least one tile (the merge relies on it).
-  const int32_t P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
-  if (static_cast<int32_t>(blockIdx.x) >= P) return;
+  // Launched as a programmatic dependent: nothing above reads an input;
+  // wait for the previous grid before anything below does.
+  pdl_wait();
+  pdl_trigger();
   int64_t lo, hi;
-  cta_range(W, P, blockIdx.x, lo, hi);
-  if (warp == 0)
-    producer<D, FP8>(p, &tm_q, &tm_k, &tm_v, hdr, qbuf, ring, lo, hi);
-  else
-    consumer<D, FP8>(p, hdr, qbuf, ring, lo, hi, blockIdx.x);
-  (void)lane;
+  if (!my_range(p, lo, hi)) return;
+  Loader ld;
+  loader_init(p, lo, hi, ld);
+  if (threadIdx.x < 32) {
+    produce<D, FP8>(p, tm, sb, ld, hi);
+  } else {
+    uint32_t used, qread;
+    run_math<D, FP8, false>(p, tm, sb, ld, ld.c, lo, hi, blockIdx.x, used, qread);
+  }
+}
+
+// One warp that issues its own copies between tiles.
+template <int D, bool FP8>
+__global__ void __launch_bounds__(32, 16)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v,
+                        const DecodeParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  Bufs sb;
+  if (!carve<D, FP8>(p, smem_raw, sb)) return;
+  const Maps tm{&tm_q, &tm_k, &tm_v};
+  const int lane = threadIdx.x & 31;
+  if (lane == 0) {
+    for (int st = 0; st < p.stages; ++st) mbar_init(smem_addr(&sb.hdr->full[st]), 1);
+    for (int st = 0; st < kQSlots; ++st) mbar_init(smem_addr(&sb.hdr->qfull[st]), 1);
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  __syncwarp();
+  pdl_wait();  // as in the two-warp kernel
+  pdl_trigger();
+  int64_t lo, hi;
+  if (!my_range(p, lo, hi)) return;
+  Loader ld;
+  loader_init(p, lo, hi, ld);
+  uint32_t used, qread;
+  run_math<D, FP8, true>(p, tm, sb, ld, ld.c, lo, hi, blockIdx.x, used, qread);
+  // No copy may still target shared memory when the CTA exits.  On the
+  // normal path every issued copy has been waited for already.
+  if (lane == 0) {
+    const uint32_t S = p.stages;
+    for (uint32_t k = used; k < ld.it; ++k)
+      mbar_wait(smem_addr(&sb.hdr->full[k % S]), (k / S) & 1, 1u << 16);
+    for (uint32_t k = qread; k < ld.qn; ++k)
+      mbar_wait(smem_addr(&sb.hdr->qfull[k % kQSlots]), (k / kQSlots) & 1, 1u << 16);
+  }
 }
 
 // ----------------------------------------------------------------- merge --
-// One CTA per segment (b, g).  Empty sequences get zeros; segments covered
-// by a single CTA were written by the decode kernel; split segments combine
-// their pieces:  M = max_j m_j,  out = sum_j 2^(m_j - M) o_j /
-// sum_j 2^(m_j - M) l_j.
+// One CTA per segment (b, g), thread (h, d4) owns 4 output columns of head
+// h.  Empty sequences get zeros; segments covered by a single CTA were
+// written by the decode kernel; split segments combine their pieces:
+//   M = max_j m_j,  out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
+// The loads over pieces are independent, so several are kept in flight.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kMaxG * D / 4)
     paged_decode_merge_kernel(const DecodeParams p) {
+  pdl_wait();  // the decode grid's partials are complete and visible
   const int32_t seg = blockIdx.x;
   const int32_t b = seg / p.num_kv_heads, g = seg % p.num_kv_heads;
   __shared__ int64_t s_before;
   __shared__ int64_t s_W;
+  const int h = threadIdx.x / (D / 4);
+  const int d4 = (threadIdx.x % (D / 4)) * 4;
   const int32_t n = clamp_len(p, p.seq_lens[b]);
   const int32_t T = cdiv16(n);
   __nv_bfloat16* ob = p.out + (static_cast<int64_t>(b) * p.num_q_heads + g * p.group) * D;
   if (T == 0) {
-    for (int i = threadIdx.x; i < p.group * D; i += blockDim.x)
-      ob[i] = __float2bfloat16_rn(0.f);
+    if (h < p.group) *reinterpret_cast<uint2*>(ob + h * D + d4) = make_uint2(0u, 0u);
     return;
   }
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int64_t before = 0, all = 0;
+#pragma unroll 4
     for (int32_t bb = lane; bb < p.num_seqs; bb += 32) {
       const int64_t t = cdiv16(clamp_len(p, p.seq_lens[bb]));
       all += t;
@@ -879,22 +1041,32 @@ __global__ void __launch_bounds__(256)
   const int32_t P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
   const int32_t c0 = cta_of(W, P, start);
   const int32_t c1 = cta_of(W, P, start + T - 1);
-  if (c0 == c1) return;
-  const int64_t pbase = static_cast<int64_t>(seg);
-  for (int idx = threadIdx.x; idx < p.group * D; idx += blockDim.x) {
-    const int h = idx / D;
-    float M = -INFINITY;
-    for (int32_t c = c0; c <= c1; ++c)
-      M = fmaxf(M, p.ws_ml[(pbase + c) * kMaxG + h].x);
-    float num = 0.f, den = 0.f;
-    for (int32_t c = c0; c <= c1; ++c) {
-      const float2 ml = p.ws_ml[(pbase + c) * kMaxG + h];
-      const float w = fast_exp2(ml.x - M);
-      num = fmaf(w, p.ws_o[(pbase + c) * kMaxG * D + idx], num);
-      den = fmaf(w, ml.y, den);
-    }
-    ob[idx] = __float2bfloat16_rn(num / den);
+  if (c0 == c1 || h >= p.group) return;
+  const int np = c1 - c0 + 1;
+  const int64_t first = static_cast<int64_t>(seg) + c0;  // piece index of c0
+  const float2* ml = p.ws_ml + first * kMaxG + h;
+  const float4* o = reinterpret_cast<const float4*>(p.ws_o + (first * kMaxG + h) * D + d4);
+  constexpr int kOStride = kMaxG * D / 4;  // float4s per piece
+  float M = -INFINITY;
+#pragma unroll 8
+  for (int k = 0; k < np; ++k) M = fmaxf(M, ml[k * kMaxG].x);
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll 4
+  for (int k = 0; k < np; ++k) {
+    const float2 v = ml[k * kMaxG];
+    const float4 x = o[k * kOStride];
+    const float w = fast_exp2(v.x - M);
+    num.x = fmaf(w, x.x, num.x);
+    num.y = fmaf(w, x.y, num.y);
+    num.z = fmaf(w, x.z, num.z);
+    num.w = fmaf(w, x.w, num.w);
+    den = fmaf(w, v.y, den);
   }
+  uint2 r;
+  r.x = pack_bf16x2(num.x / den, num.y / den);
+  r.y = pack_bf16x2(num.z / den, num.w / den);
+  *reinterpret_cast<uint2*>(ob + h * D + d4) = r;
 }
 
 }  // namespace pa

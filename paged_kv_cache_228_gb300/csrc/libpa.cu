@@ -93,45 +93,57 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base,
   return r == CUDA_SUCCESS;
 }
 
-// Decode launch plan for one (head_dim, dtype) instantiation.
-constexpr int kTargetCtasPerSm = 8;
+// Decode launch plan for one (head_dim, dtype) instantiation: as many CTAs
+// of its shape per SM as registers allow up to kMaxCtasPerSm, each with the
+// deepest stage ring that lets that many share the SM's shared memory.
+constexpr int kMaxCtasPerSm = 16;
 constexpr size_t kSmemPerSm = 228 * 1024;
 constexpr size_t kSmemReservedPerCta = 1024;
 
+using DecodeFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeParams);
+
 template <int D, bool FP8>
-struct Plan {
-  using L = Smem<D, FP8>;
-  static int stages() {
-    const size_t per_cta = kSmemPerSm / kTargetCtasPerSm - kSmemReservedPerCta;
-    const size_t fixed = L::kHeaderBytes + 2 * L::kQBytes;
-    int s = static_cast<int>((per_cta - fixed) / L::kStageBytes);
-    if (s < 2) s = 2;
-    if (s > L::kMaxStages) s = L::kMaxStages;
-    return s;
-  }
-  static size_t smem_bytes(int s) {
-    return L::kHeaderBytes + 2 * L::kQBytes + static_cast<size_t>(s) * L::kStageBytes;
-  }
+DecodeFn decode_fn() {
+  return DecodeShape<D, FP8>::kTwoWarps ? paged_decode_ws_kernel<D, FP8>
+                                        : paged_decode_kernel<D, FP8>;
+}
+
+struct DecodePlan {
+  int ctas_per_sm = 0;
+  int stages = 0;
 };
 
 template <int D, bool FP8>
-pa_status decode_ctas_per_sm(int dev, int stages, int* out) {
-  static int cached[kMaxDevices] = {0};
+pa_status decode_plan(int dev, DecodePlan* out) {
+  using L = Smem<D, FP8>;
+  static DecodePlan cached[kMaxDevices];
   std::lock_guard<std::mutex> lk(g_mu);
-  if (cached[dev] == 0) {
-    const size_t smem = Plan<D, FP8>::smem_bytes(stages);
-    if (cudaFuncSetAttribute(paged_decode_kernel<D, FP8>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+  DecodePlan& pl = cached[dev];
+  if (pl.ctas_per_sm == 0) {
+    const DecodeFn fn = decode_fn<D, FP8>();
+    const int threads = DecodeShape<D, FP8>::kThreads;
+    // CTAs per SM that registers (and the thread/CTA limits) allow
+    int by_regs = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&by_regs, fn, threads, 0) != cudaSuccess)
+      return PA_ERR_CUDA;
+    const int want = by_regs < kMaxCtasPerSm ? by_regs : kMaxCtasPerSm;
+    if (want < 1) return PA_ERR_UNSUPPORTED;
+    const size_t per_cta = kSmemPerSm / want - kSmemReservedPerCta;
+    int s = static_cast<int>((per_cta - decode_smem_bytes<D, FP8>(0)) / L::kStageBytes);
+    if (s < 2) s = 2;
+    if (s > kMaxStages) s = kMaxStages;
+    const size_t smem = decode_smem_bytes<D, FP8>(s);
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PA_ERR_CUDA;
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &n, paged_decode_kernel<D, FP8>, 64, smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess)
       return PA_ERR_CUDA;
     if (n < 1) return PA_ERR_UNSUPPORTED;
-    cached[dev] = n;
+    pl.stages = s;
+    pl.ctas_per_sm = n;
   }
-  *out = cached[dev];
+  *out = pl;
   return PA_OK;
 }
 
@@ -145,15 +157,14 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
                         const void* k_cache, const void* v_cache,
                         void* workspace, size_t workspace_bytes,
                         int32_t num_splits, cudaStream_t stream) {
-  using L = Smem<D, FP8>;
   int sms = 0, dev = 0;
   pa_status st = device_sms(&sms, &dev);
   if (st != PA_OK) return st;
-  const int stages = Plan<D, FP8>::stages();
-  int per_sm = 0;
-  st = decode_ctas_per_sm<D, FP8>(dev, stages, &per_sm);
+  DecodePlan plan;
+  st = decode_plan<D, FP8>(dev, &plan);
   if (st != PA_OK) return st;
-  const int32_t P = num_splits > 0 ? num_splits : sms * per_sm;
+  const int stages = plan.stages;
+  const int32_t P = num_splits > 0 ? num_splits : sms * plan.ctas_per_sm;
   const int64_t segs = static_cast<int64_t>(prm_in.num_seqs) * prm_in.num_kv_heads;
   const size_t need = P > 1 ? workspace_bytes_for(P + segs, D) : 0;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
@@ -191,13 +202,27 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
                    CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
   }
-  const size_t smem = Plan<D, FP8>::smem_bytes(stages);
-  (void)L::kStageBytes;
-  paged_decode_kernel<D, FP8><<<P, 64, smem, stream>>>(tq, tk, tv, prm);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  // Both grids are programmatic dependents of the work before them in the
+  // stream: each launches early and waits on the device (griddepcontrol)
+  // before it reads anything, which hides the launch gaps.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(P));
+  cfg.blockDim = dim3(DecodeShape<D, FP8>::kThreads);
+  cfg.dynamicSmemBytes = decode_smem_bytes<D, FP8>(stages);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, decode_fn<D, FP8>(), tq, tk, tv, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
   if (segs > 0) {
-    paged_decode_merge_kernel<D><<<static_cast<unsigned>(segs), 256, 0, stream>>>(prm);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    cfg.gridDim = dim3(static_cast<unsigned>(segs));
+    cfg.blockDim = dim3(kMaxG * D / 4);
+    cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D>, prm) != cudaSuccess)
+      return PA_ERR_CUDA;
   }
   return PA_OK;
 }
@@ -319,18 +344,19 @@ pa_status auto_ctas(int32_t head_dim, pa_kv_dtype dt, int32_t* out) {
   int sms = 0, dev = 0;
   pa_status st = device_sms(&sms, &dev);
   if (st != PA_OK) return st;
-  int per = 0;
+  DecodePlan pl;
   if (dt == PA_KV_BF16 && head_dim == 128)
-    st = decode_ctas_per_sm<128, false>(dev, Plan<128, false>::stages(), &per);
+    st = decode_plan<128, false>(dev, &pl);
   else if (dt == PA_KV_BF16 && head_dim == 64)
-    st = decode_ctas_per_sm<64, false>(dev, Plan<64, false>::stages(), &per);
+    st = decode_plan<64, false>(dev, &pl);
   else if (dt == PA_KV_FP8_E4M3 && head_dim == 128)
-    st = decode_ctas_per_sm<128, true>(dev, Plan<128, true>::stages(), &per);
+    st = decode_plan<128, true>(dev, &pl);
   else if (dt == PA_KV_FP8_E4M3 && head_dim == 64)
-    st = decode_ctas_per_sm<64, true>(dev, Plan<64, true>::stages(), &per);
+    st = decode_plan<64, true>(dev, &pl);
   else
     return PA_ERR_UNSUPPORTED;
   if (st != PA_OK) return st;
+  const int per = pl.ctas_per_sm;
   *out = sms * per;
   return PA_OK;
 }

@@ -73,6 +73,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
   return false;
 }
 
+// Programmatic dependent launch.  pdl_wait blocks until the grid this one
+// depends on has completed and its memory is visible (a no-op for a grid
+// launched without the dependency); pdl_trigger lets the next grid in the
+// stream begin launching.
+__device__ __forceinline__ void pdl_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Generic-proxy shared-memory writes must be ordered before later
 // async-proxy (TMA) writes to the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -80,6 +91,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // ------------------------------------------------------------------ TMA ---
+// 2D tiled TMA load of one box into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map,
                                             int32_t x, int32_t y,
                                             uint32_t bar) {
