@@ -414,6 +414,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--fp8", action="store_true",
                     help="with --profile: run the FP8 cache path of the workload")
+    ap.add_argument("--num-seqs", type=int, default=None,
+                    help="with --profile: a smaller batch of the 128K workload "
+                         "(ncu captures that must stay a few GB)")
     ap.add_argument("--profile", action="store_true",
                     help="only the warm-up and timed steps of the main workload "
                          "(for ncu captures); prints the step time")
@@ -422,7 +425,12 @@ def main():
         ap.error("--warmup must be >= 3")
 
     from paged_kv_cache_228_gb300 import workloads as W
-    w = W.WORKLOADS[args.workload]()
+    if args.num_seqs is not None:
+        if not args.profile or args.workload != "llama3.1-70b-128k":
+            ap.error("--num-seqs only goes with --profile --workload llama3.1-70b-128k")
+        w = W.llama31_70b_128k(num_seqs=args.num_seqs)
+    else:
+        w = W.WORKLOADS[args.workload]()
     if args.impl == "reference":
         run_reference(args, w)
         return
@@ -514,10 +522,11 @@ def main():
             "graph_us_per_step": (res["graph_ms_per_step"] * 1e3
                                   if isinstance(res["graph_ms_per_step"], float)
                                   else res["graph_ms_per_step"]),
-            "host_block_manager_us_per_append": res["host_append_us"],
+            "host_block_manager_us_per_step": res["host_append_us"],
+            "host_block_manager_us_per_append": res["host_append_us"] / w.num_seqs,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                         "kernel": "paged_decode_kernel<128,bf16> + merge (per launch pair)",
+                         "kernel": "paged_decode_ws_kernel<128,bf16> + merge (per launch pair)",
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": nbytes / (e2e["ms_per_step"] / 1e3) / 1e9, "unit": "GB/s",

@@ -20,6 +20,10 @@ __global__ void __launch_bounds__(256)
                        uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
                        int64_t num_slots, int32_t num_kv_heads,
                        int32_t block_size, int32_t chunks_per_row) {
+  // Launched as a programmatic dependent: wait for the previous grid
+  // before reading any input, then let the next grid begin launching.
+  pdl_wait();
+  pdl_trigger();
   const int64_t per_token = 2LL * num_kv_heads * chunks_per_row;
   const int64_t total = per_token * num_tokens;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;

@@ -59,6 +59,8 @@ struct DecodeParams {
   __nv_bfloat16* out;
   float* ws_o;    // [pieces][kMaxG][D] unnormalised partial outputs
   float2* ws_ml;  // [pieces][kMaxG] (running max in log2 units, sum)
+  int2* ws_job;   // [P]: (segment, first CTA) of the split segment that
+                  // CTA finishes, else (-1, -1)
   int32_t num_seqs, num_q_heads, num_kv_heads, group, block_size, log2_bs;
   int32_t max_blocks, num_blocks;
   int32_t rows_total;  // num_blocks * num_kv_heads * block_size
@@ -803,8 +805,9 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, const SegSta
 // query slots consumed.
 template <int D, bool FP8, bool kFused>
 __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, const Bufs& sb,
-                                         Loader& ld, Cursor c, int64_t lo, int64_t hi,
-                                         int32_t cta, uint32_t& used, uint32_t& qread) {
+                                         Loader& ld, Cursor c, int64_t W, int32_t P,
+                                         int64_t lo, int64_t hi, int32_t cta, uint32_t& used,
+                                         uint32_t& qread) {
   using L = Smem<D, FP8>;
   Header* hdr = sb.hdr;
   const int lane = threadIdx.x & 31;
@@ -867,6 +870,11 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
     }
     if (!ok) break;
     finish_piece<D, FP8>(p, s, c, whole, cta);
+    // The CTA that finishes a split segment hands its merge to the merge
+    // kernel's CTA of the same index (at most one per CTA: only the first
+    // segment of a range can have started in an earlier CTA).
+    if (!whole && seg_end == c.T && lane == 0)
+      p.ws_job[cta] = make_int2(c.b * p.num_kv_heads + c.g, cta_of(W, P, u - c.tile));
     u += seg_end - c.tile;
     if (u < hi) next_segment(p, c);
   }
@@ -899,13 +907,17 @@ __device__ __forceinline__ bool carve(const DecodeParams& p, uint8_t* smem_raw, 
   return true;
 }
 
-// This CTA's range [lo, hi) of the flat tile list; false if it has none.
-// With fewer tiles than CTAs only the first W CTAs take part, so that
-// every participating CTA owns at least one tile (the merge relies on it).
-__device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& lo, int64_t& hi) {
-  const int64_t W = total_tiles(p);
+// This CTA's range [lo, hi) of the flat tile list (W tiles over P
+// participating CTAs); false if it has none.  With fewer tiles than CTAs
+// only the first W CTAs take part, so that every participating CTA owns at
+// least one tile.  The math warp's lane 0 first clears the CTA's merge job.
+__device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& W, int32_t& P,
+                                         int64_t& lo, int64_t& hi) {
+  if (p.ws_job != nullptr && threadIdx.x == blockDim.x - 32)
+    p.ws_job[blockIdx.x] = make_int2(-1, -1);
+  W = total_tiles(p);
   if (W == 0) return false;
-  const int32_t P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
+  P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
   if (static_cast<int32_t>(blockIdx.x) >= P) return false;
   cta_range(W, P, blockIdx.x, lo, hi);
   return true;
@@ -941,15 +953,16 @@ __global__ void __launch_bounds__(64, 8)
   // wait for the previous grid before anything below does.
   pdl_wait();
   pdl_trigger();
-  int64_t lo, hi;
-  if (!my_range(p, lo, hi)) return;
+  int64_t W, lo, hi;
+  int32_t P;
+  if (!my_range(p, W, P, lo, hi)) return;
   Loader ld;
   loader_init(p, lo, hi, ld);
   if (threadIdx.x < 32) {
     produce<D, FP8>(p, tm, sb, ld, hi);
   } else {
     uint32_t used, qread;
-    run_math<D, FP8, false>(p, tm, sb, ld, ld.c, lo, hi, blockIdx.x, used, qread);
+    run_math<D, FP8, false>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used, qread);
   }
 }
 
@@ -976,12 +989,13 @@ __global__ void __launch_bounds__(32, 16)
   __syncwarp();
   pdl_wait();  // as in the two-warp kernel
   pdl_trigger();
-  int64_t lo, hi;
-  if (!my_range(p, lo, hi)) return;
+  int64_t W, lo, hi;
+  int32_t P;
+  if (!my_range(p, W, P, lo, hi)) return;
   Loader ld;
   loader_init(p, lo, hi, ld);
   uint32_t used, qread;
-  run_math<D, FP8, true>(p, tm, sb, ld, ld.c, lo, hi, blockIdx.x, used, qread);
+  run_math<D, FP8, true>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used, qread);
   // No copy may still target shared memory when the CTA exits.  On the
   // normal path every issued copy has been waited for already.
   if (lane == 0) {
@@ -994,54 +1008,32 @@ __global__ void __launch_bounds__(32, 16)
 }
 
 // ----------------------------------------------------------------- merge --
-// One CTA per segment (b, g), thread (h, d4) owns 4 output columns of head
-// h.  Empty sequences get zeros; segments covered by a single CTA were
-// written by the decode kernel; split segments combine their pieces:
+// Launched with one CTA per decode CTA.  Zeroes the output of empty
+// sequences (one thread per sequence), then CTA c merges the split segment
+// decode CTA c finished, if any: thread (h, d4) owns 4 output columns of
+// head h, and over the segment's pieces j
 //   M = max_j m_j,  out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
 // The loads over pieces are independent, so several are kept in flight.
 template <int D>
 __global__ void __launch_bounds__(kMaxG * D / 4)
     paged_decode_merge_kernel(const DecodeParams p) {
   pdl_wait();  // the decode grid's partials are complete and visible
-  const int32_t seg = blockIdx.x;
+  for (int32_t bb = blockIdx.x * blockDim.x + threadIdx.x; bb < p.num_seqs;
+       bb += gridDim.x * blockDim.x) {
+    if (clamp_len(p, p.seq_lens[bb]) == 0) {
+      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(bb) * p.num_q_heads * D);
+      for (int i = 0; i < p.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  if (p.ws_job == nullptr) return;
+  const int2 job = p.ws_job[blockIdx.x];
+  if (job.x < 0) return;
+  const int32_t seg = job.x, c0 = job.y, c1 = blockIdx.x;
   const int32_t b = seg / p.num_kv_heads, g = seg % p.num_kv_heads;
-  __shared__ int64_t s_before;
-  __shared__ int64_t s_W;
   const int h = threadIdx.x / (D / 4);
   const int d4 = (threadIdx.x % (D / 4)) * 4;
-  const int32_t n = clamp_len(p, p.seq_lens[b]);
-  const int32_t T = cdiv16(n);
+  if (h >= p.group) return;
   __nv_bfloat16* ob = p.out + (static_cast<int64_t>(b) * p.num_q_heads + g * p.group) * D;
-  if (T == 0) {
-    if (h < p.group) *reinterpret_cast<uint2*>(ob + h * D + d4) = make_uint2(0u, 0u);
-    return;
-  }
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int64_t before = 0, all = 0;
-#pragma unroll 4
-    for (int32_t bb = lane; bb < p.num_seqs; bb += 32) {
-      const int64_t t = cdiv16(clamp_len(p, p.seq_lens[bb]));
-      all += t;
-      if (bb < b) before += t;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      before += __shfl_xor_sync(0xffffffffu, before, o);
-      all += __shfl_xor_sync(0xffffffffu, all, o);
-    }
-    if (lane == 0) {
-      s_before = before * p.num_kv_heads;
-      s_W = all * p.num_kv_heads;
-    }
-  }
-  __syncthreads();
-  const int64_t start = s_before + static_cast<int64_t>(g) * T;
-  const int64_t W = s_W;
-  const int32_t P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
-  const int32_t c0 = cta_of(W, P, start);
-  const int32_t c1 = cta_of(W, P, start + T - 1);
-  if (c0 == c1 || h >= p.group) return;
   const int np = c1 - c0 + 1;
   const int64_t first = static_cast<int64_t>(seg) + c0;  // piece index of c0
   const float2* ml = p.ws_ml + first * kMaxG + h;

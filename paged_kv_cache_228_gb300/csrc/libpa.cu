@@ -59,6 +59,25 @@ pa_status device_sms(int* sms, int* dev_out) {
   return PA_OK;
 }
 
+// Launch as a programmatic dependent of the previous work in the stream:
+// the grid may start launching before that work ends, and waits for it on
+// the device (griddepcontrol.wait) before it reads anything.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
 // dependency on libcuda).
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -147,9 +166,14 @@ pa_status decode_plan(int dev, DecodePlan* out) {
   return PA_OK;
 }
 
-size_t workspace_bytes_for(int64_t pieces, int32_t head_dim) {
+// Workspace for P decode CTAs over `segs` segments: P + segs partial
+// slots (a CTA's pieces never collide: piece = cta + segment), then P
+// merge jobs.
+size_t workspace_bytes_for(int64_t P, int64_t segs, int32_t head_dim) {
+  const int64_t pieces = P + segs;
   return static_cast<size_t>(pieces) * kMaxG *
-         (static_cast<size_t>(head_dim) * sizeof(float) + sizeof(float2));
+             (static_cast<size_t>(head_dim) * sizeof(float) + sizeof(float2)) +
+         static_cast<size_t>(P) * sizeof(int2);
 }
 
 template <int D, bool FP8>
@@ -166,21 +190,24 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
   const int stages = plan.stages;
   const int32_t P = num_splits > 0 ? num_splits : sms * plan.ctas_per_sm;
   const int64_t segs = static_cast<int64_t>(prm_in.num_seqs) * prm_in.num_kv_heads;
-  const size_t need = P > 1 ? workspace_bytes_for(P + segs, D) : 0;
+  const size_t need = P > 1 ? workspace_bytes_for(P, segs, D) : 0;
   if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
     return PA_ERR_WORKSPACE;
 
   DecodeParams prm = prm_in;
   prm.num_ctas = P;
   prm.stages = stages;
+  prm.ws_o = nullptr;
+  prm.ws_ml = nullptr;
+  prm.ws_job = nullptr;
   if (need > 0) {
     const int64_t pieces = P + segs;
-    prm.ws_o = static_cast<float*>(workspace);
-    prm.ws_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
-                                          static_cast<size_t>(pieces) * kMaxG * D * sizeof(float));
-  } else {
-    prm.ws_o = nullptr;
-    prm.ws_ml = nullptr;
+    char* w = static_cast<char*>(workspace);
+    prm.ws_o = reinterpret_cast<float*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * D * sizeof(float);
+    prm.ws_ml = reinterpret_cast<float2*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * sizeof(float2);
+    prm.ws_job = reinterpret_cast<int2*>(w);
   }
 
   CUtensorMap tq, tk, tv;
@@ -203,27 +230,14 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
       return PA_ERR_CUDA;
   }
   // Both grids are programmatic dependents of the work before them in the
-  // stream: each launches early and waits on the device (griddepcontrol)
-  // before it reads anything, which hides the launch gaps.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(P));
-  cfg.blockDim = dim3(DecodeShape<D, FP8>::kThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes<D, FP8>(stages);
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (cudaLaunchKernelEx(&cfg, decode_fn<D, FP8>(), tq, tk, tv, prm) != cudaSuccess)
+  // stream, which hides the launch gaps.
+  if (launch_pdl(decode_fn<D, FP8>(), dim3(static_cast<unsigned>(P)),
+                 dim3(DecodeShape<D, FP8>::kThreads), decode_smem_bytes<D, FP8>(stages), stream,
+                 tq, tk, tv, prm) != cudaSuccess)
     return PA_ERR_CUDA;
-  if (segs > 0) {
-    cfg.gridDim = dim3(static_cast<unsigned>(segs));
-    cfg.blockDim = dim3(kMaxG * D / 4);
-    cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&cfg, paged_decode_merge_kernel<D>, prm) != cudaSuccess)
-      return PA_ERR_CUDA;
-  }
+  if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
+                 dim3(kMaxG * D / 4), 0, stream, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
   return PA_OK;
 }
 
@@ -278,11 +292,13 @@ extern "C" pa_status pa_cache_write(const void* k_new, const void* v_new,
   const int64_t total = 2LL * num_tokens * num_kv_heads * cpr;
   int64_t grid = (total + 255) / 256;
   if (grid > static_cast<int64_t>(sms) * 16) grid = static_cast<int64_t>(sms) * 16;
-  cache_write_kernel<<<static_cast<unsigned>(grid), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), slot_mapping,
-      num_tokens, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
-      static_cast<int64_t>(num_blocks) * block_size, num_kv_heads, block_size, cpr);
-  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+  const cudaError_t e = launch_pdl(
+      cache_write_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+      static_cast<cudaStream_t>(stream), static_cast<const uint4*>(k_new),
+      static_cast<const uint4*>(v_new), slot_mapping, num_tokens, static_cast<uint4*>(k_cache),
+      static_cast<uint4*>(v_cache), static_cast<int64_t>(num_blocks) * block_size,
+      num_kv_heads, block_size, cpr);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale,
@@ -381,7 +397,7 @@ extern "C" pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
     if (st != PA_OK) return st;
     P = a > b ? a : b;
   }
-  *bytes = P > 1 ? workspace_bytes_for(P + static_cast<int64_t>(num_seqs) * num_kv_heads,
+  *bytes = P > 1 ? workspace_bytes_for(P, static_cast<int64_t>(num_seqs) * num_kv_heads,
                                        head_dim)
                  : 0;
   return PA_OK;
