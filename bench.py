@@ -3,9 +3,11 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
                     [--impl native|reference]
 
-One step = one decode layer-step of the whole hot path on one batch:
-pa_cache_write of the step's new K/V (one appended token per sequence),
-pa_decode (paged attention over every cached token) and its split-K merge.
+One step = one decode layer-step of the whole hot path on one batch: the
+cache write of the step's new K/V (one appended token per sequence) and
+paged attention over every cached token, in one pa_decode_append launch,
+then its split-K merge launch.  (The FP8 figures run pa_decode on a cache
+quantised beforehand: FP8 append is not part of the step.)
 The host block manager has already placed the appended tokens (its cost is
 reported separately).  Inputs are seeded synthetic tensors shaped like the
 workload, resident in HBM; consecutive steps rotate over several
@@ -219,12 +221,15 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     def step(i, ev=None):
         k, v = pools[i % n_pools]
         ks, vs = scales[i % n_pools]
-        if not fp8:
-            pa.pa_cache_write(kn, vn, slots, k, v, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks, v_scale=vs,
-                     stream=stream)
+        if fp8:
+            pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks, v_scale=vs,
+                         stream=stream)
+        else:
+            # this step's cache write and decode in one launch
+            pa.pa_decode_append(q, kn, vn, slots, k, v, tab, lens, w.scale, out, ws,
+                                stream=stream)
         if ev is not None:
             ev[1].record(stream)
 
@@ -269,10 +274,12 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
                 for i in range(n_pools):
                     k, v = pools[i]
                     ks, vs = scales[i]
-                    if not fp8:
-                        pa.pa_cache_write(kn, vn, slots, k, v, stream=s2)
-                    pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks,
-                                 v_scale=vs, stream=s2)
+                    if fp8:
+                        pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks,
+                                     v_scale=vs, stream=s2)
+                    else:
+                        pa.pa_decode_append(q, kn, vn, slots, k, v, tab, lens, w.scale, out,
+                                            ws, stream=s2)
         stream.wait_stream(s2)
         reps = max(1, steps // n_pools)
         for _ in range(3):
@@ -302,7 +309,7 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
         "pool_bytes": per_pool // (2 if fp8 else 1),
         "clocks": sampler.summary() if sampler else None,
         "e2e": e2e,
-        "launches_per_step": (1 if fp8 else 2) + 1,
+        "launches_per_step": 2,  # decode (with the fused cache write) + merge
     }
 
 
@@ -325,10 +332,12 @@ def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps)
     def one():
         for n in h:
             d[n].copy_(h[n], non_blocking=True)
-        if not fp8:
-            pa.pa_cache_write(d["kn"], d["vn"], d["slots"], k, v, stream=stream)
-        pa.pa_decode(d["q"], k, v, d["tab"], d["lens"], w.scale, out_d, ws, k_scale=ks,
-                     v_scale=vs, stream=stream)
+        if fp8:
+            pa.pa_decode(d["q"], k, v, d["tab"], d["lens"], w.scale, out_d, ws, k_scale=ks,
+                         v_scale=vs, stream=stream)
+        else:
+            pa.pa_decode_append(d["q"], d["kn"], d["vn"], d["slots"], k, v, d["tab"],
+                                d["lens"], w.scale, out_d, ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
 
     for _ in range(5):
@@ -514,7 +523,8 @@ def main():
                 "l2": f"inputs larger than L2: {res['n_pools']} rotating layer pools of "
                       f"{res['pool_bytes'] / 1e9:.2f} GB",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
-                "step": "pa_cache_write + pa_decode (+ split merge), eager launches",
+                "step": "pa_decode_append: cache write fused into the decode launch, "
+                        "+ merge launch; eager launches",
             },
             "seqs_per_s": w.num_seqs * ws / step_s,
             "us_per_step": step_s * 1e6,
@@ -526,7 +536,8 @@ def main():
             "host_block_manager_us_per_append": res["host_append_us"] / w.num_seqs,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-                         "kernel": "paged_decode_ws_kernel<128,bf16> + merge (per launch pair)",
+                         "kernel": "paged_decode_ws_kernel<128,bf16> (fused append) + merge "
+                                   "(per launch pair)",
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": nbytes / (e2e["ms_per_step"] / 1e3) / 1e9, "unit": "GB/s",

@@ -198,6 +198,34 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
                     void* out, void* workspace, size_t workspace_bytes,
                     int32_t num_splits, void* stream);
 
+/* pa_decode_append -- this step's cache write and decode in one launch.
+ * The same result, in the cache and in out, as
+ *     pa_cache_write(k_new, v_new, slot_mapping, num_seqs, ...);
+ *     pa_decode(q, k_cache, v_cache, ..., PA_KV_BF16, ...);
+ * for a decode step where sequence b appends one token (row b of
+ * k_new/v_new) at its last position: "Paged Attention and KV Cache
+ * Fragmentation", section "How PagedAttention maps an OS concept onto GPU
+ * memory" (a new token lands in the block the table names for its
+ * position, then the kernel walks the table).  The CTA that owns sequence
+ * b's last tile stores the row just before it copies that tile.
+ *   k_new, v_new   device bf16 [num_seqs][num_kv_heads][head_dim]
+ *   slot_mapping   device int64 [num_seqs]; < 0: sequence b appends nothing
+ *   other arguments as pa_decode, with a bf16 cache (no scales)
+ * Requirements, beyond pa_decode's: slot_mapping[b] >= 0 must be the slot
+ * of position seq_lens[b] - 1 (block_tables[b][(n-1)/bs] * bs + (n-1) % bs,
+ * as the block manager returns it), and that block must be private to b
+ * (copy-on-write done).  A slot elsewhere, or on an empty sequence, is not
+ * written and flags PA_DEVERR_BAD_SLOT.  FP8 caches: PA_ERR_UNSUPPORTED. */
+pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
+                           const int64_t* slot_mapping, void* k_cache,
+                           void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                           int32_t num_seqs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim,
+                           int32_t block_size, int32_t num_blocks, float scale,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           int32_t num_splits, void* stream);
+
 /* pa_decode_noalloc -- pa_decode for callers that cannot allocate.
  * The pages have no counterpart: this is a library-only convenience.
  * Some callers cannot call cudaMalloc or otherwise obtain device memory:

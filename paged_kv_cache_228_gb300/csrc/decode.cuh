@@ -61,6 +61,14 @@ struct DecodeParams {
   float2* ws_ml;  // [pieces][kMaxG] (running max in log2 units, sum)
   int2* ws_job;   // [P]: (segment, first CTA) of the split segment that
                   // CTA finishes, else (-1, -1)
+  // Fused append (bf16 caches; null when off): sequence b's new token
+  // k_new/v_new[b][Hkv][D] goes to slot_mapping[b] (< 0: none), which must
+  // be the slot the table gives position seq_lens[b] - 1.
+  const uint8_t* k_new;
+  const uint8_t* v_new;
+  const int64_t* slot_mapping;
+  uint8_t* k_cache;
+  uint8_t* v_cache;
   int32_t num_seqs, num_q_heads, num_kv_heads, group, block_size, log2_bs;
   int32_t max_blocks, num_blocks;
   int32_t rows_total;  // num_blocks * num_kv_heads * block_size
@@ -226,6 +234,8 @@ struct Loader {
   uint32_t it;       // tiles issued
   uint32_t qn;       // query slots filled (segments begun)
   bool fresh;        // the next tile opens a segment
+  int64_t slot;      // fused append: slot of the segment's new token
+  uint4 row;         // fused append: this lane's 16 bytes of its K|V row
 };
 
 // log2 of the blocks per 16-token tile
@@ -330,6 +340,52 @@ __device__ __forceinline__ void copy_tile(const DecodeParams& p, const Maps& tm,
   }
 }
 
+// Fused append, at the start of segment (b, g): load the slot of sequence
+// b's new token and, lane l < 2 * D / 8, 16 bytes of its K (l < D / 8) or
+// V row for head g.  Used only at the segment's last tile.
+template <int D>
+__device__ __forceinline__ void fetch_new_token(const DecodeParams& p, Loader& ld) {
+  constexpr int kChunks = D * 2 / 16;
+  const int lane = threadIdx.x & 31;
+  ld.slot = p.slot_mapping[ld.c.b];
+  if (lane < 2 * kChunks) {
+    const int kv = lane / kChunks, ch = lane % kChunks;
+    const int64_t src = (static_cast<int64_t>(ld.c.b) * p.num_kv_heads + ld.c.g) * (D * 2) + ch * 16;
+    ld.row = *reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) + src);
+  }
+}
+
+// Warp-collective, before the copy of the segment's last tile: store the
+// new token's K and V rows of head g at its slot, then fence so the tile's
+// TMA read sees them.  Only this CTA reads that tile, and copy-on-write
+// keeps every appended slot private to its sequence.  A slot that is not
+// where the table puts position n - 1 flags PA_DEVERR_BAD_SLOT and is not
+// written.
+template <int D>
+__device__ __forceinline__ void store_new_token(const DecodeParams& p, const Loader& ld,
+                                                int32_t b0, int32_t b1) {
+  constexpr int kChunks = D * 2 / 16;
+  const int lane = threadIdx.x & 31;
+  if (ld.slot < 0) return;
+  const int32_t pos = ld.c.n - 1;
+  const int32_t blk = (p.block_size < kTile && (pos & (kTile - 1)) >= p.block_size) ? b1 : b0;
+  const int32_t off = pos & (p.block_size - 1);
+  if (blk < 0 || blk >= p.num_blocks ||
+      ld.slot != static_cast<int64_t>(blk) * p.block_size + off) {
+    if (lane == 0) flag_error(PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  if (lane < 2 * kChunks) {
+    const int kv = lane / kChunks, ch = lane % kChunks;
+    const int64_t dst =
+        ((static_cast<int64_t>(blk) * p.num_kv_heads + ld.c.g) * p.block_size + off) * (D * 2) +
+        ch * 16;
+    *reinterpret_cast<uint4*>((kv ? p.v_cache : p.k_cache) + dst) = ld.row;
+    fence_proxy_async_global();
+  }
+  __syncwarp();
+}
+
 // Warp-collective: issue the loader's next tile (and, if it opens a
 // segment, the segment's query rows) into the next stage, then advance
 // the loader.  The caller has made sure the stage and query slot are free.
@@ -341,6 +397,7 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm
     if (lane == 0) copy_query<D, FP8>(p, tm, sb, ld.c, ld.qn % kQSlots);
     ++ld.qn;
     ld.fresh = false;
+    if (!FP8 && p.k_new != nullptr) fetch_new_token<D>(p, ld);
   }
   advance_table<FP8>(p, ld);
   const int lr = rpt_log2(p);
@@ -363,6 +420,7 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm
     // written before the stage's arrive, read after its completion
     if (lane == 0) sb.hdr->scales[stage] = sc;
   }
+  if (!FP8 && p.k_new != nullptr && ld.c.tile == ld.c.T - 1) store_new_token<D>(p, ld, b0, b1);
   if (lane == 0) copy_tile<D, FP8>(p, tm, sb, ld.c, stage, b0, b1);
   ++ld.it;
   ++ld.u;
@@ -385,6 +443,8 @@ __device__ __forceinline__ void loader_init(const DecodeParams& p, int64_t lo, i
   ld.ks = ld.vs = ld.nks = ld.nvs = 1.f;
   ld.it = ld.qn = 0;
   ld.fresh = true;
+  ld.slot = -1;
+  ld.row = make_uint4(0u, 0u, 0u, 0u);
 }
 
 __device__ __forceinline__ bool can_issue(const DecodeParams& p, const Loader& ld,
@@ -1021,6 +1081,8 @@ __global__ void __launch_bounds__(kMaxG * D / 4)
   for (int32_t bb = blockIdx.x * blockDim.x + threadIdx.x; bb < p.num_seqs;
        bb += gridDim.x * blockDim.x) {
     if (clamp_len(p, p.seq_lens[bb]) == 0) {
+      // a fused append needs the new token inside the sequence
+      if (p.slot_mapping != nullptr && p.slot_mapping[bb] >= 0) flag_error(PA_DEVERR_BAD_SLOT);
       uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(bb) * p.num_q_heads * D);
       for (int i = 0; i < p.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
     }

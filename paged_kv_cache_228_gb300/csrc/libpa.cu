@@ -403,14 +403,23 @@ extern "C" pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
   return PA_OK;
 }
 
-extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
-                               const float* k_scale, const float* v_scale,
-                               pa_kv_dtype kv_dtype, const int32_t* block_tables,
-                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                               float scale, void* out, void* workspace,
-                               size_t workspace_bytes, int32_t num_splits, void* stream) {
+namespace pa {
+namespace {
+
+struct AppendArgs {
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+};
+
+pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
+                       const float* k_scale, const float* v_scale, pa_kv_dtype kv_dtype,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                       int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                       int32_t num_blocks, float scale, void* out, void* workspace,
+                       size_t workspace_bytes, int32_t num_splits, void* stream,
+                       const AppendArgs* app) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq < 0 || num_splits < 0 || !(scale == scale) ||
       num_q_heads % num_kv_heads != 0)
@@ -420,11 +429,16 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (group > kMaxG) return PA_ERR_UNSUPPORTED;
   if (!pow2_in(block_size, 8, 256)) return PA_ERR_UNSUPPORTED;
+  if (app != nullptr && kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (app != nullptr &&
+      (!app->k_new || !app->v_new || !app->slot_mapping || !aligned16(app->k_new) ||
+       !aligned16(app->v_new) || (reinterpret_cast<uintptr_t>(app->slot_mapping) & 7u)))
     return PA_ERR_INVALID_ARG;
   if (kv_dtype == PA_KV_FP8_E4M3 && (!k_scale || !v_scale)) return PA_ERR_INVALID_ARG;
   const int64_t rows = static_cast<int64_t>(num_blocks) * num_kv_heads * block_size;
@@ -450,6 +464,13 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
   p.num_blocks = num_blocks;
   p.rows_total = static_cast<int32_t>(rows);
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (app != nullptr) {
+    p.k_new = static_cast<const uint8_t*>(app->k_new);
+    p.v_new = static_cast<const uint8_t*>(app->v_new);
+    p.slot_mapping = app->slot_mapping;
+    p.k_cache = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+    p.v_cache = static_cast<uint8_t*>(const_cast<void*>(v_cache));
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (kv_dtype == PA_KV_BF16) {
     if (head_dim == 128)
@@ -459,6 +480,38 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
   if (head_dim == 128)
     return launch_decode<128, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
   return launch_decode<64, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
+                               const float* k_scale, const float* v_scale,
+                               pa_kv_dtype kv_dtype, const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                               int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                               float scale, void* out, void* workspace,
+                               size_t workspace_bytes, int32_t num_splits, void* stream) {
+  return decode_entry(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_tables,
+                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
+                      num_splits, stream, nullptr);
+}
+
+extern "C" pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
+                                      const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* seq_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, int32_t num_kv_heads,
+                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                      float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const AppendArgs app{k_new, v_new, slot_mapping};
+  return decode_entry(q, k_cache, v_cache, nullptr, nullptr, PA_KV_BF16, block_tables,
+                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
+                      num_splits, stream, &app);
 }
 
 // ------------------------------------------------------------ no-alloc ---

@@ -45,6 +45,10 @@ SIGNATURES = {
     "pa_decode": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                            _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                            ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int, _c_ptr]),
+    "pa_decode_append": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                  _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                  _c_int, ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int,
+                                  _c_ptr]),
     "pa_decode_noalloc": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr,
                                    _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, ctypes.c_float, _c_ptr, _c_int, _c_ptr]),
@@ -191,6 +195,33 @@ def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out, workspace
         _kv_dtype(k_cache), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B,
         hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits,
         _stream(stream)))
+
+
+def pa_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tables, seq_lens,
+                     scale, out, workspace=None, num_splits=0, stream=None):
+    """This step's cache write and decode in one launch (bf16 cache): the
+    same cache and out as pa_cache_write(k_new, v_new, slot_mapping, ...)
+    then pa_decode(...), where row b of k_new / v_new is sequence b's new
+    token and slot_mapping[b] its slot (< 0: none)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    if k_cache.dtype != torch.bfloat16 or v_cache.dtype != torch.bfloat16:
+        raise ValueError("pa_decode_append: the cache must be bf16")
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if tuple(k_new.shape) != (B, hkv, d) or tuple(v_new.shape) != (B, hkv, d) or \
+            slot_mapping.shape[0] != B:
+        raise ValueError("pa_decode_append: k_new/v_new must be [B, Hkv, d], slot_mapping [B]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_append", lib().pa_decode_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, bs, nb,
+        float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024

@@ -68,6 +68,13 @@ def test_host_validation_without_gpu(palib):
                             palib.PA_KV_FP8_E4M3, None) == palib.PA_ERR_UNSUPPORTED
     assert L.pa_cache_write(None, None, None, 0, None, None, 1, 1, 16, 64,
                             palib.PA_KV_BF16, None) == palib.PA_OK
+    # fused append: missing new-token buffers, unsupported shapes
+    assert L.pa_decode_append(None, None, None, None, None, None, None, 1, None, 1, 4, 2, 64,
+                              16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_decode_append(None, None, None, None, None, None, None, 1, None, 1, 4, 2, 96,
+                              16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_UNSUPPORTED
+    assert L.pa_decode_append(None, None, None, None, None, None, None, 1, None, 0, 4, 2, 64,
+                              16, 8, 1.0, None, None, 0, 0, None) == palib.PA_OK
 
 
 def _compare_models(pa, seed, steps=2000, N=48, bs=4):

@@ -1,0 +1,116 @@
+"""GPU tests of pa_decode_append, the step's cache write and decode in one
+launch: it must leave exactly the cache and the output that pa_cache_write
+followed by pa_decode leave (bit for bit), and so match the fp64 oracle.
+
+Cases cover block sizes 8 (two blocks per 16-token tile), 16 and 32, split
+and unsplit segments (automatic and 7 partitions), sequences that append
+nothing (slot -1), and a slot that is not where the table puts the last
+position (flagged, not written).
+"""
+import pytest
+import torch
+
+from paged_kv_cache_228_gb300 import pa
+from paged_kv_cache_228_gb300 import workloads as W
+
+from cases import assert_close, build_case, oracle_decode, snapshot_blocks
+
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from paged_kv_cache_228_gb300 import build
+    build.build()
+    pa.pa_get_device_error()
+
+
+def _workspace(w, num_splits):
+    n = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                    num_splits)
+    return torch.full((max(n, 16),), 255, dtype=torch.uint8, device="cuda")
+
+
+def _out(w):
+    return torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"),
+                      dtype=torch.bfloat16, device="cuda")
+
+
+def _two_ways(case, slots, num_splits):
+    """(out, k, v) of write-then-decode and of the fused call, each on its
+    own copy of the pool."""
+    w = case.w
+    k1, v1 = case.k_cache.clone(), case.v_cache.clone()
+    k2, v2 = case.k_cache.clone(), case.v_cache.clone()
+    o1, o2 = _out(w), _out(w)
+    pa.pa_cache_write(case.k_new, case.v_new, slots, k1, v1)
+    pa.pa_decode(case.q, k1, v1, case.table_t, case.lens_t, w.scale, o1,
+                 _workspace(w, num_splits), num_splits=num_splits)
+    pa.pa_decode_append(case.q, case.k_new, case.v_new, slots, k2, v2, case.table_t,
+                        case.lens_t, w.scale, o2, _workspace(w, num_splits),
+                        num_splits=num_splits)
+    torch.cuda.synchronize()
+    return (o1, k1, v1), (o2, k2, v2)
+
+
+def _bits(t):
+    return t.view(torch.int16)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3.2-1b", "llama3.1-8b", "shared_prefix_bs8",
+                                  "shared_prefix_bs32"])
+@pytest.mark.parametrize("splits", [0, 7])
+def test_fused_equals_write_then_decode(name, splits):
+    case = build_case(W.WORKLOADS[name]())
+    (o1, k1, v1), (o2, k2, v2) = _two_ways(case, case.slots_t, splits)
+    assert torch.equal(_bits(o1), _bits(o2)), name
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2)), name
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fused_matches_oracle():
+    case = build_case(W.llama31_8b(), poison_unused=True)
+    seqs = range(case.w.num_seqs)
+    snap = snapshot_blocks(case, seqs)
+    w = case.w
+    out = _out(w)
+    pa.pa_decode_append(case.q, case.k_new, case.v_new, case.slots_t, case.k_cache,
+                        case.v_cache, case.table_t, case.lens_t, w.scale, out,
+                        _workspace(w, 0))
+    torch.cuda.synchronize()
+    assert_close(out, oracle_decode(case, snap, seqs), TOL_BF16, "fused append 8B")
+    assert pa.pa_get_device_error() == 0
+
+
+def test_sequences_without_append():
+    # slot -1: the sequence appends nothing; position n - 1 keeps what the
+    # pool held, in both ways of running the step
+    case = build_case(W.llama32_1b())
+    slots = case.slots_t.clone()
+    slots[::3] = -1
+    (o1, k1, v1), (o2, k2, v2) = _two_ways(case, slots, 0)
+    assert torch.equal(_bits(o1), _bits(o2))
+    assert torch.equal(_bits(k1), _bits(k2)) and torch.equal(_bits(v1), _bits(v2))
+    assert pa.pa_get_device_error() == 0
+
+
+def test_misplaced_slot_is_flagged_and_not_written():
+    case = build_case(W.tiny())
+    w = case.w
+    slots = case.slots_t.clone()
+    slots[1] = slots[1] - 1          # a slot, but not position n - 1's
+    k2, v2 = case.k_cache.clone(), case.v_cache.clone()
+    before_k = k2.clone()
+    pa.pa_decode_append(case.q, case.k_new, case.v_new, slots, k2, v2, case.table_t,
+                        case.lens_t, w.scale, _out(w), _workspace(w, 0))
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() & pa.DEVERR_BAD_SLOT
+    s = int(case.slots[1]) - 1
+    blk, off = s // w.block_size, s % w.block_size
+    assert torch.equal(_bits(k2[blk, :, off]), _bits(before_k[blk, :, off]))
+    # the other sequences still appended
+    s0 = int(case.slots[0])
+    assert torch.equal(_bits(k2[s0 // w.block_size, :, s0 % w.block_size]),
+                       _bits(case.k_new[0]))
