@@ -156,18 +156,16 @@ def step_inputs(w, device):
     maxb = w.max_blocks_per_seq
     alloc, tables, lens = pa.replay_script(W.build_script(w), w.num_seqs, w.block_size, maxb,
                                            w.pool_blocks)
-    t0 = time.perf_counter()
-    slots = []
-    for b in range(w.num_seqs):
-        st, s, _ = alloc.append_slots(tables[b], lens[b], 1, w.block_size, maxb)
-        assert st == pa.PA_OK
-        slots += s
-    host_us = (time.perf_counter() - t0) * 1e6
-    tab = torch.full((w.num_seqs, maxb), -1, dtype=torch.int32)
-    for b, t in enumerate(tables):
-        tab[b, :len(t)] = torch.tensor(t, dtype=torch.int32)
+    # the step's appends: one native call for the batch (timed)
+    ba = pa.BatchAppender(alloc, tables, maxb)
+    ones = [1] * w.num_seqs
+    st, slots, _, done = ba.append(lens, ones, w.block_size)
+    host_us = ba.last_call_us  # the native call (one per step) with its FFI entry
+    assert st == pa.PA_OK and done == w.num_seqs
+    tab = torch.from_numpy(ba.tables.copy())
+    tables = [list(r[r >= 0]) for r in ba.tables]
     return (tables, tab.to(device), torch.tensor(w.seq_lens, dtype=torch.int32, device=device),
-            torch.tensor(slots, dtype=torch.int64, device=device), host_us)
+            torch.from_numpy(slots.copy()).to(device), host_us)
 
 
 def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):

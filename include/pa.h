@@ -306,6 +306,23 @@ pa_status pa_seq_append_slots(pa_allocator* a, int32_t* table,
                               int32_t block_size, int64_t* slots_out,
                               int32_t* cow_pair_out, int32_t* num_cow);
 
+/* pa_batch_append_slots -- one step's appends for a whole batch in one call:
+ * for i = 0, 1, ..., num_seqs - 1 in order, sequence i (row i of tables,
+ * host int32 [num_seqs][max_blocks]) grows from lens[i] by n_new[i] tokens
+ * exactly as pa_seq_append_slots would.  slots_out (host int64,
+ * sum(n_new) entries) receives the slots sequence after sequence;
+ * cow_pairs_out (host int32 [num_seqs][3]) and n_cow_out[i] each
+ * sequence's copy request.  The first sequence that fails stops the batch:
+ * its status is returned, *num_done (host) = i, sequences >= i are
+ * untouched and sequences < i keep their appends (each one is
+ * all-or-nothing, the batch is not).  On success *num_done = num_seqs. */
+pa_status pa_batch_append_slots(pa_allocator* a, int32_t* tables,
+                                int32_t max_blocks, const int32_t* lens,
+                                const int32_t* n_new, int32_t num_seqs,
+                                int32_t block_size, int64_t* slots_out,
+                                int32_t* cow_pairs_out, int32_t* n_cow_out,
+                                int32_t* num_done);
+
 #ifdef __cplusplus
 }
 #endif

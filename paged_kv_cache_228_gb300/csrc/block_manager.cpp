@@ -160,3 +160,28 @@ extern "C" pa_status pa_seq_append_slots(pa_allocator* a, int32_t* table,
   }
   return PA_OK;
 }
+
+extern "C" pa_status pa_batch_append_slots(pa_allocator* a, int32_t* tables,
+                                           int32_t max_blocks, const int32_t* lens,
+                                           const int32_t* n_new, int32_t num_seqs,
+                                           int32_t block_size, int64_t* slots_out,
+                                           int32_t* cow_pairs_out, int32_t* n_cow_out,
+                                           int32_t* num_done) {
+  if (num_done == nullptr) return PA_ERR_INVALID_ARG;
+  *num_done = 0;
+  if (a == nullptr || num_seqs < 0 || max_blocks < 0) return PA_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (lens == nullptr || n_new == nullptr || cow_pairs_out == nullptr ||
+                       n_cow_out == nullptr || (max_blocks > 0 && tables == nullptr)))
+    return PA_ERR_INVALID_ARG;
+  int64_t at = 0;  // next slot index in slots_out
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    const pa_status st = pa_seq_append_slots(
+        a, tables + static_cast<int64_t>(i) * max_blocks, max_blocks, lens[i], n_new[i],
+        block_size, slots_out == nullptr ? nullptr : slots_out + at, cow_pairs_out + 3 * i,
+        n_cow_out + i);
+    if (st != PA_OK) return st;
+    at += n_new[i];
+    *num_done = i + 1;
+  }
+  return PA_OK;
+}

@@ -10,6 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import time
 
 import torch
 
@@ -61,6 +62,8 @@ SIGNATURES = {
     "pa_block_num_free": (_c_int, [_c_ptr]),
     "pa_seq_append_slots": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
                                      _c_ptr, _c_ptr, ctypes.POINTER(_c_int)]),
+    "pa_batch_append_slots": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
+                                       _c_ptr, _c_ptr, _c_ptr, ctypes.POINTER(_c_int)]),
 }
 
 
@@ -314,6 +317,43 @@ class Allocator:
         table[:] = list(tab[:want])
         pairs = [tuple(cow[:3])] if ncow.value else []
         return st, list(slots[:n]), pairs
+
+
+class BatchAppender:
+    """One decode step's appends for a batch through pa_batch_append_slots.
+
+    Holds host arrays sized for the batch so that each call is one native
+    call with no per-sequence Python work: ``tables`` (int32 [B, max_blocks],
+    -1 padded) is updated in place.
+    """
+
+    def __init__(self, alloc: "Allocator", tables, max_blocks: int):
+        import numpy as np
+        self.alloc = alloc
+        self.max_blocks = max_blocks
+        B = len(tables)
+        self.tables = np.full((B, max_blocks), -1, dtype=np.int32)
+        for b, t in enumerate(tables):
+            self.tables[b, :len(t)] = t
+        self.cow = np.zeros((B, 3), dtype=np.int32)
+        self.ncow = np.zeros(B, dtype=np.int32)
+
+    def append(self, lens, n_new, block_size: int):
+        """(status, slots int64 [sum n_new], cow pairs list, num_done)."""
+        import numpy as np
+        lens = np.ascontiguousarray(lens, dtype=np.int32)
+        n_new = np.ascontiguousarray(n_new, dtype=np.int32)
+        slots = np.zeros(max(1, int(n_new.sum())), dtype=np.int64)
+        done = ctypes.c_int32(0)
+        fn = lib().pa_batch_append_slots
+        args = (self.alloc._h, self.tables.ctypes.data, self.max_blocks, lens.ctypes.data,
+                n_new.ctypes.data, len(lens), block_size, slots.ctypes.data,
+                self.cow.ctypes.data, self.ncow.ctypes.data, ctypes.byref(done))
+        t0 = time.perf_counter()
+        st = fn(*args)
+        self.last_call_us = (time.perf_counter() - t0) * 1e6  # the native call alone
+        pairs = [tuple(int(x) for x in self.cow[i]) for i in np.flatnonzero(self.ncow[:done.value])]
+        return st, slots[:int(n_new[:done.value].sum())], pairs, done.value
 
 
 def replay_script(ops, num_seqs: int, block_size: int, max_blocks: int, num_blocks: int):

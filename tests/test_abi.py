@@ -145,3 +145,50 @@ def test_native_replay_matches_model_on_workloads(palib):
         a, t2, l2 = palib.replay_script(ops, w.num_seqs, w.block_size, w.max_blocks_per_seq,
                                         w.pool_blocks)
         assert t1 == t2 and l1 == l2, name
+
+
+def test_batch_append_matches_model(palib):
+    # One native call per step against the oracle's model appending the
+    # same batch sequence by sequence; a step that runs out of blocks stops
+    # at the failing sequence and leaves it and later ones untouched.
+    from oracle import block_manager as BM
+    pa = palib
+    rng = np.random.default_rng(11)
+    N, bs, maxb, B = 40, 4, 16, 9
+    m = BM.BlockManagerModel(N)
+    a = pa.Allocator(N)
+    tm = [[] for _ in range(B)]
+    ba = pa.BatchAppender(a, tm, maxb)
+    lens = np.zeros(B, dtype=np.int32)
+    saw_stop = False
+    for step in range(60):
+        n_new = rng.integers(0, 4, size=B).astype(np.int32)
+        if step % 7 == 3:           # fork a sequence into another slot's place
+            src, dst = rng.integers(0, B, size=2)
+            if src != dst and lens[src] > 0:
+                m.free(tm[dst]); assert a.free(list(ba.tables[dst][ba.tables[dst] >= 0])) == 0
+                tm[dst] = list(tm[src]); ba.tables[dst] = ba.tables[src]
+                assert m.fork(tm[dst]) == 0 and a.fork(tm[dst]) == 0
+                lens[dst] = lens[src]
+        st, slots, pairs, done = ba.append(lens, n_new, bs)
+        ms, mp, mdone, mst = [], [], 0, BM.OK
+        for i in range(B):
+            st_i, s_i, p_i = m.append_slots(tm[i], int(lens[i]), int(n_new[i]), bs, maxb)
+            if st_i != BM.OK:
+                mst = st_i
+                break
+            ms += s_i; mp += p_i; mdone = i + 1
+        assert (st, done) == (mst, mdone), step
+        assert list(slots) == ms and pairs == mp, step
+        for i in range(B):
+            assert list(ba.tables[i][:len(tm[i])]) == tm[i] and \
+                (ba.tables[i][len(tm[i]):] == -1).all(), (step, i)
+        lens[:done] += n_new[:done]
+        if st != 0:
+            saw_stop = True
+            # finish some sequences to make room again
+            for i in range(0, B, 2):
+                assert m.free(tm[i]) == 0
+                assert a.free(list(ba.tables[i][ba.tables[i] >= 0])) == 0
+                tm[i] = []; ba.tables[i] = -1; lens[i] = 0
+    assert saw_stop
