@@ -74,3 +74,60 @@ def quantize_blocks(cache_f32: np.ndarray, block_ids, valid_lens):
 def dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
     """fp64 values decode(code) * scale for a whole [nb, Hkv, bs, d] cache."""
     return e4m3.decode(codes) * scales.astype(np.float64)[:, :, None, None]
+
+
+# ------------------------------------------------------------ FP8 append ---
+# Appending a token to an FP8 block.  The pages name only whole-block
+# quantisation; appending into a partly filled block is this restatement's
+# reading, the plainest one that keeps one fp32 scale per (block, KV head)
+# and never lets a stored value overflow:
+#
+#   the token's own scale   s_t = a_t / 448        (a_t = max |x_t|; fp32)
+#   first token of a block  (offset 0): scale = s_t, or 1 when a_t == 0
+#   later tokens            scale = max(old scale, s_t)   ("grow only")
+#   when the scale grows, every earlier row r < offset is requantised:
+#       y    = decode(code) * old_scale          (fp32 product, RN)
+#       code = e4m3_rne_satfinite(y / new_scale) (fp32 IEEE divide)
+#   the token itself        code = e4m3_rne_satfinite(x_t / scale)
+#
+# Filling a block in order of falling absmax therefore never requantises and
+# gives exactly the whole-block quantiser's codes, and whatever the order the
+# final scale equals the whole-block scale of the block's tokens.
+
+
+def append_token(codes_tile: np.ndarray, scale, offset: int, x_f32: np.ndarray):
+    """Append one token row x (fp32 [d]) at ``offset`` of one (block, head)
+    tile of codes (uint8 [bs, d], rows >= offset unused).  Returns the new
+    (codes, scale); the input is not modified."""
+    codes = np.array(codes_tile, dtype=np.uint8, copy=True)
+    x = np.asarray(x_f32, dtype=np.float32)
+    a = np.float32(np.max(np.abs(x))) if x.size else np.float32(0)
+    s_t = np.float32(a / np.float32(e4m3.E4M3_MAX))
+    old = np.float32(scale)
+    if offset == 0:
+        new = np.float32(1.0) if a == 0 else s_t
+    elif s_t > old:
+        new = s_t
+        y = (e4m3.decode(codes[:offset]).astype(np.float32) * old).astype(np.float32)
+        codes[:offset] = e4m3.encode_fast((y / new).astype(np.float32))
+    else:
+        new = old
+    codes[offset] = e4m3.encode_fast((x / new).astype(np.float32))
+    return codes, new
+
+
+def cache_write_fp8(k_new, v_new, slots, k_codes, v_codes, k_scale, v_scale):
+    """FP8 cache write of tokens t (in order) with slot s = slots[t] >= 0:
+    append_token on block s // bs, row s % bs, for every KV head, K and V.
+    Arrays are copied; returns (k_codes, v_codes, k_scale, v_scale)."""
+    kc, vc = np.array(k_codes, copy=True), np.array(v_codes, copy=True)
+    ks, vs = np.array(k_scale, copy=True), np.array(v_scale, copy=True)
+    bs = kc.shape[2]
+    for t, s in enumerate(np.asarray(slots, dtype=np.int64)):
+        if s < 0:
+            continue
+        blk, off = int(s) // bs, int(s) % bs
+        for h in range(kc.shape[1]):
+            kc[blk, h], ks[blk, h] = append_token(kc[blk, h], ks[blk, h], off, k_new[t, h])
+            vc[blk, h], vs[blk, h] = append_token(vc[blk, h], vs[blk, h], off, v_new[t, h])
+    return kc, vc, ks, vs
