@@ -103,13 +103,43 @@ pa_status pa_get_device_error(uint32_t* err);
  *   k_cache/v_cache device bf16 pools (layout above)
  * Slots >= num_blocks * block_size are skipped and flag
  * PA_DEVERR_BAD_SLOT.  Two tokens naming the same slot give an unspecified
- * winner.  kv_dtype must be PA_KV_BF16 (FP8 append: PA_ERR_UNSUPPORTED).
+ * winner.  kv_dtype must be PA_KV_BF16 (FP8 caches: pa_cache_write_fp8,
+ * else PA_ERR_UNSUPPORTED).
  * head_dim must be a multiple of 8. */
 pa_status pa_cache_write(const void* k_new, const void* v_new,
                          const int64_t* slot_mapping, int32_t num_tokens,
                          void* k_cache, void* v_cache, int32_t num_blocks,
                          int32_t num_kv_heads, int32_t block_size,
                          int32_t head_dim, pa_kv_dtype kv_dtype, void* stream);
+
+/* pa_cache_write_fp8 -- append this step's new K/V to an FP8 E4M3 cache.
+ * "Paged Attention and KV Cache Fragmentation", section "Quantization as
+ * a way to stretch paged memory further" (FP8 KV, fp32 scales); appending
+ * into a partly filled block is this library's reading.  For each token t
+ * with s = slot_mapping[t] >= 0, block = s / block_size, offset =
+ * s % block_size, every KV head h, separately for K and V, with
+ * s_t = max|x| / 448 over the token's row x (fp32):
+ *   offset 0:          scale = s_t (1 if x is all zero)
+ *   s_t > scale:       scale = s_t; rows r < offset are requantised,
+ *                      code = e4m3(fp32(decode(code) * old) / scale)
+ *   otherwise:         the scale is kept
+ *   row offset:        code = e4m3(x / scale)
+ * (fp32 IEEE multiply and divide, E4M3 round-to-nearest-even, saturating
+ * to +-448.)  Filling a block in falling-absmax order reproduces
+ * pa_quantize_fp8 exactly; in any order the final scale is the block's.
+ *   k_new, v_new   device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping   device int64 [num_tokens]
+ *   k_cache/v_cache device uint8 E4M3 pools [num_blocks][Hkv][bs][head_dim]
+ *   k_scale/v_scale device float [num_blocks][num_kv_heads], updated
+ * The tokens of one call must name distinct blocks; slots >= num_blocks *
+ * block_size are skipped and flag PA_DEVERR_BAD_SLOT.  head_dim in
+ * {64, 128}. */
+pa_status pa_cache_write_fp8(const void* k_new, const void* v_new,
+                             const int64_t* slot_mapping, int32_t num_tokens,
+                             void* k_cache, void* v_cache, float* k_scale,
+                             float* v_scale, int32_t num_blocks,
+                             int32_t num_kv_heads, int32_t block_size,
+                             int32_t head_dim, void* stream);
 
 /* pa_copy_blocks -- copy-on-write of shared partial blocks.
  * "Paged Attention and KV Cache Fragmentation", section "How PagedAttention

@@ -153,4 +153,82 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// FP8 append ("Paged Attention and KV Cache Fragmentation", section
+// "Quantization as a way to stretch paged memory further", for the FP8
+// cache; appending into a partly filled block is this library's reading).
+// One warp per (token t, KV head h, K|V); lane l owns bytes
+// [l * D/32, (l+1) * D/32) of every row.  With s_t = absmax(x) / 448:
+//   offset 0:        scale = s_t (1 when the row is all zero)
+//   s_t > old scale: scale = s_t, and earlier rows r < offset become
+//                    e4m3(fp32(decode(code) * old) / scale)
+//   otherwise:       the scale stays
+// then the row is e4m3(x / scale) (fp32 IEEE division, RNE, satfinite).
+// Tokens of one call must name distinct blocks (a block updated by two
+// warps at once ends unspecified).
+template <int D>
+__global__ void __launch_bounds__(256)
+    cache_write_fp8_kernel(const __nv_bfloat16* __restrict__ k_new,
+                           const __nv_bfloat16* __restrict__ v_new,
+                           const int64_t* __restrict__ slots, int32_t num_tokens,
+                           uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
+                           float* __restrict__ k_scale, float* __restrict__ v_scale,
+                           int64_t num_slots, int32_t num_kv_heads, int32_t block_size) {
+  pdl_wait();  // as cache_write_kernel
+  pdl_trigger();
+  constexpr int E = D / 32;  // bytes (and elements) per lane per row
+  const int lane = threadIdx.x & 31;
+  const int64_t wid = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= static_cast<int64_t>(num_tokens) * num_kv_heads * 2) return;
+  const int kv = static_cast<int>(wid & 1);
+  const int64_t th = wid >> 1;
+  const int32_t h = static_cast<int32_t>(th % num_kv_heads);
+  const int64_t t = th / num_kv_heads;
+  const int64_t s = slots[t];
+  if (s < 0) return;
+  if (s >= num_slots) {
+    if (lane == 0 && h == 0 && kv == 0) flag_error(PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const int64_t blk = s / block_size;
+  const int32_t off = static_cast<int32_t>(s - blk * block_size);
+
+  const __nv_bfloat16* src = (kv ? v_new : k_new) + (t * num_kv_heads + h) * D + lane * E;
+  float x[E];
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; i += 2) {
+    const float2 f = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(src + i));
+    x[i] = f.x;
+    x[i + 1] = f.y;
+    a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+
+  float* sp = (kv ? v_scale : k_scale) + blk * num_kv_heads + h;
+  uint8_t* rows = (kv ? v_cache : k_cache) + (blk * num_kv_heads + h) * block_size * D + lane * E;
+  const float old = *sp;
+  const float st = __fdiv_rn(a, 448.f);
+  float sc = old;
+  if (off == 0) {
+    sc = a == 0.f ? 1.f : st;
+  } else if (st > old) {
+    sc = st;
+    for (int32_t r = 0; r < off; ++r) {
+      uint8_t* row = rows + static_cast<int64_t>(r) * D;
+#pragma unroll
+      for (int i = 0; i < E; ++i) {
+        const __half_raw hr = __nv_cvt_fp8_to_halfraw(row[i], __NV_E4M3);
+        const float y = __fmul_rn(__half2float(__half(hr)), old);
+        row[i] = __nv_cvt_float_to_fp8(__fdiv_rn(y, sc), __NV_SATFINITE, __NV_E4M3);
+      }
+    }
+  }
+  uint8_t* row = rows + static_cast<int64_t>(off) * D;
+#pragma unroll
+  for (int i = 0; i < E; ++i)
+    row[i] = __nv_cvt_float_to_fp8(__fdiv_rn(x[i], sc), __NV_SATFINITE, __NV_E4M3);
+  if (lane == 0) *sp = sc;
+}
+
 }  // namespace pa

@@ -301,6 +301,43 @@ extern "C" pa_status pa_cache_write(const void* k_new, const void* v_new,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+extern "C" pa_status pa_cache_write_fp8(const void* k_new, const void* v_new,
+                                        const int64_t* slot_mapping, int32_t num_tokens,
+                                        void* k_cache, void* v_cache, float* k_scale,
+                                        float* v_scale, int32_t num_blocks,
+                                        int32_t num_kv_heads, int32_t block_size,
+                                        int32_t head_dim, void* stream) {
+  if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_scale || !v_scale)
+    return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(k_new) & 3u) || (reinterpret_cast<uintptr_t>(v_new) & 3u) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(k_scale) & 3u) || (reinterpret_cast<uintptr_t>(v_scale) & 3u))
+    return PA_ERR_INVALID_ARG;
+  const int64_t warps = 2LL * num_tokens * num_kv_heads;
+  const int64_t grid = (warps * 32 + 255) / 256;
+  if (grid > INT_MAX) return PA_ERR_UNSUPPORTED;
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  if (head_dim == 128)
+    e = launch_pdl(cache_write_fp8_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                   s, static_cast<const __nv_bfloat16*>(k_new),
+                   static_cast<const __nv_bfloat16*>(v_new), slot_mapping, num_tokens,
+                   static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
+                   v_scale, num_slots, num_kv_heads, block_size);
+  else
+    e = launch_pdl(cache_write_fp8_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                   s, static_cast<const __nv_bfloat16*>(k_new),
+                   static_cast<const __nv_bfloat16*>(v_new), slot_mapping, num_tokens,
+                   static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
+                   v_scale, num_slots, num_kv_heads, block_size);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale,
                                     float* v_scale, const int32_t* pairs, int32_t num_pairs,
                                     int32_t num_blocks, int32_t num_kv_heads,

@@ -37,6 +37,8 @@ SIGNATURES = {
     "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "pa_cache_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_cache_write_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr,
+                                    _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr]),
     "pa_copy_blocks": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_ptr]),
     "pa_quantize_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr,
@@ -149,6 +151,23 @@ def pa_cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, stream=None):
     _check("pa_cache_write", lib().pa_cache_write(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache),
         _ptr(v_cache), nb, hkv, bs, d, _kv_dtype(k_cache), _stream(stream)))
+
+
+def pa_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                       stream=None):
+    """Append bf16 k_new/v_new [T, Hkv, d] to an E4M3 cache (uint8 pools,
+    fp32 scales [num_blocks, Hkv]) at slot_mapping[T]; grow-only scales."""
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    if _kv_dtype(k_cache) != PA_KV_FP8_E4M3:
+        raise TypeError("pa_cache_write_fp8: the cache must hold E4M3 bytes")
+    nb, hkv, bs, d = k_cache.shape
+    _check("pa_cache_write_fp8", lib().pa_cache_write_fp8(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache),
+        _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), nb, hkv, bs, d, _stream(stream)))
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):

@@ -140,3 +140,59 @@ def test_quantize_codes_agree_with_torch_cast():
     x = kc / s[:, :, None, None]
     ref = x.to(torch.float8_e4m3fn).view(torch.uint8)
     assert torch.equal(ref, kq.cpu())
+
+
+# ------------------------------------------------------------ FP8 append ---
+def _fp8_pool(nb, H, bs, d, fill, seed, dev="cuda"):
+    """An FP8 pool whose blocks [0, nb) hold `fill[b]` valid tokens, built by
+    the oracle's whole-block quantiser from seeded bf16 values (outliers
+    included), with stale bytes past each fill."""
+    x = W.normal_bf16((nb, H, bs, d), seed, "cpu", outlier_prob=0.01, outlier_scale=20.0)
+    codes, scales = OQ.quantize_blocks(x.float().numpy(), list(range(nb)), fill)
+    for b, n in enumerate(fill):
+        codes[b, :, n:] = 0x3C          # stale bytes a reused block may hold
+    return (torch.from_numpy(codes).to(dev), torch.from_numpy(scales).to(dev))
+
+
+@pytest.mark.parametrize("bs,d", [(16, 128), (8, 64), (32, 128), (16, 64)])
+def test_cache_write_fp8_bit_exact(bs, d):
+    # Several steps of one appended token per sequence, each sequence in its
+    # own block: fresh blocks (offset 0), appends under the current scale
+    # and appends that grow it (outlier tokens), against the oracle.
+    dev = "cuda"
+    nb, H, T = 24, 4, 20
+    g = np.random.default_rng(bs * 1000 + d)
+    fill = [int(x) for x in g.integers(0, bs - 3, size=nb)]
+    kq, ks = _fp8_pool(nb, H, bs, d, fill, 51)
+    vq, vs = _fp8_pool(nb, H, bs, d, fill, 52)
+    blocks = g.permutation(nb)[:T]
+    ref = [kq.cpu().numpy(), vq.cpu().numpy(), ks.cpu().numpy(), vs.cpu().numpy()]
+    for step in range(3):
+        scale = torch.ones((T, H, 1))
+        scale[::3] = 30.0               # these tokens raise their block's scale
+        kn = (W.normal_bf16((T, H, d), 60 + step).float() * scale).to(torch.bfloat16)
+        vn = (W.normal_bf16((T, H, d), 70 + step).float() * scale).to(torch.bfloat16)
+        slots = np.array([b * bs + fill[b] + step for b in blocks], dtype=np.int64)
+        slots[5] = -1                    # skipped
+        pa.pa_cache_write_fp8(kn.to(dev), vn.to(dev), torch.from_numpy(slots).to(dev),
+                              kq, vq, ks, vs)
+        ref = list(OQ.cache_write_fp8(kn.float().numpy(), vn.float().numpy(), slots, *ref))
+    torch.cuda.synchronize()
+    assert np.array_equal(kq.cpu().numpy(), ref[0])
+    assert np.array_equal(vq.cpu().numpy(), ref[1])
+    assert np.array_equal(ks.cpu().numpy(), ref[2])
+    assert np.array_equal(vs.cpu().numpy(), ref[3])
+    assert pa.pa_get_device_error() == 0
+
+
+def test_cache_write_fp8_bad_slot_is_flagged_and_skipped():
+    dev = "cuda"
+    kq, ks = _fp8_pool(4, 2, 16, 64, [3] * 4, 81)
+    vq, vs = _fp8_pool(4, 2, 16, 64, [3] * 4, 82)
+    k0, s0 = kq.clone(), ks.clone()
+    kn = W.normal_bf16((2, 2, 64), 83).to(dev)
+    pa.pa_cache_write_fp8(kn, kn, torch.tensor([4 * 16, -5], dtype=torch.int64, device=dev),
+                          kq, vq, ks, vs)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() & pa.DEVERR_BAD_SLOT
+    assert torch.equal(kq, k0) and torch.equal(ks, s0)

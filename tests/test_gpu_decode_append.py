@@ -5,7 +5,9 @@ followed by pa_decode leave (bit for bit), and so match the fp64 oracle.
 Cases cover block sizes 8 (two blocks per 16-token tile), 16 and 32, split
 and unsplit segments (automatic and 7 partitions), sequences that append
 nothing (slot -1), and a slot that is not where the table puts the last
-position (flagged, not written).
+position (flagged, not written).  The FP8 decode step (pa_cache_write_fp8
+then pa_decode) is checked against the oracle: the cache bit for bit, the
+output within the FP8 tolerance.
 """
 import pytest
 import torch
@@ -114,3 +116,59 @@ def test_misplaced_slot_is_flagged_and_not_written():
     s0 = int(case.slots[0])
     assert torch.equal(_bits(k2[s0 // w.block_size, :, s0 % w.block_size]),
                        _bits(case.k_new[0]))
+
+
+# ------------------------------------------------- FP8 step: append+decode ---
+@pytest.mark.parametrize("name", ["tiny", "llama3.1-8b", "shared_prefix_bs8"])
+def test_fp8_append_then_decode_matches_oracle(name):
+    # The FP8 decode step: the pre-step cache is the oracle's whole-block
+    # quantisation of each block's valid tokens; pa_cache_write_fp8 appends
+    # the step's tokens (grow-only scales), pa_decode reads the result.
+    import numpy as np
+    from oracle import paged_attention as OPA
+    from oracle import quantize as OQ
+    from cases import _to_np32, _to_np64
+
+    case = build_case(W.WORKLOADS[name]())
+    w = case.w
+    bs = w.block_size
+    seqs = list(range(w.num_seqs)) if w.num_seqs <= 128 else list(range(0, w.num_seqs, 8))
+    ids, kk, vv = snapshot_blocks(case, range(w.num_seqs))
+    local = {bid: i for i, bid in enumerate(ids)}
+    valid = {}
+    for b in range(w.num_seqs):
+        n0 = w.seq_lens[b] - 1                       # before the append
+        for j, x in enumerate(case.tables[b]):
+            valid[local[x]] = max(valid.get(local[x], 0), max(0, min(bs, n0 - j * bs)))
+    blocks = sorted(valid)
+    kq, ks = OQ.quantize_blocks(kk, blocks, [valid[x] for x in blocks])
+    vq, vs = OQ.quantize_blocks(vv, blocks, [valid[x] for x in blocks])
+
+    dev = "cuda"
+    shape = (w.pool_blocks, w.num_kv_heads, bs, w.head_dim)
+    gk = torch.zeros(shape, dtype=torch.uint8, device=dev)
+    gv = torch.zeros_like(gk)
+    gks = torch.ones((w.pool_blocks, w.num_kv_heads), device=dev)
+    gvs = torch.ones_like(gks)
+    idx = torch.tensor(ids, dtype=torch.int64, device=dev)
+    gk[idx], gv[idx] = torch.from_numpy(kq).to(dev), torch.from_numpy(vq).to(dev)
+    gks[idx], gvs[idx] = torch.from_numpy(ks).to(dev), torch.from_numpy(vs).to(dev)
+    out = _out(w)
+    pa.pa_cache_write_fp8(case.k_new, case.v_new, case.slots_t, gk, gv, gks, gvs)
+    pa.pa_decode(case.q, gk, gv, case.table_t, case.lens_t, w.scale, out, _workspace(w, 0),
+                 k_scale=gks, v_scale=gvs)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+
+    sl = np.array([local[s // bs] * bs + s % bs for s in case.slots], dtype=np.int64)
+    kq2, vq2, ks2, vs2 = OQ.cache_write_fp8(_to_np32(case.k_new), _to_np32(case.v_new), sl,
+                                            kq, vq, ks, vs)
+    # the cache the kernel left equals the oracle's, bit for bit
+    assert np.array_equal(gk[idx].cpu().numpy(), kq2) and np.array_equal(gv[idx].cpu().numpy(), vq2)
+    assert np.array_equal(gks[idx].cpu().numpy(), ks2) and np.array_equal(gvs[idx].cpu().numpy(), vs2)
+    tab = -np.ones((w.num_seqs, max(len(t) for t in case.tables)), dtype=np.int64)
+    for b in range(w.num_seqs):
+        tab[b, :len(case.tables[b])] = [local[x] for x in case.tables[b]]
+    ref = OPA.decode(_to_np64(case.q), kq2, vq2, tab, np.array(w.seq_lens), w.scale,
+                     k_scale=ks2, v_scale=vs2, seqs=seqs)
+    assert_close(out, ref, 5e-2, f"{name} fp8 append+decode")
