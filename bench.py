@@ -168,6 +168,30 @@ def step_inputs(w, device):
             torch.from_numpy(slots.copy()).to(device), host_us)
 
 
+def fragmentation_report(w, max_len):
+    """Host block manager's usage after the step's appends (the pages'
+    fragmentation claim): share of reserved slots holding no token, against
+    a contiguous cache reserving ``max_len`` (and the batch's own maximum)
+    per sequence."""
+    from paged_kv_cache_228_gb300 import pa
+    from paged_kv_cache_228_gb300 import workloads as W
+    alloc, tables, lens = pa.replay_script(W.build_script(w), w.num_seqs, w.block_size,
+                                           w.max_blocks_per_seq, w.pool_blocks)
+    ba = pa.BatchAppender(alloc, tables, w.max_blocks_per_seq)
+    st, _, _, _ = ba.append(lens, [1] * w.num_seqs, w.block_size)
+    assert st == pa.PA_OK
+    u = pa.allocator_usage(alloc, ba.tables, w.seq_lens, w.block_size)
+    return {
+        **u,
+        "paged_waste": 1.0 - u["tokens_stored"] / u["slots_reserved"],
+        "contiguous_waste_at_max_len": 1.0 - u["tokens_logical"] / (w.num_seqs * max_len),
+        "contiguous_waste_at_batch_max": 1.0 - u["tokens_logical"] /
+                                         (w.num_seqs * max(w.seq_lens)),
+        "max_len": max_len,
+        "sharing": u["tokens_logical"] / u["tokens_stored"],
+    }
+
+
 def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
     """Algorithmic KV bytes of one layer-step: per-token footprint
     2 * H_kv * d_h * s (one layer) for every cached token, plus, for FP8,
@@ -350,37 +374,62 @@ def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps)
 
 
 # ------------------------------------------------------------ oracle arm ---
-def oracle_sample(w, device, budget_s):
+def oracle_sample(w, device, budget_s, part=(0, 1)):
     """Time the fp64 oracle (as it stands) on whole (sequence, KV head)
-    segments of this workload for about ``budget_s`` seconds; returns
-    (GB/s, segments, seconds)."""
+    segments of this workload -- the sequences b with b % part[1] ==
+    part[0], repeated -- until about ``budget_s`` seconds of oracle time;
+    returns (GB/s, segments, seconds)."""
     from oracle import paged_attention as OPA
     from paged_kv_cache_228_gb300 import workloads as W
     tables, _, _, _, _ = step_inputs(w, "cpu")
     shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
     done_bytes, done, t_used = 0, 0, 0.0
     G = w.group
-    for b in range(w.num_seqs):
-        # only this sequence's blocks are materialised on the host
-        kb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b, device)
-        vb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b + 500, device)
-        kk = kb.float().cpu().numpy()
-        vv = vb.float().cpu().numpy()
-        qq = W.normal_bf16((w.num_q_heads, w.head_dim), w.seed * 1000 + b + 900,
-                           device).double().cpu().numpy()
-        local = np.arange(len(tables[b]))
-        for gk in range(w.num_kv_heads):
-            t0 = time.perf_counter()
-            kc = OPA.gather_sequence(kk[:, gk:gk + 1], local, w.seq_lens[b], w.block_size)[:, 0]
-            vc = OPA.gather_sequence(vv[:, gk:gk + 1], local, w.seq_lens[b], w.block_size)[:, 0]
-            for h in range(gk * G, (gk + 1) * G):
-                OPA.attend(qq[h], kc, vc, w.scale)
-            t_used += time.perf_counter() - t0
-            done += 1
-            done_bytes += w.seq_lens[b] * w.head_dim * 2 * 2
-            if t_used >= budget_s:
-                return done_bytes / t_used / 1e9, done, t_used
+    mine = [b for b in range(w.num_seqs) if b % part[1] == part[0]]
+    while mine:
+        for b in mine:
+            # only this sequence's blocks are materialised on the host
+            kb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b, device)
+            vb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b + 500, device)
+            kk = kb.float().cpu().numpy()
+            vv = vb.float().cpu().numpy()
+            qq = W.normal_bf16((w.num_q_heads, w.head_dim), w.seed * 1000 + b + 900,
+                               device).double().cpu().numpy()
+            local = np.arange(len(tables[b]))
+            for gk in range(w.num_kv_heads):
+                t0 = time.perf_counter()
+                kc = OPA.gather_sequence(kk[:, gk:gk + 1], local, w.seq_lens[b],
+                                         w.block_size)[:, 0]
+                vc = OPA.gather_sequence(vv[:, gk:gk + 1], local, w.seq_lens[b],
+                                         w.block_size)[:, 0]
+                for h in range(gk * G, (gk + 1) * G):
+                    OPA.attend(qq[h], kc, vc, w.scale)
+                t_used += time.perf_counter() - t0
+                done += 1
+                done_bytes += w.seq_lens[b] * w.head_dim * 2 * 2
+                if t_used >= budget_s:
+                    return done_bytes / t_used / 1e9, done, t_used
     return done_bytes / max(t_used, 1e-9) / 1e9, done, t_used
+
+
+def _oracle_part(args):
+    """Worker of oracle_sample_all_cores (a spawned process)."""
+    name, rank, n, budget = args
+    from paged_kv_cache_228_gb300 import workloads as W
+    gbs, segs, secs = oracle_sample(W.WORKLOADS[name](), "cpu", budget, (rank, n))
+    return gbs * secs * 1e9, segs, secs
+
+
+def oracle_sample_all_cores(name, budget_s):
+    """The oracle on every host core: one spawned process per core, each on
+    its share of the sequences (single-threaded BLAS in each); returns
+    (GB/s = all bytes / the slowest process's oracle time, segments, cores)."""
+    import multiprocessing as mp
+    n = os.cpu_count() or 1
+    with mp.get_context("spawn").Pool(n) as pool:
+        res = pool.map(_oracle_part, [(name, r, n, budget_s) for r in range(n)])
+    total = sum(r[0] for r in res)
+    return total / max(r[2] for r in res) / 1e9, sum(r[1] for r in res), n
 
 
 def run_reference(args, w):
@@ -418,7 +467,8 @@ def main():
     ap.add_argument("--workload", default="llama3.1-8b")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--fp8", action="store_true",
                     help="with --profile: run the FP8 cache path of the workload")
     ap.add_argument("--num-seqs", type=int, default=None,
@@ -482,6 +532,30 @@ def main():
     dec_s = res["decode_ms_mean"] / 1e3
     achieved = nbytes / dec_s / 1e9
     secondary = {}
+    if rank == 0 and not args.no_secondary and args.workload == "llama3.1-8b":
+        # paging tax: the same batch with contiguous physical blocks; the
+        # other report-only shapes (decode kernel pair only, logical bytes)
+        for wl in (W.contiguous(w), W.llama32_1b(), W.shared_prefix(16)):
+            r = run_native(wl, max(50, args.steps // 20), max(3, args.warmup // 10), device,
+                           profile_only=True)
+            nb = kv_bytes(wl)
+            secondary[wl.name] = {
+                "kv_bytes_per_step": nb,
+                "decode_us": r["decode_ms_mean"] * 1e3,
+                "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
+                "us_per_step": r["ms_per_step"] * 1e3,
+            }
+        secondary["fragmentation"] = {
+            w.name: fragmentation_report(w, 4096),
+            W.shared_prefix(16).name: fragmentation_report(W.shared_prefix(16), 2048 + 512),
+        }
+        c = secondary[W.contiguous(w).name]["decode_GB_per_s"]
+        secondary["paging_tax"] = {
+            "scattered_decode_GB_per_s": achieved, "contiguous_decode_GB_per_s": c,
+            "tax": 1.0 - achieved / c}
+        secondary[W.shared_prefix(16).name]["note"] = (
+            "logical bytes: the 2048-token prefix is counted once per sequence; "
+            "its blocks are read from L2 after the first")
     if rank == 0 and not args.no_secondary and args.workload != "llama3.1-70b-128k":
         wl = W.llama31_70b_128k()
         for fp8 in (False, True):
@@ -504,8 +578,13 @@ def main():
     if rank == 0:
         v, segs, secs = oracle_sample(w, "cpu", args.cpu_budget)
         cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"{segs} whole (sequence, KV head) segments of {w.name} "
-                         f"({secs:.1f} s), fp64 numpy, single-threaded BLAS"}
+               "sample": f"{segs} whole (sequence, KV head) segments of {w.name}, "
+                         f"the batch repeated ({secs:.1f} s of oracle time), fp64 numpy, "
+                         f"single-threaded BLAS"}
+        if not args.no_secondary and args.workload in W.WORKLOADS:
+            va, sega, cores = oracle_sample_all_cores(args.workload, args.cpu_budget / 3)
+            cpu["all_cores"] = {"value": va, "unit": "GB/s", "cores": cores,
+                                "sample": f"{sega} segments, one process per core"}
     e2e = res["e2e"]
     if rank == 0:
         line = {

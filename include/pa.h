@@ -353,6 +353,24 @@ pa_status pa_batch_append_slots(pa_allocator* a, int32_t* tables,
                                 int32_t* cow_pairs_out, int32_t* n_cow_out,
                                 int32_t* num_done);
 
+/* pa_allocator_usage -- how full the reserved blocks are.  "KV cache
+ * fragmentation" field guide, section "Why it matters", and "Paged
+ * Attention and KV Cache Fragmentation", section "How PagedAttention maps
+ * an OS concept onto GPU memory": a paged cache wastes at most each
+ * sequence's unfilled last block, where a contiguous one reserves every
+ * request's maximum length.  For the sequences given (host tables
+ * [num_seqs][max_blocks], lengths lens[num_seqs]):
+ *   out[0] live_blocks     blocks of the allocator with refcount > 0
+ *   out[1] slots_reserved  live_blocks * block_size
+ *   out[2] tokens_stored   distinct (block, offset) slots holding a token of
+ *                          some sequence (shared blocks counted once)
+ *   out[3] tokens_logical  sum of lens
+ * BAD_BLOCK_ID if a table entry a length reaches is not live. */
+pa_status pa_allocator_usage(const pa_allocator* a, const int32_t* tables,
+                             int32_t max_blocks, const int32_t* lens,
+                             int32_t num_seqs, int32_t block_size,
+                             int64_t* out);
+
 #ifdef __cplusplus
 }
 #endif

@@ -159,3 +159,27 @@ def replay_script(ops, num_seqs: int, block_size: int, max_blocks: int,
         else:
             raise ValueError(kind)
     return m, tables, lens
+
+
+# ------------------------------------------------------- usage report ---
+# The pages' fragmentation argument ("KV cache fragmentation" field guide,
+# section "Why it matters"; "Paged Attention and KV Cache Fragmentation",
+# section "How PagedAttention maps an OS concept onto GPU memory"): a paged
+# cache wastes at most the unfilled tail of each sequence's last block,
+# where a contiguous cache reserves each request's maximum length up front.
+# The report counts, for a set of sequences (tables + lengths):
+#   live_blocks     blocks with a nonzero refcount
+#   slots_reserved  live_blocks * block_size
+#   tokens_stored   distinct (block, offset) slots holding a token of some
+#                   sequence (a shared block counted once)
+#   tokens_logical  sum of the sequence lengths
+
+
+def usage(model: BlockManagerModel, tables, lens, block_size: int) -> dict:
+    live = sum(1 for r in model.refcount if r > 0)
+    held = set()
+    for t, n in zip(tables, lens):
+        for p in range(int(n)):
+            held.add((t[p // block_size], p % block_size))
+    return {"live_blocks": live, "slots_reserved": live * block_size,
+            "tokens_stored": len(held), "tokens_logical": int(sum(int(n) for n in lens))}

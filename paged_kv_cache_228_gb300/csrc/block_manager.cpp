@@ -185,3 +185,37 @@ extern "C" pa_status pa_batch_append_slots(pa_allocator* a, int32_t* tables,
   }
   return PA_OK;
 }
+
+extern "C" pa_status pa_allocator_usage(const pa_allocator* a, const int32_t* tables,
+                                        int32_t max_blocks, const int32_t* lens,
+                                        int32_t num_seqs, int32_t block_size, int64_t* out) {
+  if (a == nullptr || out == nullptr || num_seqs < 0 || max_blocks < 0 || block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (lens == nullptr || (max_blocks > 0 && tables == nullptr)))
+    return PA_ERR_INVALID_ARG;
+  // per block: the furthest offset any sequence fills (slots 0..fill-1 of a
+  // block hold tokens of its holders; a sequence fills its blocks from 0)
+  std::vector<int32_t> fill(a->refcount.size(), 0);
+  int64_t logical = 0;
+  for (int32_t i = 0; i < num_seqs; ++i) {
+    const int64_t n = lens[i];
+    if (n < 0 || cdiv(n, block_size) > max_blocks) return PA_ERR_INVALID_ARG;
+    logical += n;
+    const int32_t* t = tables + static_cast<int64_t>(i) * max_blocks;
+    for (int64_t j = 0; j < cdiv(n, block_size); ++j) {
+      if (!live(a, t[j])) return PA_ERR_BAD_BLOCK_ID;
+      const int64_t f = n - j * block_size < block_size ? n - j * block_size : block_size;
+      if (f > fill[t[j]]) fill[t[j]] = static_cast<int32_t>(f);
+    }
+  }
+  int64_t live_blocks = 0, stored = 0;
+  for (size_t b = 0; b < fill.size(); ++b) {
+    live_blocks += a->refcount[b] > 0;
+    stored += fill[b];
+  }
+  out[0] = live_blocks;
+  out[1] = live_blocks * block_size;
+  out[2] = stored;
+  out[3] = logical;
+  return PA_OK;
+}

@@ -64,6 +64,7 @@ SIGNATURES = {
     "pa_block_num_free": (_c_int, [_c_ptr]),
     "pa_seq_append_slots": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int,
                                      _c_ptr, _c_ptr, ctypes.POINTER(_c_int)]),
+    "pa_allocator_usage": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_ptr, _c_int, _c_int, _c_ptr]),
     "pa_batch_append_slots": (_c_int, [_c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int, _c_int,
                                        _c_ptr, _c_ptr, _c_ptr, ctypes.POINTER(_c_int)]),
 }
@@ -373,6 +374,26 @@ class BatchAppender:
         self.last_call_us = (time.perf_counter() - t0) * 1e6  # the native call alone
         pairs = [tuple(int(x) for x in self.cow[i]) for i in np.flatnonzero(self.ncow[:done.value])]
         return st, slots[:int(n_new[:done.value].sum())], pairs, done.value
+
+
+def allocator_usage(alloc: "Allocator", tables, lens, block_size: int) -> dict:
+    """pa_allocator_usage over the sequences (tables: lists or an int32
+    [B, max_blocks] array; lens: per-sequence lengths)."""
+    import numpy as np
+    if isinstance(tables, np.ndarray):
+        tab = np.ascontiguousarray(tables, dtype=np.int32)
+    else:
+        width = max([1] + [len(t) for t in tables])
+        tab = np.full((len(tables), width), -1, dtype=np.int32)
+        for b, t in enumerate(tables):
+            tab[b, :len(t)] = t
+    ln = np.ascontiguousarray(lens, dtype=np.int32)
+    out = np.zeros(4, dtype=np.int64)
+    _check("pa_allocator_usage", lib().pa_allocator_usage(
+        alloc._h, tab.ctypes.data, tab.shape[1], ln.ctypes.data, len(ln), block_size,
+        out.ctypes.data))
+    return dict(zip(("live_blocks", "slots_reserved", "tokens_stored", "tokens_logical"),
+                    (int(x) for x in out)))
 
 
 def replay_script(ops, num_seqs: int, block_size: int, max_blocks: int, num_blocks: int):

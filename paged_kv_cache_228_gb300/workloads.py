@@ -41,6 +41,7 @@ class Workload:
     outlier_scale: float = 1.0
     shared_prefix: int = 0     # tokens of a prefix shared by every sequence
     scale: float = field(default=0.0)
+    scattered: bool = True     # False: blocks handed out in order 0, 1, 2, ...
 
     def __post_init__(self):
         if not self.scale:
@@ -139,8 +140,19 @@ WORKLOADS = {
 # ------------------------------------------------------------- op script ---
 def free_order(w: Workload) -> list:
     """Seeded permutation in which a freshly allocated pool is freed, so the
-    LIFO free list hands blocks out in a scattered order."""
+    LIFO free list hands blocks out in a scattered order (or, for a
+    workload with ``scattered=False``, in order 0, 1, 2, ..., which gives
+    every sequence contiguous physical blocks)."""
+    if not w.scattered:
+        return list(range(w.pool_blocks - 1, -1, -1))
     return torch.randperm(w.pool_blocks, generator=_gen(1000 + w.seed)).tolist()
+
+
+def contiguous(w: Workload) -> Workload:
+    """The same workload with every sequence's blocks physically contiguous
+    (the paging tax is the difference between the two)."""
+    from dataclasses import replace
+    return replace(w, name=w.name + "_contiguous", scattered=False)
 
 
 def build_script(w: Workload) -> list:

@@ -192,3 +192,16 @@ def test_batch_append_matches_model(palib):
                 assert a.free(list(ba.tables[i][ba.tables[i] >= 0])) == 0
                 tm[i] = []; ba.tables[i] = -1; lens[i] = 0
     assert saw_stop
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3.1-8b", "shared_prefix_bs8"])
+def test_allocator_usage_matches_model(palib, name):
+    # the fragmentation report of a workload's pre-step state, native vs model
+    from oracle import block_manager as BM
+    from paged_kv_cache_228_gb300 import workloads as W
+    w = W.WORKLOADS[name]()
+    ops = W.build_script(w)
+    maxb = w.max_blocks_per_seq
+    m, tm, lm = BM.replay_script(ops, w.num_seqs, w.block_size, maxb, w.pool_blocks)
+    a, ta, la = palib.replay_script(ops, w.num_seqs, w.block_size, maxb, w.pool_blocks)
+    assert palib.allocator_usage(a, ta, la, w.block_size) == BM.usage(m, tm, lm, w.block_size)

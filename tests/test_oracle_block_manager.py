@@ -129,3 +129,35 @@ def test_footprint_matches_page_numbers():
         assert round(b / 1e9, 1) == float(gb)
     # one layer of the 70B / 128K request, bf16: exactly 2 * 8 * 128 * 131072 * 2
     assert footprint.decode_step_kv_bytes([131072], 8, 128, 2) == 536870912
+
+
+def test_usage_closed_forms():
+    # B private sequences of length n: ceil(n / bs) blocks each, n tokens each
+    bs, B, n = 16, 5, 37
+    m = BM.BlockManagerModel(64)
+    tables = []
+    for _ in range(B):
+        t = []
+        assert m.append_slots(t, 0, n, bs, 8)[0] == BM.OK
+        tables.append(t)
+    u = BM.usage(m, tables, [n] * B, bs)
+    assert u == {"live_blocks": B * 3, "slots_reserved": B * 48, "tokens_stored": B * n,
+                 "tokens_logical": B * n}
+    # a shared 32-token prefix (2 full blocks) forked into 4 children that
+    # each add r tokens: stored = 32 + sum(r), logical = 4 * 32 + sum(r)
+    m = BM.BlockManagerModel(64)
+    parent = []
+    m.append_slots(parent, 0, 32, bs, 8)
+    kids, lens = [], []
+    for r in (1, 16, 17, 5):
+        t = list(parent)
+        m.fork(t)
+        assert m.append_slots(t, 32, r, bs, 8)[0] == BM.OK
+        kids.append(t)
+        lens.append(32 + r)
+    m.free(parent)
+    u = BM.usage(m, kids, lens, bs)
+    assert u["tokens_stored"] == 32 + 1 + 16 + 17 + 5
+    assert u["tokens_logical"] == 4 * 32 + 39
+    assert u["live_blocks"] == 2 + (1 + 1 + 2 + 1)
+    assert u["slots_reserved"] == u["live_blocks"] * bs
