@@ -206,7 +206,7 @@ def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
 
 # ----------------------------------------------------------- native arm ---
 def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None,
-               profile_only=False):
+               profile_only=False, cascade=False):
     from paged_kv_cache_228_gb300 import pa
     from paged_kv_cache_228_gb300 import workloads as W
     per_pool = w.pool_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
@@ -219,9 +219,13 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     vn = W.normal_bf16((w.num_seqs, w.num_kv_heads, w.head_dim), w.seed * 100 + 52, device)
     out = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
                       device=device)
-    ws = torch.empty(max(16, pa.pa_decode_workspace_size(
-        w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim)), dtype=torch.uint8,
-        device=device)
+    if cascade:
+        ws_n = pa.pa_decode_cascade_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                                   w.head_dim, w.block_size, w.shared_prefix)
+    else:
+        ws_n = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads,
+                                           w.head_dim)
+    ws = torch.empty(max(16, ws_n), dtype=torch.uint8, device=device)
     scales = [(None, None)] * n_pools
     if fp8:
         qpools, scales = [], []
@@ -243,9 +247,15 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     def step(i, ev=None):
         k, v = pools[i % n_pools]
         ks, vs = scales[i % n_pools]
+        if cascade:
+            pa.pa_cache_write(kn, vn, slots, k, v, stream=stream)
         if ev is not None:
             ev[0].record(stream)
-        if fp8:
+        if cascade:
+            # the shared prefix read once for all sequences
+            pa.pa_decode_cascade(q, k, v, tab, lens, w.shared_prefix, w.scale, out, ws,
+                                 stream=stream)
+        elif fp8:
             pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks, v_scale=vs,
                          stream=stream)
         else:
@@ -474,6 +484,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="with --profile: a smaller batch of the 128K workload "
                          "(ncu captures that must stay a few GB)")
+    ap.add_argument("--cascade", action="store_true",
+                    help="with --profile on a shared_prefix workload: pa_decode_cascade")
     ap.add_argument("--profile", action="store_true",
                     help="only the warm-up and timed steps of the main workload "
                          "(for ncu captures); prints the step time")
@@ -513,9 +525,11 @@ def main():
         except ValueError:
             pass
     if args.profile:
+        if args.cascade and not w.shared_prefix:
+            ap.error("--cascade needs a shared_prefix workload")
         r = run_native(w, args.steps, args.warmup, device, fp8=args.fp8,
                        n_pools=1 if w.num_seqs * max(w.seq_lens) > 10 ** 6 else None,
-                       profile_only=True)
+                       profile_only=True, cascade=args.cascade)
         print(json.dumps({"workload": w.name, "ms_per_step": r["ms_per_step"],
                           "decode_ms_mean": r["decode_ms_mean"]}))
         return
@@ -535,11 +549,12 @@ def main():
     if rank == 0 and not args.no_secondary and args.workload == "llama3.1-8b":
         # paging tax: the same batch with contiguous physical blocks; the
         # other report-only shapes (decode kernel pair only, logical bytes)
-        for wl in (W.contiguous(w), W.llama32_1b(), W.shared_prefix(16)):
+        for wl, casc in ((W.contiguous(w), False), (W.llama32_1b(), False),
+                         (W.shared_prefix(16), False), (W.shared_prefix(16), True)):
             r = run_native(wl, max(50, args.steps // 20), max(3, args.warmup // 10), device,
-                           profile_only=True)
+                           profile_only=True, cascade=casc)
             nb = kv_bytes(wl)
-            secondary[wl.name] = {
+            secondary[wl.name + ("_cascade" if casc else "")] = {
                 "kv_bytes_per_step": nb,
                 "decode_us": r["decode_ms_mean"] * 1e3,
                 "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
@@ -556,6 +571,10 @@ def main():
         secondary[W.shared_prefix(16).name]["note"] = (
             "logical bytes: the 2048-token prefix is counted once per sequence; "
             "its blocks are read from L2 after the first")
+        secondary[W.shared_prefix(16).name + "_cascade"]["note"] = (
+            "pa_decode_cascade: the prefix's attention computed once for all 256 sequences "
+            "(tensor-core product of all query rows with the prefix), suffixes paged; "
+            "logical bytes as above")
     if rank == 0 and not args.no_secondary and args.workload != "llama3.1-70b-128k":
         wl = W.llama31_70b_128k()
         for fp8 in (False, True):

@@ -256,6 +256,41 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
                            void* out, void* workspace, size_t workspace_bytes,
                            int32_t num_splits, void* stream);
 
+/* pa_decode_cascade -- pa_decode for a batch whose sequences all start with
+ * the same prefix_len tokens in the same physical blocks (forks of one
+ * prompt): "Paged Attention and KV Cache Fragmentation", section "How
+ * PagedAttention maps an OS concept onto GPU memory", and the "KV cache
+ * fragmentation" field guide, section "Why it matters" (sequences sharing
+ * a prefix point at the same blocks).  The result equals pa_decode's
+ * (bf16 cache): softmax attention over every token of each sequence.  The
+ * prefix is read once for all sequences -- its attention partial for every
+ * (sequence, query head) is a dense product of all query rows with the
+ * prefix keys and values on the tensor cores -- and each sequence's tokens
+ * past the prefix run through the paged decode, which folds the prefix
+ * partial in by a log-sum-exp merge.
+ *   prefix_len   a multiple of 16 and of block_size, <= the table width; the
+ *                prefix blocks are read from block_tables[0] and must be
+ *                the first prefix_len / block_size entries of every row
+ *   seq_lens[b]  >= prefix_len (shorter ones give zeros and flag
+ *                PA_DEVERR_BAD_SEQ_LEN)
+ *   workspace    >= pa_decode_cascade_workspace_size() bytes (same
+ *                shapes, block_size, prefix_len and num_splits), 16-byte
+ *                aligned (no initialisation needed)
+ * other arguments as pa_decode.  prefix_len == 0 is plain pa_decode. */
+pa_status pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                           int32_t num_kv_heads, int32_t head_dim,
+                                           int32_t block_size, int32_t prefix_len,
+                                           int32_t num_splits, size_t* bytes);
+pa_status pa_decode_cascade(const void* q, const void* k_cache,
+                            const void* v_cache, const int32_t* block_tables,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t num_seqs, int32_t num_q_heads,
+                            int32_t num_kv_heads, int32_t head_dim,
+                            int32_t block_size, int32_t num_blocks,
+                            int32_t prefix_len, float scale, void* out,
+                            void* workspace, size_t workspace_bytes,
+                            int32_t num_splits, void* stream);
+
 /* pa_decode_noalloc -- pa_decode for callers that cannot allocate.
  * The pages have no counterpart: this is a library-only convenience.
  * Some callers cannot call cudaMalloc or otherwise obtain device memory:

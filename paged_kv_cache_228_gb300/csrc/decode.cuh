@@ -69,6 +69,13 @@ struct DecodeParams {
   const int64_t* slot_mapping;
   uint8_t* k_cache;
   uint8_t* v_cache;
+  // Cascade (null / 0 when off): this call's tiles start at token `skip` of
+  // every sequence, and the attention over tokens [0, skip) arrives as a
+  // partial per (sequence, query head) to fold in: pf_o[B][Hq][D]
+  // unnormalised, pf_ml[B][Hq] (max in log2 units, sum).
+  int32_t skip;
+  const float* pf_o;
+  const float2* pf_ml;
   int32_t num_seqs, num_q_heads, num_kv_heads, group, block_size, log2_bs;
   int32_t max_blocks, num_blocks;
   int32_t rows_total;  // num_blocks * num_kv_heads * block_size
@@ -113,6 +120,11 @@ __host__ __device__ constexpr size_t decode_smem_bytes(int stages) {
 
 __device__ __forceinline__ int32_t cdiv16(int32_t n) { return (n + 15) >> 4; }
 
+// Tiles of a sequence of n tokens in this call (its tokens from `skip` on).
+__device__ __forceinline__ int32_t seg_tiles(const DecodeParams& p, int32_t n) {
+  return n > p.skip ? cdiv16(n - p.skip) : 0;
+}
+
 __device__ __forceinline__ int32_t clamp_len(const DecodeParams& p, int32_t n) {
   const int32_t cap = p.max_blocks * p.block_size;
   if (n < 0 || n > cap) {
@@ -144,7 +156,7 @@ __device__ __forceinline__ void locate(const DecodeParams& p, int64_t u,
     for (int k = 0; k < 4; ++k) {
       const int32_t b0 = b00 + 32 * k;
       const int32_t n = nk[k];
-      const int64_t w = static_cast<int64_t>(p.num_kv_heads) * cdiv16(n);
+      const int64_t w = static_cast<int64_t>(p.num_kv_heads) * seg_tiles(p, n);
       int64_t incl = w;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -160,7 +172,7 @@ __device__ __forceinline__ void locate(const DecodeParams& p, int64_t u,
         const int64_t rem = u - (base + excl);
         c.b = b0 + L;
         c.n = nn;
-        c.T = cdiv16(nn);
+        c.T = seg_tiles(p, nn);
         c.g = static_cast<int32_t>(rem / c.T);
         c.tile = static_cast<int32_t>(rem % c.T);
         return;
@@ -180,7 +192,7 @@ __device__ __forceinline__ void next_segment(const DecodeParams& p, Cursor& c) {
   do {
     ++c.b;
     c.n = c.b < p.num_seqs ? clamp_len(p, p.seq_lens[c.b]) : 1;
-    c.T = cdiv16(c.n);
+    c.T = seg_tiles(p, c.n);
   } while (c.T == 0);
 }
 
@@ -202,7 +214,7 @@ __device__ __forceinline__ int64_t total_tiles(const DecodeParams& p) {
   int64_t w = 0;
 #pragma unroll 4
   for (int32_t b = lane; b < p.num_seqs; b += 32)
-    w += cdiv16(clamp_len(p, p.seq_lens[b]));
+    w += seg_tiles(p, clamp_len(p, p.seq_lens[b]));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
   return w * p.num_kv_heads;
@@ -250,7 +262,7 @@ __device__ __forceinline__ int32_t fetch_entry(const DecodeParams& p, const Load
   const int lane = threadIdx.x & 31;
   const int lr = rpt_log2(p);
   const int32_t tile = t + (lane >> lr);
-  const int32_t tok = tile * kTile + (lane & ((1 << lr) - 1)) * p.block_size;
+  const int32_t tok = p.skip + tile * kTile + (lane & ((1 << lr) - 1)) * p.block_size;
   if (tile >= ld.seg_end || tok >= ld.c.n) return -1;
   return p.block_tables[static_cast<int64_t>(ld.c.b) * p.max_blocks + (tok >> p.log2_bs)];
 }
@@ -313,7 +325,7 @@ __device__ __forceinline__ void copy_tile(const DecodeParams& p, const Maps& tm,
                                           const Bufs& sb, const Cursor& c, uint32_t stage,
                                           int32_t b0, int32_t b1) {
   using L = Smem<D, FP8>;
-  const int32_t tok = c.tile * kTile;
+  const int32_t tok = p.skip + c.tile * kTile;
   const int box_rows = p.block_size < kTile ? p.block_size : kTile;
   const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * (FP8 ? D : 128);
   const int nbox = (p.block_size < kTile && tok + p.block_size < c.n) ? 2 : 1;
@@ -818,7 +830,7 @@ __device__ __forceinline__ void load_query(const DecodeParams& p, uint32_t qslot
 // piece is the whole segment, else the unnormalised partial (o, m, l) at
 // piece index cta + b*Hkv + g.
 template <int D, bool FP8>
-__device__ __forceinline__ void finish_piece(const DecodeParams& p, const SegState<D>& s,
+__device__ __forceinline__ void finish_piece(const DecodeParams& p, SegState<D>& s,
                                              const Cursor& c, bool whole, int32_t cta) {
   const int lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -829,7 +841,43 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, const SegSta
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   const int h0 = 2 * tq, h1 = 2 * tq + 1;
-  if (whole) {
+  if (whole && p.pf_o != nullptr) {
+    // cascade: fold in the prefix partial of each head,
+    // out = (2^(m-M) acc + 2^(mp-M) op) / (2^(m-M) l + 2^(mp-M) lp)
+    const int64_t row = static_cast<int64_t>(c.b) * p.num_q_heads + c.g * p.group;
+    __nv_bfloat16* ob = p.out + row * D;
+    float a[2] = {0.f, 0.f}, ap[2] = {0.f, 0.f}, inv[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int h = k ? h1 : h0;
+      if (h < p.group) {
+        const float2 pml = p.pf_ml[row + h];
+        const float M = fmaxf(s.m[k], pml.x);
+        a[k] = fast_exp2(s.m[k] - M);
+        ap[k] = fast_exp2(pml.x - M);
+        inv[k] = 1.f / fmaf(k ? l1 : l0, a[k], pml.y * ap[k]);
+      }
+    }
+    // fold the prefix in with loads only (kept in flight together; a store
+    // between them would serialise them), then store
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = q & 1, h = k ? h1 : h0;
+        if (h < p.group)
+          s.acc[i][q] = fmaf(s.acc[i][q], a[k],
+                             p.pf_o[(row + h) * D + acc_d<D, FP8>(i, q, gq)] * ap[k]);
+      }
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int k = q & 1, h = k ? h1 : h0;
+        if (h < p.group)
+          ob[h * D + acc_d<D, FP8>(i, q, gq)] = __float2bfloat16_rn(s.acc[i][q] * inv[k]);
+      }
+  } else if (whole) {
     const float i0 = 1.f / l0, i1 = 1.f / l1;
     __nv_bfloat16* ob = p.out + (static_cast<int64_t>(c.b) * p.num_q_heads +
                                  c.g * p.group) * D;
@@ -902,7 +950,7 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
       if (!ok) break;
       const uint32_t kb = sb.ring + stage * L::kStageBytes;
       const uint32_t vb = kb + L::kKVBytes;
-      const int valid = min(kTile, c.n - tile * kTile);
+      const int valid = min(kTile, c.n - (p.skip + tile * kTile));
       if (valid < kTile) {
         // Rows past the sequence end hold stale or foreign data: zero the V
         // rows (0 * NaN would poison the MMA); K rows are masked by -inf.
@@ -1068,10 +1116,12 @@ __global__ void __launch_bounds__(32, 16)
 }
 
 // ----------------------------------------------------------------- merge --
-// Launched with one CTA per decode CTA.  Zeroes the output of empty
-// sequences (one thread per sequence), then CTA c merges the split segment
-// decode CTA c finished, if any: thread (h, d4) owns 4 output columns of
-// head h, and over the segment's pieces j
+// Launched with one CTA per decode CTA.  Writes the sequences the decode
+// grid had no tile of (one thread per sequence): zeros for empty ones, the
+// normalised prefix partial for a cascade sequence that ends at the prefix.
+// Then CTA c merges the split segment decode CTA c finished, if any: thread
+// (h, d4) owns 4 output columns of head h, and over the segment's pieces j
+// (plus, in a cascade, the prefix partial)
 //   M = max_j m_j,  out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
 // The loads over pieces are independent, so several are kept in flight.
 template <int D>
@@ -1080,12 +1130,24 @@ __global__ void __launch_bounds__(kMaxG * D / 4)
   pdl_wait();  // the decode grid's partials are complete and visible
   for (int32_t bb = blockIdx.x * blockDim.x + threadIdx.x; bb < p.num_seqs;
        bb += gridDim.x * blockDim.x) {
-    if (clamp_len(p, p.seq_lens[bb]) == 0) {
-      // a fused append needs the new token inside the sequence
-      if (p.slot_mapping != nullptr && p.slot_mapping[bb] >= 0) flag_error(PA_DEVERR_BAD_SLOT);
-      uint4* o = reinterpret_cast<uint4*>(p.out + static_cast<int64_t>(bb) * p.num_q_heads * D);
-      for (int i = 0; i < p.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
+    const int32_t n = clamp_len(p, p.seq_lens[bb]);
+    if (n > p.skip) continue;  // the decode grid covered it
+    const int64_t row = static_cast<int64_t>(bb) * p.num_q_heads;
+    if (p.pf_o != nullptr && n == p.skip) {
+      // cascade, nothing past the prefix: the prefix partial alone
+      for (int h = 0; h < p.num_q_heads; ++h) {
+        const float inv = 1.f / p.pf_ml[row + h].y;
+        for (int d = 0; d < D; ++d)
+          p.out[(row + h) * D + d] = __float2bfloat16_rn(p.pf_o[(row + h) * D + d] * inv);
+      }
+      continue;
     }
+    // empty sequence (or, in a cascade, one shorter than the prefix): zeros
+    if (n > 0) flag_error(PA_DEVERR_BAD_SEQ_LEN);
+    // a fused append needs the new token inside the sequence
+    if (p.slot_mapping != nullptr && p.slot_mapping[bb] >= 0) flag_error(PA_DEVERR_BAD_SLOT);
+    uint4* o = reinterpret_cast<uint4*>(p.out + row * D);
+    for (int i = 0; i < p.num_q_heads * D / 8; ++i) o[i] = make_uint4(0u, 0u, 0u, 0u);
   }
   if (p.ws_job == nullptr) return;
   const int2 job = p.ws_job[blockIdx.x];
@@ -1106,6 +1168,16 @@ __global__ void __launch_bounds__(kMaxG * D / 4)
   for (int k = 0; k < np; ++k) M = fmaxf(M, ml[k * kMaxG].x);
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
+  if (p.pf_o != nullptr) {
+    // cascade: the prefix partial is one more piece
+    const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + g * p.group + h;
+    const float2 pml = p.pf_ml[row];
+    const float4 x = *reinterpret_cast<const float4*>(p.pf_o + row * D + d4);
+    M = fmaxf(M, pml.x);
+    const float w = fast_exp2(pml.x - M);
+    num = make_float4(w * x.x, w * x.y, w * x.z, w * x.w);
+    den = w * pml.y;
+  }
 #pragma unroll 4
   for (int k = 0; k < np; ++k) {
     const float2 v = ml[k * kMaxG];

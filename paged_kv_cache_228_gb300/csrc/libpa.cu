@@ -12,6 +12,7 @@
 #include <mutex>
 
 #include "cache_ops.cuh"
+#include "cascade.cuh"
 #include "decode.cuh"
 #include "pa.h"
 
@@ -449,6 +450,71 @@ struct AppendArgs {
   const int64_t* slot_mapping;
 };
 
+struct CascadeArgs {
+  int32_t prefix_len;
+  float* pf_o;
+  float2* pf_ml;
+  int32_t splits;
+  int64_t stride;
+};
+
+// Token splits of the prefix pass: enough CTAs for ~3 per SM, and few
+// enough blocks per split to stage their ids in shared memory.
+int32_t prefix_splits(int sms, int64_t num_seqs, int32_t group, int32_t num_kv_heads,
+                      int32_t block_size, int32_t prefix_len) {
+  const int64_t chunks = (prefix_len + kPfChunk - 1) / kPfChunk;
+  const int64_t ctas = (num_seqs * group + kPfRows - 1) / kPfRows * num_kv_heads;
+  int64_t s = (3LL * sms + ctas - 1) / ctas;
+  const int64_t per_split_max = static_cast<int64_t>(kPfMaxBlocks - 2) * block_size / kPfChunk;
+  const int64_t s_ids = (chunks + per_split_max - 1) / per_split_max;
+  if (s < s_ids) s = s_ids;
+  if (s > chunks) s = chunks;
+  if (s < 1) s = 1;
+  return static_cast<int32_t>(s);
+}
+
+// Bytes of the prefix partials of a cascade, rounded up to 256.
+size_t prefix_partial_bytes(int32_t splits, int64_t num_seqs, int32_t num_q_heads,
+                            int32_t head_dim) {
+  const size_t b = static_cast<size_t>(splits) * num_seqs * num_q_heads *
+                   (static_cast<size_t>(head_dim) * sizeof(float) + sizeof(float2));
+  return (b + 255) & ~static_cast<size_t>(255);
+}
+
+template <int D>
+pa_status launch_prefix(const PrefixParams& pp, cudaStream_t stream) {
+  static bool attr_set[kMaxDevices] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(prefix_attention_kernel<D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               PfSmem<D>::kBytes) != cudaSuccess)
+        return PA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  const int64_t rows = static_cast<int64_t>(pp.num_seqs) * pp.group;
+  const int64_t bx = (rows + kPfRows - 1) / kPfRows;
+  if (bx > INT_MAX || pp.num_kv_heads > 65535 || pp.splits > 65535) return PA_ERR_UNSUPPORTED;
+  if (launch_pdl(prefix_attention_kernel<D>,
+                 dim3(static_cast<unsigned>(bx), static_cast<unsigned>(pp.num_kv_heads),
+                      static_cast<unsigned>(pp.splits)),
+                 dim3(kPfWarps * 32), PfSmem<D>::kBytes, stream, pp) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (pp.splits == 1) return PA_OK;
+  // one partial per row for the suffix pass
+  const int64_t warps = static_cast<int64_t>(pp.num_seqs) * pp.num_q_heads;
+  const int64_t mx = (warps * 32 + 255) / 256;
+  if (mx > INT_MAX) return PA_ERR_UNSUPPORTED;
+  return launch_pdl(prefix_merge_kernel<D>, dim3(static_cast<unsigned>(mx)), dim3(256), 0,
+                    stream, pp) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
 pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
                        const float* k_scale, const float* v_scale, pa_kv_dtype kv_dtype,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -456,7 +522,7 @@ pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                        int32_t num_blocks, float scale, void* out, void* workspace,
                        size_t workspace_bytes, int32_t num_splits, void* stream,
-                       const AppendArgs* app) {
+                       const AppendArgs* app, const CascadeArgs* cas = nullptr) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq < 0 || num_splits < 0 || !(scale == scale) ||
       num_q_heads % num_kv_heads != 0)
@@ -501,6 +567,11 @@ pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
   p.num_blocks = num_blocks;
   p.rows_total = static_cast<int32_t>(rows);
   p.scale_log2 = scale * 1.4426950408889634f;
+  if (cas != nullptr) {
+    p.skip = cas->prefix_len;
+    p.pf_o = cas->pf_o;
+    p.pf_ml = cas->pf_ml;
+  }
   if (app != nullptr) {
     p.k_new = static_cast<const uint8_t*>(app->k_new);
     p.v_new = static_cast<const uint8_t*>(app->v_new);
@@ -549,6 +620,102 @@ extern "C" pa_status pa_decode_append(const void* q, const void* k_new, const vo
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                       head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
                       num_splits, stream, &app);
+}
+
+extern "C" pa_status pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t num_q_heads,
+                                                      int32_t num_kv_heads, int32_t head_dim,
+                                                      int32_t block_size, int32_t prefix_len,
+                                                      int32_t num_splits, size_t* bytes) {
+  if (bytes == nullptr || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      block_size <= 0 || prefix_len < 0 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  size_t dec = 0;
+  const pa_status st = pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                                num_splits, &dec);
+  if (st != PA_OK) return st;
+  size_t pf = 0;
+  if (prefix_len > 0 && num_seqs > 0) {
+    int sms = 0;
+    const pa_status s2 = device_sms(&sms, nullptr);
+    if (s2 != PA_OK) return s2;
+    const int32_t sp = prefix_splits(sms, num_seqs, num_q_heads / num_kv_heads, num_kv_heads,
+                                     block_size, prefix_len);
+    pf = prefix_partial_bytes(sp, num_seqs, num_q_heads, head_dim);
+  }
+  *bytes = pf + dec;
+  return PA_OK;
+}
+
+extern "C" pa_status pa_decode_cascade(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* seq_lens, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads,
+                                       int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                       int32_t prefix_len, float scale, void* out,
+                                       void* workspace, size_t workspace_bytes,
+                                       int32_t num_splits, void* stream) {
+  if (prefix_len < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+      block_size <= 0 || max_blocks_per_seq < 0 || num_q_heads % num_kv_heads != 0)
+    return PA_ERR_INVALID_ARG;
+  if (prefix_len % kTile != 0 || prefix_len % block_size != 0 ||
+      static_cast<int64_t>(prefix_len) > static_cast<int64_t>(max_blocks_per_seq) * block_size)
+    return PA_ERR_INVALID_ARG;
+  if (prefix_len == 0 || num_seqs == 0)
+    return decode_entry(q, k_cache, v_cache, nullptr, nullptr, PA_KV_BF16, block_tables,
+                        max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                        head_dim, block_size, num_blocks, scale, out, workspace,
+                        workspace_bytes, num_splits, stream, nullptr);
+  if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
+  if (num_q_heads / num_kv_heads > kMaxG) return PA_ERR_UNSUPPORTED;
+  if (!pow2_in(block_size, 8, 256)) return PA_ERR_UNSUPPORTED;
+  if (!q || !k_cache || !v_cache || !block_tables || !workspace || !aligned16(workspace) ||
+      !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  if (!(scale == scale)) return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_blocks) * num_kv_heads * block_size > INT_MAX - 64)
+    return PA_ERR_UNSUPPORTED;
+  int sms = 0;
+  pa_status st = device_sms(&sms, nullptr);
+  if (st != PA_OK) return st;
+  const int32_t group = num_q_heads / num_kv_heads;
+  const int32_t sp = prefix_splits(sms, num_seqs, group, num_kv_heads, block_size, prefix_len);
+  const size_t pf = prefix_partial_bytes(sp, num_seqs, num_q_heads, head_dim);
+  if (workspace_bytes < pf) return PA_ERR_WORKSPACE;
+  CascadeArgs cas;
+  cas.prefix_len = prefix_len;
+  cas.splits = 1;  // the prefix merge leaves one partial per row (split 0's slot)
+  cas.stride = static_cast<int64_t>(num_seqs) * num_q_heads;
+  cas.pf_o = static_cast<float*>(workspace);
+  cas.pf_ml = reinterpret_cast<float2*>(static_cast<char*>(workspace) +
+                                        static_cast<size_t>(sp) * cas.stride * head_dim *
+                                            sizeof(float));
+  PrefixParams pp;
+  std::memset(&pp, 0, sizeof(pp));
+  pp.q = static_cast<const uint8_t*>(q);
+  pp.k_cache = static_cast<const uint8_t*>(k_cache);
+  pp.v_cache = static_cast<const uint8_t*>(v_cache);
+  pp.prefix_table = block_tables;  // sequence 0's row
+  pp.pf_o = cas.pf_o;
+  pp.pf_ml = cas.pf_ml;
+  pp.num_seqs = num_seqs;
+  pp.num_q_heads = num_q_heads;
+  pp.num_kv_heads = num_kv_heads;
+  pp.group = group;
+  pp.block_size = block_size;
+  pp.log2_bs = ilog2(block_size);
+  pp.num_blocks = num_blocks;
+  pp.prefix_tokens = prefix_len;
+  pp.prefix_chunks = (prefix_len + kPfChunk - 1) / kPfChunk;
+  pp.splits = sp;
+  pp.scale_log2 = scale * 1.4426950408889634f;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = head_dim == 128 ? launch_prefix<128>(pp, s) : launch_prefix<64>(pp, s);
+  if (st != PA_OK) return st;
+  return decode_entry(q, k_cache, v_cache, nullptr, nullptr, PA_KV_BF16, block_tables,
+                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, out,
+                      static_cast<char*>(workspace) + pf, workspace_bytes - pf, num_splits,
+                      stream, nullptr, &cas);
 }
 
 // ------------------------------------------------------------ no-alloc ---

@@ -52,6 +52,11 @@ SIGNATURES = {
                                   _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
                                   _c_int, ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int,
                                   _c_ptr]),
+    "pa_decode_cascade_workspace_size": (_c_int, [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                                  _c_int, _c_int, ctypes.POINTER(_c_size)]),
+    "pa_decode_cascade": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
+                                   _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                   ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int, _c_ptr]),
     "pa_decode_noalloc": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr,
                                    _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, ctypes.c_float, _c_ptr, _c_int, _c_ptr]),
@@ -245,6 +250,34 @@ def pa_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tabl
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, bs, nb,
         float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
+
+
+def pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                     block_size, prefix_len, num_splits=0):
+    n = _c_size(0)
+    _check("pa_decode_cascade_workspace_size", lib().pa_decode_cascade_workspace_size(
+        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, prefix_len, num_splits,
+        ctypes.byref(n)))
+    return n.value
+
+
+def pa_decode_cascade(q, k_cache, v_cache, block_tables, seq_lens, prefix_len, scale, out,
+                      workspace, num_splits=0, stream=None):
+    """pa_decode for a batch whose sequences share their first prefix_len
+    tokens (the same physical blocks): the prefix is read once."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    if k_cache.dtype != torch.bfloat16 or v_cache.dtype != torch.bfloat16:
+        raise ValueError("pa_decode_cascade: the cache must be bf16")
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("pa_decode_cascade", lib().pa_decode_cascade(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), B, hq, hkv, d, bs, nb, int(prefix_len), float(scale), _ptr(out),
+        _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024

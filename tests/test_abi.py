@@ -75,6 +75,11 @@ def test_host_validation_without_gpu(palib):
                               16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_UNSUPPORTED
     assert L.pa_decode_append(None, None, None, None, None, None, None, 1, None, 0, 4, 2, 64,
                               16, 8, 1.0, None, None, 0, 0, None) == palib.PA_OK
+    # cascade: the prefix must be a multiple of 16 and of the block size
+    assert L.pa_decode_cascade(None, None, None, None, 8, None, 1, 4, 2, 64, 16, 8, 24, 1.0,
+                               None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_decode_cascade(None, None, None, None, 8, None, 1, 4, 2, 64, 32, 8, 16, 1.0,
+                               None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
 
 
 def _compare_models(pa, seed, steps=2000, N=48, bs=4):
