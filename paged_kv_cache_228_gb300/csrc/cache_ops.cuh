@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(256)
 // Tokens of one call must name distinct blocks (a block updated by two
 // warps at once ends unspecified).
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 1)
     cache_write_fp8_kernel(const __nv_bfloat16* __restrict__ k_new,
                            const __nv_bfloat16* __restrict__ v_new,
                            const int64_t* __restrict__ slots, int32_t num_tokens,

@@ -1125,7 +1125,7 @@ __global__ void __launch_bounds__(32, 16)
 //   M = max_j m_j,  out = sum_j 2^(m_j - M) o_j / sum_j 2^(m_j - M) l_j.
 // The loads over pieces are independent, so several are kept in flight.
 template <int D>
-__global__ void __launch_bounds__(kMaxG * D / 4)
+__global__ void __launch_bounds__(kMaxG * D / 4, 1)
     paged_decode_merge_kernel(const DecodeParams p) {
   pdl_wait();  // the decode grid's partials are complete and visible
   for (int32_t bb = blockIdx.x * blockDim.x + threadIdx.x; bb < p.num_seqs;
