@@ -295,51 +295,71 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     if profile_only:
         return {"ms_per_step": total_ms / steps, "decode_ms_mean": statistics.mean(dec_ms)}
 
-    # CUDA-graph replay of one step per pool (launch overhead amortised)
-    graph_ms = None
+    # The headline timed region: exactly `steps` steps, each replayed from a
+    # CUDA graph of that step's launches (one graph per layer pool).
+    graphs = []
     try:
-        g = torch.cuda.CUDAGraph()
         s2 = torch.cuda.Stream()
         s2.wait_stream(stream)
         with torch.cuda.stream(s2):
-            with torch.cuda.graph(g, stream=s2):
-                for i in range(n_pools):
-                    k, v = pools[i]
-                    ks, vs = scales[i]
+            for i in range(n_pools):
+                g = torch.cuda.CUDAGraph()
+                k, v = pools[i]
+                ks, vs = scales[i]
+                with torch.cuda.graph(g, stream=s2):
                     if fp8:
                         pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks,
                                      v_scale=vs, stream=s2)
                     else:
                         pa.pa_decode_append(q, kn, vn, slots, k, v, tab, lens, w.scale, out,
                                             ws, stream=s2)
+                graphs.append(g)
         stream.wait_stream(s2)
-        reps = max(1, steps // n_pools)
-        for _ in range(3):
-            g.replay()
+        for i in range(max(3, warmup)):
+            graphs[i % n_pools].replay()
         torch.cuda.synchronize()
+    except Exception as e:  # no graph: the eager loop above is the figure
+        graphs = f"unavailable: {type(e).__name__}: {e}"
+    graph_ms = None
+    clocks = None
+    if isinstance(graphs, list):
+        if torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        sampler = sample_clocks() if sample_clocks else None
+        if sampler:
+            time.sleep(0.3)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record(stream)
-        for _ in range(reps):
-            g.replay()
+        for i in range(steps):
+            graphs[i % n_pools].replay()
         b.record(stream)
         torch.cuda.synchronize()
-        graph_ms = a.elapsed_time(b) / (reps * n_pools)
-    except Exception as e:  # graph capture is an extra figure only
-        graph_ms = f"unavailable: {type(e).__name__}: {e}"
+        if sampler:
+            sampler.stop()
+            clocks = sampler.summary()
+        if torch.distributed.is_initialized():
+            torch.distributed.barrier()
+        graph_ms = a.elapsed_time(b) / steps
+        err = pa.pa_get_device_error()
+        if err:
+            raise RuntimeError(f"device error word 0x{err:x} during the graph replays")
 
     # end to end through the public API with host buffers
     e2e = run_e2e(w, pools[0], scales[0], tab, lens, slots, q, kn, vn, ws, fp8, stream,
                   max(20, min(steps, 2000)))
     return {
-        "ms_per_step": total_ms / steps,
+        "ms_per_step": graph_ms if graph_ms is not None else total_ms / steps,
+        "eager_ms_per_step": total_ms / steps,
+        "timed": "graph" if graph_ms is not None else "eager",
         "decode_ms_mean": statistics.mean(dec_ms),
         "decode_ms_median": statistics.median(dec_ms),
-        "graph_ms_per_step": graph_ms,
+        "graph_ms_per_step": graph_ms if graph_ms is not None else graphs,
         "host_append_us": host_us,
         "n_pools": n_pools,
         "pool_bytes": per_pool // (2 if fp8 else 1),
-        "clocks": sampler.summary() if sampler else None,
+        "clocks": clocks if clocks is not None else (sampler.summary() if sampler else None),
         "e2e": e2e,
         "launches_per_step": 2,  # decode (with the fused cache write) + merge
     }
@@ -620,20 +640,22 @@ def main():
                       f"{res['pool_bytes'] / 1e9:.2f} GB",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
                 "step": "pa_decode_append: cache write fused into the decode launch, "
-                        "+ merge launch; eager launches",
+                        "+ merge launch",
+                "timing": ("each timed step replays a CUDA graph of its launches"
+                           if res["timed"] == "graph" else "eager launches"),
             },
             "seqs_per_s": w.num_seqs * ws / step_s,
             "us_per_step": step_s * 1e6,
             "hbm_frac": value / ws / peak,
-            "graph_us_per_step": (res["graph_ms_per_step"] * 1e3
-                                  if isinstance(res["graph_ms_per_step"], float)
-                                  else res["graph_ms_per_step"]),
+            "eager_us_per_step": res["eager_ms_per_step"] * 1e3,
+            "eager_value": nbytes / res["eager_ms_per_step"] * 1e3 / 1e9 * ws,
             "host_block_manager_us_per_step": res["host_append_us"],
             "host_block_manager_us_per_append": res["host_append_us"] / w.num_seqs,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic(w.name),
                          "kernel": "paged_decode_ws_kernel<128,bf16> (fused append) + merge "
-                                   "(per launch pair)",
+                                   "(per launch pair, CUDA events around each eager call "
+                                   "over a timed loop of the same steps)",
                          "peak_source": peak_kind},
             "cpu_baseline": cpu,
             "e2e": {"value": nbytes / (e2e["ms_per_step"] / 1e3) / 1e9, "unit": "GB/s",
