@@ -458,13 +458,14 @@ struct CascadeArgs {
   int64_t stride;
 };
 
-// Token splits of the prefix pass: enough CTAs for ~3 per SM, and few
-// enough blocks per split to stage their ids in shared memory.
+// Token splits of the prefix pass: as many as one wave of CTAs allows (3
+// resident per SM), and enough that each split's block ids fit in shared
+// memory.
 int32_t prefix_splits(int sms, int64_t num_seqs, int32_t group, int32_t num_kv_heads,
                       int32_t block_size, int32_t prefix_len) {
   const int64_t chunks = (prefix_len + kPfChunk - 1) / kPfChunk;
   const int64_t ctas = (num_seqs * group + kPfRows - 1) / kPfRows * num_kv_heads;
-  int64_t s = (3LL * sms + ctas - 1) / ctas;
+  int64_t s = 3LL * sms / ctas;
   const int64_t per_split_max = static_cast<int64_t>(kPfMaxBlocks - 2) * block_size / kPfChunk;
   const int64_t s_ids = (chunks + per_split_max - 1) / per_split_max;
   if (s < s_ids) s = s_ids;
