@@ -58,6 +58,16 @@ def dist_env():
     return ws, rank, local
 
 
+def replica_value(step_s, nbytes, ws, device):
+    """Whole-job figure of N independent replicas: the slowest rank's step
+    time (max over ranks) and the bytes of all ranks per that time, GB/s."""
+    if ws > 1:
+        t = torch.tensor([step_s], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_s = float(t.item())
+    return step_s, nbytes * ws / step_s / 1e9
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -557,11 +567,7 @@ def main():
                      sample_clocks=(lambda: ClockSampler(gpu_index)) if rank == 0 else None)
     nbytes = kv_bytes(w)
     step_s = res["ms_per_step"] / 1e3
-    if ws > 1:
-        t = torch.tensor([step_s], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_s = float(t.item())
-    value = nbytes * ws / step_s / 1e9
+    step_s, value = replica_value(step_s, nbytes, ws, device)
     peak, peak_kind = peaks()
     dec_s = res["decode_ms_mean"] / 1e3
     achieved = nbytes / dec_s / 1e9
