@@ -159,6 +159,31 @@ def test_decode_parity_fp8(name, bs):
     assert pa.pa_get_device_error() == 0
 
 
+@pytest.mark.parametrize("bs", [16, 8])
+def test_decode_parity_fp8_large_v_scales(bs):
+    # Every other block's V is scaled by 300 (V scales up to ~0.7): FP8
+    # tiles whose V scale is >= 0.5 take the normalised-P path, the rest
+    # put the scale into P; both mix within a sequence (and, at bs 8,
+    # within a tile).
+    w = W.shared_prefix(bs, num_seqs=24, prefix=256) if bs == 8 else W.llama32_1b(24)
+    case = build_case(w)
+    case.v_cache[::2] = (case.v_cache[::2].float() * 300.0).to(torch.bfloat16)
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
+    ref, (blocks, vl, ids) = oracle_decode_fp8(case, snap, seqs)
+    phys = torch.tensor([ids[b] for b in blocks], dtype=torch.int32, device="cuda")
+    kq = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device="cuda")
+    vq = torch.zeros_like(kq)
+    ks = torch.ones((w.pool_blocks, w.num_kv_heads), device="cuda")
+    vs = torch.ones_like(ks)
+    pa.pa_quantize_fp8(case.k_cache, case.v_cache, phys,
+                       torch.tensor(vl, dtype=torch.int32, device="cuda"), kq, vq, ks, vs)
+    assert float(vs.max()) >= 0.5 and float(vs[phys.long()].min()) < 0.5
+    out = run_step(case, write=False, k_cache=kq, v_cache=vq, k_scale=ks, v_scale=vs)
+    assert_close(out, ref, TOL_FP8, f"fp8 large V scales bs{bs}")
+    assert pa.pa_get_device_error() == 0
+
+
 def test_seq_len_one_returns_v_exactly():
     w = W.Workload("one", 6, 16, 4, 128, 16, seq_lens=[1] * 6, pool_blocks=64, seed=9)
     case = build_case(w)
