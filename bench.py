@@ -202,6 +202,38 @@ def fragmentation_report(w, max_len):
     }
 
 
+def offload_figure(w, device, reps=5):
+    """Swap the batch's blocks out to pinned host memory and back in
+    (pa_swap_out / pa_swap_in, zero-copy over the host link): GB/s each way."""
+    from paged_kv_cache_228_gb300 import pa
+    from paged_kv_cache_228_gb300 import workloads as W
+    tables, _, _, _, _ = step_inputs(w, "cpu")
+    used = sorted({b for t in tables for b in t})
+    ids = torch.tensor(used, dtype=torch.int32, device=device)
+    shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    k = W.normal_bf16(shape, w.seed * 10 + 1, device)
+    v = W.normal_bf16(shape, w.seed * 10 + 2, device)
+    hk = torch.empty((len(used),) + shape[1:], dtype=torch.bfloat16, pin_memory=True)
+    hv = torch.empty_like(hk, pin_memory=True)
+    nbytes = 2 * hk.numel() * hk.element_size()
+    out = {"blocks": len(used), "bytes": nbytes}
+    for name, fn in (("out", lambda: pa.pa_swap_out(k, v, ids, hk, hv)),
+                     ("in", lambda: pa.pa_swap_in(hk, hv, ids, k, v))):
+        fn()
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize()
+        out[name + "_GB_per_s"] = nbytes * reps / (a.elapsed_time(b) / 1e3) / 1e9
+    if pa.pa_get_device_error():
+        raise RuntimeError("device error during the swap figure")
+    return out
+
+
 def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
     """Algorithmic KV bytes of one layer-step: per-token footprint
     2 * H_kv * d_h * s (one layer) for every cached token, plus, for FP8,
@@ -586,6 +618,10 @@ def main():
                 "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
                 "us_per_step": r["ms_per_step"] * 1e3,
             }
+        secondary["offload"] = offload_figure(w, device)
+        secondary["offload"]["note"] = (
+            "pa_swap_out / pa_swap_in of every block the 8B batch uses, between HBM and "
+            "pinned host memory read and written in place by the kernel")
         secondary["fragmentation"] = {
             w.name: fragmentation_report(w, 4096),
             W.shared_prefix(16).name: fragmentation_report(W.shared_prefix(16), 2048 + 512),

@@ -141,6 +141,37 @@ pa_status pa_cache_write_fp8(const void* k_new, const void* v_new,
                              int32_t num_kv_heads, int32_t block_size,
                              int32_t head_dim, void* stream);
 
+/* pa_swap_out / pa_swap_in -- move whole cache blocks to host memory and
+ * back.  "Paged Attention and KV Cache Fragmentation", section
+ * "Offloading paged KV blocks to CPU DRAM and NVMe": blocks can move down
+ * to host memory for headroom and come back when needed.  For i < num_ids and
+ * b = block_ids[i]:
+ *   swap_out: host_k[i] = k_cache[b], host_v[i] = v_cache[b] (all heads,
+ *             slots and columns), and for FP8 caches host_k_scale[i][h] =
+ *             k_scale[b][h] (likewise v);
+ *   swap_in:  the reverse, into block b.
+ * The host buffers ([num_ids][num_kv_heads][block_size][head_dim] of the
+ * cache's element type, and [num_ids][num_kv_heads] floats) must be pinned
+ * (cudaHostAlloc / cudaHostRegister) or managed: the kernel reads or
+ * writes them in place, over NVLink-C2C on a Grace host, with no per-block
+ * copy calls.  block_ids is device int32; ids outside the pool are skipped
+ * and flag PA_DEVERR_BAD_BLOCK_ID.  Caches and host buffers 16-byte
+ * aligned; head_dim * element size a multiple of 16.  Asynchronous on
+ * `stream`; the host data is complete when the stream has reached it. */
+pa_status pa_swap_out(const void* k_cache, const void* v_cache,
+                      const float* k_scale, const float* v_scale,
+                      const int32_t* block_ids, int32_t num_ids, void* host_k,
+                      void* host_v, float* host_k_scale, float* host_v_scale,
+                      int32_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim,
+                      pa_kv_dtype kv_dtype, void* stream);
+pa_status pa_swap_in(const void* host_k, const void* host_v,
+                     const float* host_k_scale, const float* host_v_scale,
+                     const int32_t* block_ids, int32_t num_ids, void* k_cache,
+                     void* v_cache, float* k_scale, float* v_scale,
+                     int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                     int32_t head_dim, pa_kv_dtype kv_dtype, void* stream);
+
 /* pa_copy_blocks -- copy-on-write of shared partial blocks.
  * "Paged Attention and KV Cache Fragmentation", section "How PagedAttention
  * maps an OS concept onto GPU memory": sequences sharing physical blocks

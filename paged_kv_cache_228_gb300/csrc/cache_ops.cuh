@@ -231,4 +231,86 @@ __global__ void __launch_bounds__(256, 1)
   if (lane == 0) *sp = sc;
 }
 
+// Block swap between the device pools and host memory the GPU addresses
+// directly ("Paged Attention and KV Cache Fragmentation", section
+// "Offloading paged KV blocks to CPU DRAM and NVMe": blocks move down to
+// host memory for headroom and back).  On
+// a GB300 the host side sits behind NVLink-C2C, so the kernel reads or
+// writes it in place (zero-copy) instead of issuing a copy per block.
+// Listed block i <-> host slot i ([num_ids][Hkv][bs][row bytes] for K and
+// for V, and [num_ids][Hkv] FP8 scales).  16-byte chunks, grid-stride, four
+// in flight per thread.
+__global__ void __launch_bounds__(256)
+    swap_blocks_kernel(uint4* __restrict__ dev_k, uint4* __restrict__ dev_v,
+                       float* __restrict__ dev_ks, float* __restrict__ dev_vs,
+                       uint4* __restrict__ host_k, uint4* __restrict__ host_v,
+                       float* __restrict__ host_ks, float* __restrict__ host_vs,
+                       const int32_t* __restrict__ block_ids, int32_t num_ids,
+                       int32_t num_blocks, int32_t num_kv_heads, int64_t block_chunks,
+                       bool to_host) {
+  pdl_wait();
+  pdl_trigger();
+  const int64_t per_id = 2 * block_chunks;  // K and V chunks of one block
+  const int64_t total = per_id * num_ids;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t base = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; base < total;
+       base += 4 * stride) {
+    uint4 v[4];
+    int64_t dst[4];
+    bool ok[4];
+    int kv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int64_t i = base + u * stride;
+      ok[u] = false;
+      if (i >= total) continue;
+      const int64_t id = i / per_id;
+      const int64_t r = i - id * per_id;
+      kv[u] = r >= block_chunks;
+      const int64_t c = kv[u] ? r - block_chunks : r;
+      const int32_t blk = block_ids[id];
+      if (blk < 0 || blk >= num_blocks) {
+        if (r == 0) flag_error(PA_DEVERR_BAD_BLOCK_ID);
+        continue;
+      }
+      const int64_t dev = static_cast<int64_t>(blk) * block_chunks + c;
+      const int64_t host = id * block_chunks + c;
+      ok[u] = true;
+      if (to_host) {
+        v[u] = (kv[u] ? dev_v : dev_k)[dev];
+        dst[u] = host;
+      } else {
+        v[u] = (kv[u] ? host_v : host_k)[host];
+        dst[u] = dev;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (!ok[u]) continue;
+      if (to_host)
+        (kv[u] ? host_v : host_k)[dst[u]] = v[u];
+      else
+        (kv[u] ? dev_v : dev_k)[dst[u]] = v[u];
+    }
+  }
+  // FP8 scales: one float per (block, head), K and V
+  if (dev_ks != nullptr) {
+    const int64_t ns = static_cast<int64_t>(num_ids) * num_kv_heads;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < ns;
+         i += stride) {
+      const int64_t id = i / num_kv_heads, h = i - id * num_kv_heads;
+      const int32_t blk = block_ids[id];
+      if (blk < 0 || blk >= num_blocks) continue;
+      const int64_t d = static_cast<int64_t>(blk) * num_kv_heads + h;
+      if (to_host) {
+        host_ks[i] = dev_ks[d];
+        host_vs[i] = dev_vs[d];
+      } else {
+        dev_ks[d] = host_ks[i];
+        dev_vs[d] = host_vs[i];
+      }
+    }
+  }
+}
+
 }  // namespace pa

@@ -369,6 +369,93 @@ extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+namespace pa {
+namespace {
+
+// The address a kernel uses for a host buffer: pinned (page-locked or
+// registered) or managed memory only.
+bool host_device_ptr(const void* p, void** out) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged) return false;
+  *out = a.devicePointer != nullptr ? a.devicePointer : const_cast<void*>(p);
+  return true;
+}
+
+pa_status swap_blocks(void* k_cache, void* v_cache, float* k_scale, float* v_scale,
+                      const int32_t* block_ids, int32_t num_ids, void* host_k, void* host_v,
+                      float* host_ks, float* host_vs, int32_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim, pa_kv_dtype kv_dtype, void* stream,
+                      bool to_host) {
+  if (num_ids < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0)
+    return PA_ERR_INVALID_ARG;
+  int esz;
+  const bool fp8 = kv_dtype == PA_KV_FP8_E4M3;
+  if (kv_dtype == PA_KV_BF16)
+    esz = 2;
+  else if (fp8)
+    esz = 1;
+  else
+    return PA_ERR_INVALID_ARG;
+  if ((head_dim * esz) % 16 != 0) return PA_ERR_INVALID_ARG;
+  if (num_ids == 0) return PA_OK;
+  if (!k_cache || !v_cache || !block_ids || !host_k || !host_v || !aligned16(k_cache) ||
+      !aligned16(v_cache) || !aligned16(host_k) || !aligned16(host_v) ||
+      (reinterpret_cast<uintptr_t>(block_ids) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (fp8 && (!k_scale || !v_scale || !host_ks || !host_vs)) return PA_ERR_INVALID_ARG;
+  void *hk = nullptr, *hv = nullptr, *hks = nullptr, *hvs = nullptr;
+  if (!host_device_ptr(host_k, &hk) || !host_device_ptr(host_v, &hv)) return PA_ERR_INVALID_ARG;
+  if (fp8 && (!host_device_ptr(host_ks, &hks) || !host_device_ptr(host_vs, &hvs)))
+    return PA_ERR_INVALID_ARG;
+  int sms = 0;
+  const pa_status st = device_sms(&sms, nullptr);
+  if (st != PA_OK) return st;
+  const int64_t block_chunks = static_cast<int64_t>(num_kv_heads) * block_size * head_dim * esz / 16;
+  const int64_t total = 2 * block_chunks * num_ids;
+  int64_t grid = (total + 4 * 256 - 1) / (4 * 256);
+  if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
+  if (grid < 1) grid = 1;
+  return launch_pdl(swap_blocks_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                    static_cast<cudaStream_t>(stream), static_cast<uint4*>(k_cache),
+                    static_cast<uint4*>(v_cache), fp8 ? k_scale : nullptr,
+                    fp8 ? v_scale : nullptr, static_cast<uint4*>(hk), static_cast<uint4*>(hv),
+                    static_cast<float*>(hks), static_cast<float*>(hvs), block_ids, num_ids,
+                    num_blocks, num_kv_heads, block_chunks, to_host) == cudaSuccess
+             ? PA_OK
+             : PA_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_swap_out(const void* k_cache, const void* v_cache, const float* k_scale,
+                                 const float* v_scale, const int32_t* block_ids, int32_t num_ids,
+                                 void* host_k, void* host_v, float* host_k_scale,
+                                 float* host_v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                                 int32_t block_size, int32_t head_dim, pa_kv_dtype kv_dtype,
+                                 void* stream) {
+  return swap_blocks(const_cast<void*>(k_cache), const_cast<void*>(v_cache),
+                     const_cast<float*>(k_scale), const_cast<float*>(v_scale), block_ids,
+                     num_ids, host_k, host_v, host_k_scale, host_v_scale, num_blocks,
+                     num_kv_heads, block_size, head_dim, kv_dtype, stream, true);
+}
+
+extern "C" pa_status pa_swap_in(const void* host_k, const void* host_v,
+                                const float* host_k_scale, const float* host_v_scale,
+                                const int32_t* block_ids, int32_t num_ids, void* k_cache,
+                                void* v_cache, float* k_scale, float* v_scale,
+                                int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
+                                int32_t head_dim, pa_kv_dtype kv_dtype, void* stream) {
+  return swap_blocks(k_cache, v_cache, k_scale, v_scale, block_ids, num_ids,
+                     const_cast<void*>(host_k), const_cast<void*>(host_v),
+                     const_cast<float*>(host_k_scale), const_cast<float*>(host_v_scale),
+                     num_blocks, num_kv_heads, block_size, head_dim, kv_dtype, stream, false);
+}
+
 extern "C" pa_status pa_quantize_fp8(const void* k_src, const void* v_src,
                                      const int32_t* block_ids, const int32_t* valid_lens,
                                      int32_t num_ids, uint8_t* k_dst, uint8_t* v_dst,

@@ -39,6 +39,10 @@ SIGNATURES = {
                                 _c_int, _c_int, _c_int, _c_int, _c_ptr]),
     "pa_cache_write_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr,
                                     _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_swap_out": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                             _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr]),
+    "pa_swap_in": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr,
+                            _c_ptr, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_ptr]),
     "pa_copy_blocks": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_int,
                                 _c_int, _c_int, _c_int, _c_int, _c_ptr]),
     "pa_quantize_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr,
@@ -174,6 +178,29 @@ def pa_cache_write_fp8(k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_
     _check("pa_cache_write_fp8", lib().pa_cache_write_fp8(
         _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k_cache),
         _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), nb, hkv, bs, d, _stream(stream)))
+
+
+def pa_swap_out(k_cache, v_cache, block_ids, host_k, host_v, k_scale=None, v_scale=None,
+                host_k_scale=None, host_v_scale=None, stream=None):
+    """Copy the listed blocks (device int32 ids) of the pools into pinned
+    host tensors [n, Hkv, bs, d] (and FP8 scales [n, Hkv])."""
+    _need(block_ids, torch.int32, "block_ids", 1)
+    nb, hkv, bs, d = k_cache.shape
+    _check("pa_swap_out", lib().pa_swap_out(
+        _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_ids),
+        block_ids.shape[0], _ptr(host_k), _ptr(host_v), _ptr(host_k_scale),
+        _ptr(host_v_scale), nb, hkv, bs, d, _kv_dtype(k_cache), _stream(stream)))
+
+
+def pa_swap_in(host_k, host_v, block_ids, k_cache, v_cache, host_k_scale=None,
+               host_v_scale=None, k_scale=None, v_scale=None, stream=None):
+    """The reverse of pa_swap_out: pinned host slots i -> blocks block_ids[i]."""
+    _need(block_ids, torch.int32, "block_ids", 1)
+    nb, hkv, bs, d = k_cache.shape
+    _check("pa_swap_in", lib().pa_swap_in(
+        _ptr(host_k), _ptr(host_v), _ptr(host_k_scale), _ptr(host_v_scale), _ptr(block_ids),
+        block_ids.shape[0], _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), nb,
+        hkv, bs, d, _kv_dtype(k_cache), _stream(stream)))
 
 
 def pa_copy_blocks(k_cache, v_cache, pairs, k_scale=None, v_scale=None, stream=None):

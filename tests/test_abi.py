@@ -75,6 +75,11 @@ def test_host_validation_without_gpu(palib):
                               16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_UNSUPPORTED
     assert L.pa_decode_append(None, None, None, None, None, None, None, 1, None, 0, 4, 2, 64,
                               16, 8, 1.0, None, None, 0, 0, None) == palib.PA_OK
+    # swap: missing buffers are rejected before any CUDA call
+    assert L.pa_swap_out(None, None, None, None, None, 3, None, None, None, None, 8, 2, 16, 64,
+                         palib.PA_KV_BF16, None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_swap_in(None, None, None, None, None, 0, None, None, None, None, 8, 2, 16, 64,
+                        palib.PA_KV_BF16, None) == palib.PA_OK
     # cascade: the prefix must be a multiple of 16 and of the block size
     assert L.pa_decode_cascade(None, None, None, None, 8, None, 1, 4, 2, 64, 16, 8, 24, 1.0,
                                None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
