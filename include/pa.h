@@ -276,7 +276,7 @@ pa_status pa_decode(const void* q, const void* k_cache, const void* v_cache,
  * of position seq_lens[b] - 1 (block_tables[b][(n-1)/bs] * bs + (n-1) % bs,
  * as the block manager returns it), and that block must be private to b
  * (copy-on-write done).  A slot elsewhere, or on an empty sequence, is not
- * written and flags PA_DEVERR_BAD_SLOT.  FP8 caches: PA_ERR_UNSUPPORTED. */
+ * written and flags PA_DEVERR_BAD_SLOT.  FP8 caches: pa_decode_append_fp8. */
 pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
                            const int64_t* slot_mapping, void* k_cache,
                            void* v_cache, const int32_t* block_tables,
@@ -286,6 +286,27 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
                            int32_t block_size, int32_t num_blocks, float scale,
                            void* out, void* workspace, size_t workspace_bytes,
                            int32_t num_splits, void* stream);
+
+/* pa_decode_append_fp8 -- pa_decode_append for an FP8 E4M3 cache: the same
+ * cache (codes and scales) and output as
+ *     pa_cache_write_fp8(k_new, v_new, slot_mapping, num_seqs, ...);
+ *     pa_decode(q, k_cache, v_cache, k_scale, v_scale, PA_KV_FP8_E4M3, ...);
+ * bit for bit.  The CTA that copies sequence b's last tile first quantises
+ * the new row into its block (growing the block's scale and requantising
+ * its earlier rows when needed), which is exact only when that tile holds
+ * the whole block: block_size must be 8 or 16 (else PA_ERR_UNSUPPORTED).
+ * k_scale / v_scale are read and updated.  Other arguments and
+ * requirements as pa_decode_append. */
+pa_status pa_decode_append_fp8(const void* q, const void* k_new, const void* v_new,
+                               const int64_t* slot_mapping, void* k_cache,
+                               void* v_cache, float* k_scale, float* v_scale,
+                               const int32_t* block_tables,
+                               int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                               int32_t num_seqs, int32_t num_q_heads,
+                               int32_t num_kv_heads, int32_t head_dim,
+                               int32_t block_size, int32_t num_blocks, float scale,
+                               void* out, void* workspace, size_t workspace_bytes,
+                               int32_t num_splits, void* stream);
 
 /* pa_decode_cascade -- pa_decode for a batch whose sequences all start with
  * the same prefix_len tokens in the same physical blocks (forks of one

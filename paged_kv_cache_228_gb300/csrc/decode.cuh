@@ -398,10 +398,123 @@ __device__ __forceinline__ void store_new_token(const DecodeParams& p, const Loa
   __syncwarp();
 }
 
+// FP8 version of store_new_token (block_size <= 16, so the tile holds the
+// whole block of the new token): lane l < 2 * D / 8 holds 8 bf16 values of
+// the K (l < D / 8) or V row.  With the token's own scale s_t = absmax /
+// 448: offset 0 sets the block's scale to s_t (1 for a zero row); a larger
+// s_t raises it and requantises the block's earlier rows through fp32
+// (decode * old / new, RNE satfinite); then the row is e4m3(x / scale).
+// Each lane owns the same 8 bytes of every row.  `sc` (this tile's scales:
+// x / y = K of the first / second block, z / w = V) gets the new scale.
+// The new row is loaded here rather than at the segment's start: the
+// single-warp FP8 kernel has no registers to keep it live across the tiles.
+template <int D>
+__device__ __forceinline__ void store_new_token_fp8(const DecodeParams& p, const Cursor& c,
+                                                 int32_t b0, int32_t b1, float4& sc) {
+  constexpr int kChunks = D * 2 / 16;  // 16-byte bf16 chunks per row = lanes per K|V
+  const int lane = threadIdx.x & 31;
+  Loader ld;
+  ld.c = c;
+  ld.slot = p.slot_mapping[c.b];
+  ld.row = make_uint4(0u, 0u, 0u, 0u);
+  if (lane < 2 * kChunks) {
+    const int kv = lane / kChunks, ch = lane % kChunks;
+    const int64_t src = (static_cast<int64_t>(c.b) * p.num_kv_heads + c.g) * (D * 2) + ch * 16;
+    ld.row = *reinterpret_cast<const uint4*>((kv ? p.v_new : p.k_new) + src);
+  }
+  if (ld.slot < 0) return;
+  const int32_t pos = ld.c.n - 1;
+  const bool second = p.block_size < kTile && (pos & (kTile - 1)) >= p.block_size;
+  const int32_t blk = second ? b1 : b0;
+  const int32_t off = pos & (p.block_size - 1);
+  if (blk < 0 || blk >= p.num_blocks ||
+      ld.slot != static_cast<int64_t>(blk) * p.block_size + off) {
+    if (lane == 0) flag_error(PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const bool active = lane < 2 * kChunks;
+  const int kv = lane / kChunks, ch = lane % kChunks;
+  float x[8];
+  float a = 0.f;
+  if (active) {
+    const uint32_t w4[4] = {ld.row.x, ld.row.y, ld.row.z, ld.row.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_bf16x2(w4[i]);
+      x[2 * i] = f.x;
+      x[2 * i + 1] = f.y;
+      a = fmaxf(a, fmaxf(fabsf(f.x), fabsf(f.y)));
+    }
+  }
+  // absmax over the K lanes and over the V lanes (groups of kChunks lanes)
+#pragma unroll
+  for (int o = 1; o < kChunks; o <<= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const int64_t sidx = static_cast<int64_t>(blk) * p.num_kv_heads + ld.c.g;
+  float* scale = const_cast<float*>(kv ? p.v_scale : p.k_scale) + sidx;
+  const float old = active ? *scale : 1.f;
+  const float st = __fdiv_rn(a, 448.f);
+  float nw = old;
+  uint8_t* rows = (kv ? p.v_cache : p.k_cache) +
+                  (static_cast<int64_t>(blk) * p.num_kv_heads + ld.c.g) * p.block_size * D + ch * 8;
+  if (off == 0) {
+    nw = a == 0.f ? 1.f : st;
+  } else if (st > old) {
+    nw = st;
+    if (active)
+      for (int32_t r = 0; r < off; ++r) {
+        uint2* q = reinterpret_cast<uint2*>(rows + static_cast<int64_t>(r) * D);
+        uint2 c = *q;
+        uint32_t cw[2] = {c.x, c.y};
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+          uint32_t out = 0;
+#pragma unroll
+          for (int bt = 0; bt < 4; ++bt) {
+            const __half_raw hr =
+                __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(cw[w] >> (8 * bt)),
+                                        __NV_E4M3);
+            const float y = __fmul_rn(__half2float(__half(hr)), old);
+            out |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(y, nw), __NV_SATFINITE,
+                                                               __NV_E4M3))
+                   << (8 * bt);
+          }
+          cw[w] = out;
+        }
+        *q = make_uint2(cw[0], cw[1]);
+      }
+  }
+  if (active) {
+    uint32_t cw[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      cw[i >> 2] |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(__fdiv_rn(x[i], nw),
+                                                                __NV_SATFINITE, __NV_E4M3))
+                    << (8 * (i & 3));
+    *reinterpret_cast<uint2*>(rows + static_cast<int64_t>(off) * D) = make_uint2(cw[0], cw[1]);
+    if (ch == 0) *scale = nw;
+    fence_proxy_async_global();
+  }
+  // this tile's scales for the consumer: K from lane 0, V from lane kChunks
+  const float nk = __shfl_sync(0xffffffffu, nw, 0);
+  const float nv = __shfl_sync(0xffffffffu, nw, kChunks);
+  if (second) {
+    sc.y = nk;
+    sc.w = nv;
+  } else {
+    sc.x = nk;
+    sc.z = nv;
+    if (p.block_size >= kTile || !(b1 >= 0 && b1 < p.num_blocks)) {
+      sc.y = nk;  // one block in the tile (or the second is absent)
+      sc.w = nv;
+    }
+  }
+  __syncwarp();
+}
+
 // Warp-collective: issue the loader's next tile (and, if it opens a
 // segment, the segment's query rows) into the next stage, then advance
 // the loader.  The caller has made sure the stage and query slot are free.
-template <int D, bool FP8>
+template <int D, bool FP8, bool kAppend = true>
 __device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm,
                                            const Bufs& sb, Loader& ld, int64_t hi) {
   const int lane = threadIdx.x & 31;
@@ -430,6 +543,8 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm
       sc.w = sc.z;
     }
     // written before the stage's arrive, read after its completion
+    if (kAppend && p.k_new != nullptr && ld.c.tile == ld.c.T - 1)
+      store_new_token_fp8<D>(p, ld.c, b0, b1, sc);
     if (lane == 0) sb.hdr->scales[stage] = sc;
   }
   if (!FP8 && p.k_new != nullptr && ld.c.tile == ld.c.T - 1) store_new_token<D>(p, ld, b0, b1);
@@ -470,13 +585,13 @@ __device__ __forceinline__ bool can_issue(const DecodeParams& p, const Loader& l
 // (`qread` = slots read).  The warp has synchronised after its last reads
 // of the bytes these copies overwrite; the proxy fence orders those reads
 // before the TMA writes.
-template <int D, bool FP8>
+template <int D, bool FP8, bool kAppend>
 __device__ __forceinline__ void top_up(const DecodeParams& p, const Maps& tm, const Bufs& sb,
                                        Loader& ld, int64_t hi, uint32_t used, uint32_t qread) {
   if (!can_issue(p, ld, hi, used, qread)) return;
   if ((threadIdx.x & 31) == 0) fence_proxy_async_smem();
   do {
-    issue_tile<D, FP8>(p, tm, sb, ld, hi);
+    issue_tile<D, FP8, kAppend>(p, tm, sb, ld, hi);
   } while (can_issue(p, ld, hi, used, qread));
   __syncwarp();
 }
@@ -911,7 +1026,7 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, SegState<D>&
 // CTAs (kFused) refill the ring themselves after each tile; two-warp CTAs
 // release stages and query slots to the copy warp.  Returns the tiles and
 // query slots consumed.
-template <int D, bool FP8, bool kFused>
+template <int D, bool FP8, bool kFused, bool kAppend = true>
 __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, const Bufs& sb,
                                          Loader& ld, Cursor c, int64_t W, int32_t P,
                                          int64_t lo, int64_t hi, int32_t cta, uint32_t& used,
@@ -925,7 +1040,7 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
   SegState<D> s;
   uint32_t qb[D / 16][2];
   float hm0, hm1;
-  if (kFused) top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
+  if (kFused) top_up<D, FP8, kAppend>(p, tm, sb, ld, hi, used, qread);
   while (u < hi && ok) {
     const int32_t seg_end = static_cast<int32_t>(
         min(static_cast<int64_t>(c.T), c.tile + (hi - u)));
@@ -938,7 +1053,7 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
     ++qread;
     __syncwarp();
     if (kFused) {
-      top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
+      top_up<D, FP8, kAppend>(p, tm, sb, ld, hi, used, qread);
     } else if (lane == 0) {
       mbar_arrive(smem_addr(&hdr->qempty[qs]));
     }
@@ -971,7 +1086,7 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
       ++used;
       __syncwarp();
       if (kFused) {
-        top_up<D, FP8>(p, tm, sb, ld, hi, used, qread);
+        top_up<D, FP8, kAppend>(p, tm, sb, ld, hi, used, qread);
       } else if (lane == 0) {
         mbar_arrive(smem_addr(&hdr->empty[stage]));
       }
@@ -1074,8 +1189,10 @@ __global__ void __launch_bounds__(64, 8)
   }
 }
 
-// One warp that issues its own copies between tiles.
-template <int D, bool FP8>
+// One warp that issues its own copies between tiles.  kAppend: compiled
+// with the fused FP8 append (a separate instantiation, so that plain
+// decode keeps its registers).
+template <int D, bool FP8, bool kAppend = false>
 __global__ void __launch_bounds__(32, 16)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
@@ -1103,7 +1220,8 @@ __global__ void __launch_bounds__(32, 16)
   Loader ld;
   loader_init(p, lo, hi, ld);
   uint32_t used, qread;
-  run_math<D, FP8, true>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used, qread);
+  run_math<D, FP8, true, kAppend || !FP8>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used,
+                                           qread);
   // No copy may still target shared memory when the CTA exits.  On the
   // normal path every issued copy has been waited for already.
   if (lane == 0) {

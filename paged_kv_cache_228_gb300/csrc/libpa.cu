@@ -123,9 +123,9 @@ constexpr size_t kSmemReservedPerCta = 1024;
 using DecodeFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, DecodeParams);
 
 template <int D, bool FP8>
-DecodeFn decode_fn() {
-  return DecodeShape<D, FP8>::kTwoWarps ? paged_decode_ws_kernel<D, FP8>
-                                        : paged_decode_kernel<D, FP8>;
+DecodeFn decode_fn(bool append = false) {
+  if (DecodeShape<D, FP8>::kTwoWarps) return paged_decode_ws_kernel<D, FP8>;
+  return append ? paged_decode_kernel<D, FP8, true> : paged_decode_kernel<D, FP8, false>;
 }
 
 struct DecodePlan {
@@ -232,7 +232,20 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
   }
   // Both grids are programmatic dependents of the work before them in the
   // stream, which hides the launch gaps.
-  if (launch_pdl(decode_fn<D, FP8>(), dim3(static_cast<unsigned>(P)),
+  const bool append = prm.k_new != nullptr;
+  if (append && !DecodeShape<D, FP8>::kTwoWarps) {
+    // the append instantiation shares the plan's shared-memory size
+    static bool attr_set[kMaxDevices] = {false};
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!attr_set[dev]) {
+      if (cudaFuncSetAttribute(decode_fn<D, FP8>(true),
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(decode_smem_bytes<D, FP8>(stages))) != cudaSuccess)
+        return PA_ERR_CUDA;
+      attr_set[dev] = true;
+    }
+  }
+  if (launch_pdl(decode_fn<D, FP8>(append), dim3(static_cast<unsigned>(P)),
                  dim3(DecodeShape<D, FP8>::kThreads), decode_smem_bytes<D, FP8>(stages), stream,
                  tq, tk, tv, prm) != cudaSuccess)
     return PA_ERR_CUDA;
@@ -620,7 +633,10 @@ pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   if (group > kMaxG) return PA_ERR_UNSUPPORTED;
   if (!pow2_in(block_size, 8, 256)) return PA_ERR_UNSUPPORTED;
-  if (app != nullptr && kv_dtype != PA_KV_BF16) return PA_ERR_UNSUPPORTED;
+  // an FP8 append must find the whole block of the new token in the
+  // sequence's last tile
+  if (app != nullptr && kv_dtype == PA_KV_FP8_E4M3 && block_size > kTile)
+    return PA_ERR_UNSUPPORTED;
   if (num_seqs == 0) return PA_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !seq_lens || !out) return PA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
@@ -693,6 +709,23 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                       head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
                       num_splits, stream, nullptr);
+}
+
+extern "C" pa_status pa_decode_append_fp8(const void* q, const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, void* k_cache,
+                                          void* v_cache, float* k_scale, float* v_scale,
+                                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                          const int32_t* seq_lens, int32_t num_seqs,
+                                          int32_t num_q_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t block_size,
+                                          int32_t num_blocks, float scale, void* out,
+                                          void* workspace, size_t workspace_bytes,
+                                          int32_t num_splits, void* stream) {
+  const AppendArgs app{k_new, v_new, slot_mapping};
+  return decode_entry(q, k_cache, v_cache, k_scale, v_scale, PA_KV_FP8_E4M3, block_tables,
+                      max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                      head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
+                      num_splits, stream, &app);
 }
 
 extern "C" pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,

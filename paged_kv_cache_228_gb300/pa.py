@@ -61,6 +61,10 @@ SIGNATURES = {
     "pa_decode_cascade": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int,
                                    _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int, _c_ptr]),
+    "pa_decode_append_fp8": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                      _c_ptr, _c_ptr, _c_int, _c_ptr, _c_int, _c_int, _c_int,
+                                      _c_int, _c_int, _c_int, ctypes.c_float, _c_ptr, _c_ptr,
+                                      _c_size, _c_int, _c_ptr]),
     "pa_decode_noalloc": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr,
                                    _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, ctypes.c_float, _c_ptr, _c_int, _c_ptr]),
@@ -277,6 +281,33 @@ def pa_decode_append(q, k_new, v_new, slot_mapping, k_cache, v_cache, block_tabl
         _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, d, bs, nb,
         float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
+
+
+def pa_decode_append_fp8(q, k_new, v_new, slot_mapping, k_cache, v_cache, k_scale, v_scale,
+                         block_tables, seq_lens, scale, out, workspace=None, num_splits=0,
+                         stream=None):
+    """The FP8 decode step in one launch: pa_cache_write_fp8 of row b of
+    k_new / v_new at slot_mapping[b], then pa_decode, bit for bit (block
+    size 8 or 16)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(k_scale, torch.float32, "k_scale", 2)
+    _need(v_scale, torch.float32, "v_scale", 2)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    if _kv_dtype(k_cache) != PA_KV_FP8_E4M3:
+        raise TypeError("pa_decode_append_fp8: the cache must hold E4M3 bytes")
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_append_fp8", lib().pa_decode_append_fp8(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k_cache), _ptr(v_cache),
+        _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), B, hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace),
+        ws_bytes, num_splits, _stream(stream)))
 
 
 def pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,

@@ -172,3 +172,65 @@ def test_fp8_append_then_decode_matches_oracle(name):
     ref = OPA.decode(_to_np64(case.q), kq2, vq2, tab, np.array(w.seq_lens), w.scale,
                      k_scale=ks2, v_scale=vs2, seqs=seqs)
     assert_close(out, ref, 5e-2, f"{name} fp8 append+decode")
+
+
+@pytest.mark.parametrize("name,splits", [("llama3.1-8b", 0), ("llama3.1-8b", 7),
+                                         ("shared_prefix_bs8", 0), ("tiny", 0)])
+def test_fp8_fused_equals_write_then_decode(name, splits):
+    # pa_decode_append_fp8 against pa_cache_write_fp8 + pa_decode on copies
+    # of one FP8 cache: codes, scales and output bit for bit.  Half the new
+    # tokens are scaled up so that their blocks' scales grow.
+    import numpy as np
+    from oracle import quantize as OQ
+    case = build_case(W.WORKLOADS[name]())
+    w = case.w
+    ids, kk, vv = snapshot_blocks(case, range(w.num_seqs))
+    valid = {}
+    local = {bid: i for i, bid in enumerate(ids)}
+    for b in range(w.num_seqs):
+        n0 = w.seq_lens[b] - 1
+        for j, x in enumerate(case.tables[b]):
+            valid[local[x]] = max(valid.get(local[x], 0), max(0, min(w.block_size, n0 - j * w.block_size)))
+    blocks = sorted(valid)
+    kq, ks = OQ.quantize_blocks(kk, blocks, [valid[x] for x in blocks])
+    vq, vs = OQ.quantize_blocks(vv, blocks, [valid[x] for x in blocks])
+    shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    idx = torch.tensor(ids, dtype=torch.int64, device="cuda")
+
+    def pool():
+        k = torch.zeros(shape, dtype=torch.uint8, device="cuda")
+        v = torch.zeros_like(k)
+        s1 = torch.ones((w.pool_blocks, w.num_kv_heads), device="cuda")
+        s2 = torch.ones_like(s1)
+        k[idx], v[idx] = torch.from_numpy(kq).cuda(), torch.from_numpy(vq).cuda()
+        s1[idx], s2[idx] = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+        return k, v, s1, s2
+
+    grow = torch.ones((w.num_seqs, 1, 1), device="cuda")
+    grow[::2] = 25.0
+    kn = (case.k_new.float() * grow).to(torch.bfloat16)
+    vn = (case.v_new.float() * grow).to(torch.bfloat16)
+    k1, v1, ks1, vs1 = pool()
+    k2, v2, ks2, vs2 = pool()
+    o1, o2 = _out(w), _out(w)
+    pa.pa_cache_write_fp8(kn, vn, case.slots_t, k1, v1, ks1, vs1)
+    pa.pa_decode(case.q, k1, v1, case.table_t, case.lens_t, w.scale, o1, _workspace(w, splits),
+                 k_scale=ks1, v_scale=vs1, num_splits=splits)
+    pa.pa_decode_append_fp8(case.q, kn, vn, case.slots_t, k2, v2, ks2, vs2, case.table_t,
+                            case.lens_t, w.scale, o2, _workspace(w, splits), num_splits=splits)
+    torch.cuda.synchronize()
+    assert pa.pa_get_device_error() == 0
+    assert torch.equal(k1, k2) and torch.equal(v1, v2), name
+    assert torch.equal(ks1, ks2) and torch.equal(vs1, vs2), name
+    assert torch.equal(_bits(o1), _bits(o2)), name
+
+
+def test_fp8_fused_rejects_large_blocks():
+    case = build_case(W.shared_prefix(32, num_seqs=4, prefix=64))
+    w = case.w
+    k = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device="cuda")
+    s = torch.ones((w.pool_blocks, w.num_kv_heads), device="cuda")
+    with pytest.raises(RuntimeError):
+        pa.pa_decode_append_fp8(case.q, case.k_new, case.v_new, case.slots_t, k, k.clone(), s,
+                                s.clone(), case.table_t, case.lens_t, w.scale, _out(w),
+                                _workspace(w, 0))
