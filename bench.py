@@ -6,8 +6,9 @@
 One step = one decode layer-step of the whole hot path on one batch: the
 cache write of the step's new K/V (one appended token per sequence) and
 paged attention over every cached token, in one pa_decode_append launch,
-then its split-K merge launch.  (The FP8 figures run pa_decode on a cache
-quantised beforehand: FP8 append is not part of the step.)
+then its split-K merge launch.  The FP8 figures do the same on an E4M3
+cache (pa_decode_append_fp8: the new rows are quantised into their blocks
+inside the decode launch).
 The host block manager has already placed the appended tokens (its cost is
 reported separately).  Inputs are seeded synthetic tensors shaped like the
 workload, resident in HBM; consecutive steps rotate over several
@@ -298,8 +299,9 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
             pa.pa_decode_cascade(q, k, v, tab, lens, w.shared_prefix, w.scale, out, ws,
                                  stream=stream)
         elif fp8:
-            pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks, v_scale=vs,
-                         stream=stream)
+            # FP8 cache: the step's quantised append fused into the decode launch
+            pa.pa_decode_append_fp8(q, kn, vn, slots, k, v, ks, vs, tab, lens, w.scale, out,
+                                    ws, stream=stream)
         else:
             # this step's cache write and decode in one launch
             pa.pa_decode_append(q, kn, vn, slots, k, v, tab, lens, w.scale, out, ws,
@@ -350,8 +352,8 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
                 ks, vs = scales[i]
                 with torch.cuda.graph(g, stream=s2):
                     if fp8:
-                        pa.pa_decode(q, k, v, tab, lens, w.scale, out, ws, k_scale=ks,
-                                     v_scale=vs, stream=s2)
+                        pa.pa_decode_append_fp8(q, kn, vn, slots, k, v, ks, vs, tab, lens,
+                                                w.scale, out, ws, stream=s2)
                     else:
                         pa.pa_decode_append(q, kn, vn, slots, k, v, tab, lens, w.scale, out,
                                             ws, stream=s2)
@@ -427,8 +429,8 @@ def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps)
         for n in h:
             d[n].copy_(h[n], non_blocking=True)
         if fp8:
-            pa.pa_decode(d["q"], k, v, d["tab"], d["lens"], w.scale, out_d, ws, k_scale=ks,
-                         v_scale=vs, stream=stream)
+            pa.pa_decode_append_fp8(d["q"], d["kn"], d["vn"], d["slots"], k, v, ks, vs,
+                                    d["tab"], d["lens"], w.scale, out_d, ws, stream=stream)
         else:
             pa.pa_decode_append(d["q"], d["kn"], d["vn"], d["slots"], k, v, d["tab"],
                                 d["lens"], w.scale, out_d, ws, stream=stream)
