@@ -19,6 +19,12 @@ e4m3
     round-to-nearest-even, saturating fp32 -> E4M3 encoder).
 quantize
     Per-(block, KV head) absmax FP8 quantisation of cache blocks.
+e2m1
+    FP4 E2M1 element codec from the OCP MX definition (decode table and a
+    round-to-nearest-even, saturating encoder).
+nvfp4
+    Two-level scaled NVFP4 cache (E2M1 values, one E4M3 scale per 16 values,
+    one fp32 scale per tensor): quantiser, byte layout, decode attention.
 block_manager
     Dictionary/list model of the host block allocator (free list, refcounts,
     fork, copy-on-write append).

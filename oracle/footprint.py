@@ -38,3 +38,10 @@ def decode_step_kv_bytes(seq_lens, num_kv_heads: int, head_dim: int,
         if scale_bytes:
             total += 2 * (-(-n // block_size)) * num_kv_heads * scale_bytes
     return total
+
+
+def nvfp4_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int) -> int:
+    """NVFP4 cache bytes per token: half a byte per value plus one E4M3
+    block scale per 16 values, for K and V of every layer.  (The page's
+    "about 10.7 GB" for Llama 3.1 70B at 128K counts the 4-bit values alone.)"""
+    return 2 * num_layers * num_kv_heads * (head_dim // 2 + head_dim // 16)
