@@ -235,6 +235,12 @@ def offload_figure(w, device, reps=5):
     return out
 
 
+def kv_bytes_nvfp4(w):
+    """Algorithmic bytes of one NVFP4 layer-step: half a byte per value plus
+    one E4M3 block scale per 16 values, K and V, every cached token."""
+    return sum(w.seq_lens) * 2 * w.num_kv_heads * (w.head_dim // 2 + w.head_dim // 16)
+
+
 def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
     """Algorithmic KV bytes of one layer-step: per-token footprint
     2 * H_kv * d_h * s (one layer) for every cached token, plus, for FP8,
@@ -249,10 +255,12 @@ def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
 
 # ----------------------------------------------------------- native arm ---
 def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None,
-               profile_only=False, cascade=False):
+               profile_only=False, cascade=False, nvfp4=False):
     from paged_kv_cache_228_gb300 import pa
     from paged_kv_cache_228_gb300 import workloads as W
     per_pool = w.pool_blocks * w.num_kv_heads * w.block_size * w.head_dim * 2 * 2
+    if nvfp4:
+        per_pool = per_pool * 9 // 32  # 4.5 bits per value
     if n_pools is None:
         n_pools = max(1, min(8, math.ceil(4 * L2_BYTES / per_pool)))
     pools = make_pools(w, n_pools, device)
@@ -284,10 +292,35 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
             scales.append((ks, vs))
         del pools
         pools = qpools
+    if nvfp4:
+        # every slot of each pool quantised; tensor scales amax / (6 * 448)
+        qpools, scales = [], []
+        nb, bs, h, d = w.pool_blocks, w.block_size, w.num_kv_heads, w.head_dim
+        all_slots = torch.arange(nb * bs, dtype=torch.int64, device=device)
+        for k, v in pools:
+            gs = (float(k.abs().amax()) / 2688.0, float(v.abs().amax()) / 2688.0)
+            c = pa.nvfp4_empty_cache(nb, h, bs, d, device)
+            pa.pa_cache_write_nvfp4(k.permute(0, 2, 1, 3).reshape(nb * bs, h, d).contiguous(),
+                                    v.permute(0, 2, 1, 3).reshape(nb * bs, h, d).contiguous(),
+                                    all_slots, c, *gs)
+            qpools.append(c)
+            scales.append(gs)
+        del pools
+        pools = qpools
+        torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     pa.pa_get_device_error()
 
     def step(i, ev=None):
+        if nvfp4:
+            c, (kg, vg) = pools[i % n_pools], scales[i % n_pools]
+            pa.pa_cache_write_nvfp4(kn, vn, slots, c, kg, vg, stream=stream)
+            if ev is not None:
+                ev[0].record(stream)
+            pa.pa_decode_nvfp4(q, c, kg, vg, tab, lens, w.scale, out, ws, stream=stream)
+            if ev is not None:
+                ev[1].record(stream)
+            return
         k, v = pools[i % n_pools]
         ks, vs = scales[i % n_pools]
         if cascade:
@@ -348,6 +381,14 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
         with torch.cuda.stream(s2):
             for i in range(n_pools):
                 g = torch.cuda.CUDAGraph()
+                if nvfp4:
+                    c, (kg, vg) = pools[i], scales[i]
+                    with torch.cuda.graph(g, stream=s2):
+                        pa.pa_cache_write_nvfp4(kn, vn, slots, c, kg, vg, stream=s2)
+                        pa.pa_decode_nvfp4(q, c, kg, vg, tab, lens, w.scale, out, ws,
+                                           stream=s2)
+                    graphs.append(g)
+                    continue
                 k, v = pools[i]
                 ks, vs = scales[i]
                 with torch.cuda.graph(g, stream=s2):
@@ -392,7 +433,7 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
 
     # end to end through the public API with host buffers
     e2e = run_e2e(w, pools[0], scales[0], tab, lens, slots, q, kn, vn, ws, fp8, stream,
-                  max(20, min(steps, 2000)))
+                  max(20, min(steps, 2000)), nvfp4=nvfp4)
     return {
         "ms_per_step": graph_ms if graph_ms is not None else total_ms / steps,
         "eager_ms_per_step": total_ms / steps,
@@ -405,11 +446,12 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
         "pool_bytes": per_pool // (2 if fp8 else 1),
         "clocks": clocks if clocks is not None else (sampler.summary() if sampler else None),
         "e2e": e2e,
-        "launches_per_step": 2,  # decode (with the fused cache write) + merge
+        # decode (with the fused cache write) + merge; NVFP4: + the cache write
+        "launches_per_step": 3 if nvfp4 else 2,
     }
 
 
-def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps):
+def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps, nvfp4=False):
     """Per step: pinned host -> device copies of q, new K/V, slots, block
     tables and lengths; cache write + decode; device -> host copy of out."""
     from paged_kv_cache_228_gb300 import pa
@@ -420,18 +462,23 @@ def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps)
     out_h = torch.empty((w.num_seqs, w.num_q_heads, w.head_dim), dtype=torch.bfloat16,
                         pin_memory=True)
     out_d = torch.empty(out_h.shape, dtype=torch.bfloat16, device=q.device)
-    k, v = pool
-    ks, vs = scale
     h2d = sum(t.numel() * t.element_size() for t in h.values())
     d2h = out_h.numel() * out_h.element_size()
 
     def one():
         for n in h:
             d[n].copy_(h[n], non_blocking=True)
-        if fp8:
+        if nvfp4:
+            pa.pa_cache_write_nvfp4(d["kn"], d["vn"], d["slots"], pool, *scale, stream=stream)
+            pa.pa_decode_nvfp4(d["q"], pool, *scale, d["tab"], d["lens"], w.scale, out_d, ws,
+                               stream=stream)
+        elif fp8:
+            k, v = pool
+            ks, vs = scale
             pa.pa_decode_append_fp8(d["q"], d["kn"], d["vn"], d["slots"], k, v, ks, vs,
                                     d["tab"], d["lens"], w.scale, out_d, ws, stream=stream)
         else:
+            k, v = pool
             pa.pa_decode_append(d["q"], d["kn"], d["vn"], d["slots"], k, v, d["tab"],
                                 d["lens"], w.scale, out_d, ws, stream=stream)
         out_h.copy_(out_d, non_blocking=True)
@@ -548,6 +595,8 @@ def main():
     ap.add_argument("--num-seqs", type=int, default=None,
                     help="with --profile: a smaller batch of the 128K workload "
                          "(ncu captures that must stay a few GB)")
+    ap.add_argument("--nvfp4", action="store_true",
+                    help="with --profile: run the NVFP4 cache path of the workload")
     ap.add_argument("--cascade", action="store_true",
                     help="with --profile on a shared_prefix workload: pa_decode_cascade")
     ap.add_argument("--profile", action="store_true",
@@ -593,7 +642,7 @@ def main():
             ap.error("--cascade needs a shared_prefix workload")
         r = run_native(w, args.steps, args.warmup, device, fp8=args.fp8,
                        n_pools=1 if w.num_seqs * max(w.seq_lens) > 10 ** 6 else None,
-                       profile_only=True, cascade=args.cascade)
+                       profile_only=True, cascade=args.cascade, nvfp4=args.nvfp4)
         print(json.dumps({"workload": w.name, "ms_per_step": r["ms_per_step"],
                           "decode_ms_mean": r["decode_ms_mean"]}))
         return
@@ -620,6 +669,19 @@ def main():
                 "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
                 "us_per_step": r["ms_per_step"] * 1e3,
             }
+        r = run_native(w, max(50, args.steps // 20), max(3, args.warmup // 10), device,
+                       nvfp4=True)
+        nb = kv_bytes_nvfp4(w)
+        secondary[w.name + "_nvfp4"] = {
+            "kv_bytes_per_step": nb,
+            "decode_us": r["decode_ms_mean"] * 1e3,
+            "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
+            "hbm_frac_of_measured": nb / (r["decode_ms_mean"] / 1e3) / 1e9 / peak,
+            "us_per_step": r["ms_per_step"] * 1e3,
+            "e2e_us_per_step": r["e2e"]["ms_per_step"] * 1e3,
+            "note": "pa_cache_write_nvfp4 of the step's tokens + pa_decode_nvfp4 (+ merge); "
+                    "bytes: 4-bit values and E4M3 block scales",
+        }
         secondary["offload"] = offload_figure(w, device)
         secondary["offload"]["note"] = (
             "pa_swap_out / pa_swap_in of every block the 8B batch uses, between HBM and "
@@ -641,11 +703,12 @@ def main():
             "logical bytes as above")
     if rank == 0 and not args.no_secondary and args.workload != "llama3.1-70b-128k":
         wl = W.llama31_70b_128k()
-        for fp8 in (False, True):
+        for fmt in ("bf16", "fp8", "nvfp4"):
+            fp8, fp4 = fmt == "fp8", fmt == "nvfp4"
             r = run_native(wl, max(20, args.steps // 50), max(3, args.warmup // 10), device,
-                           fp8=fp8, n_pools=1)
-            nb = kv_bytes(wl, 1 if fp8 else 2, 4 if fp8 else 0)
-            secondary["llama3.1-70b-128k_" + ("fp8" if fp8 else "bf16")] = {
+                           fp8=fp8, n_pools=1, nvfp4=fp4)
+            nb = kv_bytes_nvfp4(wl) if fp4 else kv_bytes(wl, 1 if fp8 else 2, 4 if fp8 else 0)
+            secondary["llama3.1-70b-128k_" + fmt] = {
                 "kv_bytes_per_step": nb,
                 "us_per_step": r["ms_per_step"] * 1e3,
                 "GB_per_s": nb / (r["ms_per_step"] / 1e3) / 1e9,

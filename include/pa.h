@@ -15,7 +15,8 @@
  *     only as a sequence grows and freed when it finishes; requests with a
  *     shared prefix point at the same physical blocks.
  *   - same page, section "Quantization as a way to stretch paged memory
- *     further": FP8 KV caches with full fp32 accumulation.
+ *     further": FP8 KV caches with full fp32 accumulation, and NVFP4 on
+ *     Blackwell.
  *
  * Conventions (all entry points):
  *   - Every function returns a pa_status; nothing throws or aborts.
@@ -68,7 +69,8 @@ typedef enum pa_status {
 
 typedef enum pa_kv_dtype {
   PA_KV_BF16 = 0,
-  PA_KV_FP8_E4M3 = 1
+  PA_KV_FP8_E4M3 = 1,
+  PA_KV_NVFP4 = 2   /* pa_cache_write_nvfp4 / pa_decode_nvfp4 only */
 } pa_kv_dtype;
 
 /* Bits of the per-device error word (pa_get_device_error). */
@@ -214,7 +216,9 @@ pa_status pa_quantize_fp8(const void* k_src, const void* v_src,
 /* ----------------------------------------------------------------- decode
  * pa_decode_workspace_size -- bytes of device workspace pa_decode needs for
  * this shape with `num_splits` work partitions (0 = the automatic choice
- * for the current device).  Writes the size to *bytes (host). */
+ * for the current device, the largest over the cache formats: the same
+ * size serves pa_decode, pa_decode_append(_fp8), pa_decode_nvfp4).  Writes
+ * the size to *bytes (host). */
 pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
                                    int32_t num_kv_heads, int32_t head_dim,
                                    int32_t num_splits, size_t* bytes);
@@ -307,6 +311,63 @@ pa_status pa_decode_append_fp8(const void* q, const void* k_new, const void* v_n
                                int32_t block_size, int32_t num_blocks, float scale,
                                void* out, void* workspace, size_t workspace_bytes,
                                int32_t num_splits, void* stream);
+
+/* --------------------------------------------------------------- NVFP4
+ * NVFP4 caches.  "Paged Attention and KV Cache Fragmentation", section
+ * "Quantization as a way to stretch paged memory further", names NVFP4 as
+ * the Blackwell cache format that halves FP8's footprint again, without
+ * defining it.  This library takes NVIDIA's published NVFP4: FP4 E2M1
+ * values (0, 0.5, 1, 1.5, 2, 3, 4, 6 and negatives), one E4M3 scale per 16
+ * consecutive values of a head row, and one fp32 scale S per tensor (the K,
+ * resp. V, cache of a layer) that the caller calibrates, e.g. S = amax /
+ * (6 * 448).  A row x (bf16, widened to fp32) is stored as
+ *     s_g = e4m3(max|x_g| / (6 S))   for each 16-value group g
+ *     q_i = e2m1(x_i / (e4m3(s_g) * S))   (0 when s_g decodes to 0)
+ * (fp32 IEEE multiply and divide; both encoders round to nearest even and
+ * saturate, E4M3 to 448, E2M1 to 6) and reads back as
+ * e2m1(q_i) * e4m3(s_g) * S.  Layout per (block, KV head), bs = block_size,
+ * D = head_dim, all uint8:
+ *     k_cache [num_blocks][Hkv][bs][D/2]    byte j of token t holds values
+ *                                           2j (low nibble) and 2j+1
+ *     k_sf    [num_blocks][Hkv][bs][D/16]   E4M3 scale of group g of token t
+ *     v_cache [num_blocks][Hkv][bs/2][D]    byte d of pair-row p holds token
+ *                                           2p (low nibble) and 2p+1 of
+ *                                           dimension d
+ *     v_sf    [num_blocks][Hkv][D/16][bs]   E4M3 scale of group g of token t
+ * 4.5 bits per value.  Supported: head_dim in {64, 128}; block_size a power
+ * of two in [16, 256]; 1 <= num_q_heads / num_kv_heads <= 8.
+ *
+ * pa_cache_write_nvfp4 -- quantise and store this step's new K/V.  For each
+ * token t < num_tokens with s = slot_mapping[t] >= 0, every KV head h: the
+ * K row k_new[t][h] and the V row v_new[t][h] are quantised as above into
+ * block s / bs, token s % bs.  Slots must be distinct; slots >= num_blocks
+ * * block_size are skipped and flag PA_DEVERR_BAD_SLOT.
+ *   k_new, v_new         device bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping         device int64 [num_tokens]
+ *   k_cache..v_sf        device pools (layout above), updated in place
+ *   k_gscale, v_gscale   the tensor scales S (host floats, > 0, finite) */
+pa_status pa_cache_write_nvfp4(const void* k_new, const void* v_new,
+                               const int64_t* slot_mapping, int32_t num_tokens,
+                               void* k_cache, void* v_cache, void* k_sf, void* v_sf,
+                               float k_gscale, float v_gscale, int32_t num_blocks,
+                               int32_t num_kv_heads, int32_t block_size,
+                               int32_t head_dim, void* stream);
+
+/* pa_decode_nvfp4 -- pa_decode over an NVFP4 cache: the same attention,
+ * with K_b[t] and V_b[t] the dequantised rows e2m1 * e4m3 block scale * S.
+ * Accumulation in fp32; K and V reach the tensor cores as f16 values, which
+ * hold every e2m1 * e4m3 product exactly; q is rounded to f16 (|q| must
+ * stay below 65504).  The workspace is pa_decode_workspace_size()'s.
+ * Other arguments, results and device-error behaviour as pa_decode. */
+pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const void* v_cache,
+                          const void* k_sf, const void* v_sf, float k_gscale,
+                          float v_gscale, const int32_t* block_tables,
+                          int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                          int32_t num_seqs, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim,
+                          int32_t block_size, int32_t num_blocks, float scale,
+                          void* out, void* workspace, size_t workspace_bytes,
+                          int32_t num_splits, void* stream);
 
 /* pa_decode_cascade -- pa_decode for a batch whose sequences all start with
  * the same prefix_len tokens in the same physical blocks (forks of one

@@ -108,29 +108,25 @@ def cache_write(k_new, v_new, slots, cache, k_gs, v_gs):
     return k, k_sf, v, v_sf
 
 
-def k_codes(k, blk, h, off) -> np.ndarray:
-    """The D 4-bit codes of token ``off`` of (block, head) from the K layout."""
-    b = k[blk, h, off]
-    return np.stack([b & 0xF, b >> 4], axis=1).reshape(-1)
-
-
-def v_codes(v, blk, h, off) -> np.ndarray:
-    """The D 4-bit codes of token ``off`` of (block, head) from the V layout."""
-    b = v[blk, h, off // 2]
-    return (b >> 4) if off % 2 else (b & 0xF)
-
-
 def gather_rows(cache, k_gs, v_gs, table_row, n, h):
-    """Dequantised fp64 K and V rows [n, D] of one sequence's KV head h,
-    token t read from block table_row[t // bs] at offset t % bs."""
+    """Dequantised fp64 K and V rows [n, D] of one sequence's KV head h:
+    token t is read from block table_row[t // bs] at offset t % bs, its K
+    codes from both nibbles of its row, its V codes from the low (even t) or
+    high (odd t) nibbles of pair-row (t % bs) // 2, each value times its
+    group's E4M3 scale and the tensor scale."""
     k, k_sf, v, v_sf = cache
     bs, D = k.shape[2], v.shape[3]
-    K = np.zeros((n, D))
-    V = np.zeros((n, D))
-    for t in range(n):
-        blk, off = int(table_row[t // bs]), t % bs
-        K[t] = dequantize_row(k_codes(k, blk, h, off), k_sf[blk, h, off], k_gs)
-        V[t] = dequantize_row(v_codes(v, blk, h, off), v_sf[blk, h, :, off], v_gs)
+    t = np.arange(int(n))
+    blk = np.asarray(table_row, dtype=np.int64)[t // bs]
+    off = t % bs
+    kb = k[blk, h, off]                                      # [n, D/2]
+    kc = np.stack([kb & 0xF, kb >> 4], axis=-1).reshape(len(t), D)
+    ks = np.repeat(e4m3.decode(k_sf[blk, h, off]), GROUP, axis=-1)
+    vb = v[blk, h, off // 2]                                 # [n, D]
+    vc = np.where((off % 2 == 1)[:, None], vb >> 4, vb & 0xF)
+    vs = np.repeat(e4m3.decode(v_sf[blk, h, :, off]), GROUP, axis=-1)
+    K = e2m1.decode(kc) * ks * float(np.float32(k_gs))
+    V = e2m1.decode(vc) * vs * float(np.float32(v_gs))
     return K, V
 
 

@@ -1,6 +1,7 @@
 // libpa: C ABI entry points (declared in include/pa.h).  Host-side argument
 // validation, TMA descriptor encoding and kernel launches; the kernels live
-// in decode.cuh and cache_ops.cuh, the host block manager in
+// in decode.cuh, nvfp4.cuh, cascade.cuh and cache_ops.cuh, the host block
+// manager in
 // block_manager.cpp.
 #include <cuda.h>
 #include <cudaTypedefs.h>
@@ -14,6 +15,7 @@
 #include "cache_ops.cuh"
 #include "cascade.cuh"
 #include "decode.cuh"
+#include "nvfp4.cuh"
 #include "pa.h"
 
 namespace pa {
@@ -164,6 +166,29 @@ pa_status decode_plan(int dev, DecodePlan* out) {
     pl.ctas_per_sm = n;
   }
   *out = pl;
+  return PA_OK;
+}
+
+// NVFP4 decode: a fixed ring depth per head_dim, so the plan is the CTAs
+// per SM that registers and that ring allow (at most kMaxCtasPerSm).
+template <int D>
+pa_status fp4_plan(int dev, int* ctas_per_sm) {
+  static int cached[kMaxDevices] = {0};
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (cached[dev] == 0) {
+    const size_t smem = fp4_smem_bytes<D>();
+    if (cudaFuncSetAttribute(paged_decode_nvfp4_kernel<D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_nvfp4_kernel<D>, 32,
+                                                      smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (n < 1) return PA_ERR_UNSUPPORTED;
+    cached[dev] = n < kMaxCtasPerSm ? n : kMaxCtasPerSm;
+  }
+  *ctas_per_sm = cached[dev];
   return PA_OK;
 }
 
@@ -507,6 +532,8 @@ pa_status auto_ctas(int32_t head_dim, pa_kv_dtype dt, int32_t* out) {
     st = decode_plan<128, true>(dev, &pl);
   else if (dt == PA_KV_FP8_E4M3 && head_dim == 64)
     st = decode_plan<64, true>(dev, &pl);
+  else if (dt == PA_KV_NVFP4)
+    st = head_dim == 128 ? fp4_plan<128>(dev, &pl.ctas_per_sm) : fp4_plan<64>(dev, &pl.ctas_per_sm);
   else
     return PA_ERR_UNSUPPORTED;
   if (st != PA_OK) return st;
@@ -526,14 +553,17 @@ extern "C" pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_he
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
   int32_t P = num_splits;
   if (P == 0) {
-    // The automatic partition count is the same for both cache dtypes'
-    // worst case; take the larger.
-    int32_t a = 0, b = 0;
+    // One size for every cache format: the largest automatic partition
+    // count.
+    int32_t a = 0, b = 0, c = 0;
     pa_status st = auto_ctas(head_dim, PA_KV_BF16, &a);
     if (st != PA_OK) return st;
     st = auto_ctas(head_dim, PA_KV_FP8_E4M3, &b);
     if (st != PA_OK) return st;
+    st = auto_ctas(head_dim, PA_KV_NVFP4, &c);
+    if (st != PA_OK) return st;
     P = a > b ? a : b;
+    P = P > c ? P : c;
   }
   *bytes = P > 1 ? workspace_bytes_for(P, static_cast<int64_t>(num_seqs) * num_kv_heads,
                                        head_dim)
@@ -886,4 +916,146 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_cache, const
                    max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                    head_dim, block_size, num_blocks, scale, out, scratch,
                    PA_NOALLOC_SCRATCH_BYTES, num_splits, stream);
+}
+
+// ------------------------------------------------------------------ NVFP4
+namespace pa {
+namespace {
+
+bool fp4_shape_ok(int32_t head_dim, int32_t block_size) {
+  return (head_dim == 64 || head_dim == 128) && pow2_in(block_size, 16, 256);
+}
+
+bool finite_pos(float x) { return x > 0.f && x <= 3.402823466e38f; }
+
+template <int D>
+pa_status launch_fp4_decode(const DecodeParams& prm_in, const Fp4Args& f, void* workspace,
+                            size_t workspace_bytes, int32_t num_splits, cudaStream_t stream) {
+  int sms = 0, dev = 0;
+  pa_status st = device_sms(&sms, &dev);
+  if (st != PA_OK) return st;
+  int per = 0;
+  st = fp4_plan<D>(dev, &per);
+  if (st != PA_OK) return st;
+  const int32_t P = num_splits > 0 ? num_splits : sms * per;
+  const int64_t segs = static_cast<int64_t>(prm_in.num_seqs) * prm_in.num_kv_heads;
+  const size_t need = P > 1 ? workspace_bytes_for(P, segs, D) : 0;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  DecodeParams prm = prm_in;
+  prm.num_ctas = P;
+  prm.ws_o = nullptr;
+  prm.ws_ml = nullptr;
+  prm.ws_job = nullptr;
+  if (need > 0) {
+    const int64_t pieces = P + segs;
+    char* w = static_cast<char*>(workspace);
+    prm.ws_o = reinterpret_cast<float*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * D * sizeof(float);
+    prm.ws_ml = reinterpret_cast<float2*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * sizeof(float2);
+    prm.ws_job = reinterpret_cast<int2*>(w);
+  }
+  if (launch_pdl(paged_decode_nvfp4_kernel<D>, dim3(static_cast<unsigned>(P)), dim3(32),
+                 fp4_smem_bytes<D>(), stream, prm, f) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
+                 dim3(kMaxG * D / 4), 0, stream, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_cache_write_nvfp4(const void* k_new, const void* v_new,
+                                          const int64_t* slot_mapping, int32_t num_tokens,
+                                          void* k_cache, void* v_cache, void* k_sf, void* v_sf,
+                                          float k_gscale, float v_gscale, int32_t num_blocks,
+                                          int32_t num_kv_heads, int32_t block_size,
+                                          int32_t head_dim, void* stream) {
+  if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || !finite_pos(k_gscale) ||
+      !finite_pos(v_gscale))
+    return PA_ERR_INVALID_ARG;
+  if (!fp4_shape_ok(head_dim, block_size)) return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;
+  if (!k_new || !v_new || !slot_mapping || !k_cache || !v_cache || !k_sf || !v_sf ||
+      !aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(k_sf) || !aligned16(v_sf) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PA_ERR_INVALID_ARG;
+  int sms = 0;
+  pa_status st = device_sms(&sms, nullptr);
+  if (st != PA_OK) return st;
+  const int64_t rows = 2LL * num_tokens * num_kv_heads;
+  const int64_t want = (rows + 7) / 8;
+  const unsigned grid = static_cast<unsigned>(want < sms * 16LL ? want : sms * 16LL);
+  const int64_t num_slots = static_cast<int64_t>(num_blocks) * block_size;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+  auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+  auto* ks = static_cast<uint8_t*>(k_sf);
+  auto* vs = static_cast<uint8_t*>(v_sf);
+  cudaError_t e;
+  if (head_dim == 128)
+    e = launch_pdl(cache_write_nvfp4_kernel<128>, dim3(grid), dim3(256), 0, s, kn, vn,
+                   slot_mapping, num_tokens, num_kv_heads, block_size, num_slots, kc, ks, vc, vs,
+                   k_gscale, v_gscale);
+  else
+    e = launch_pdl(cache_write_nvfp4_kernel<64>, dim3(grid), dim3(256), 0, s, kn, vn,
+                   slot_mapping, num_tokens, num_kv_heads, block_size, num_slots, kc, ks, vc, vs,
+                   k_gscale, v_gscale);
+  return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const void* v_cache,
+                                     const void* k_sf, const void* v_sf, float k_gscale,
+                                     float v_gscale, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                     float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, int32_t num_splits, void* stream) {
+  if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
+      max_blocks_per_seq < 0 || num_splits < 0 || !(scale == scale) ||
+      num_q_heads % num_kv_heads != 0 || !finite_pos(k_gscale) || !finite_pos(v_gscale))
+    return PA_ERR_INVALID_ARG;
+  const int32_t group = num_q_heads / num_kv_heads;
+  if (!fp4_shape_ok(head_dim, block_size) || group > kMaxG) return PA_ERR_UNSUPPORTED;
+  if (num_seqs == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !k_sf || !v_sf || !block_tables || !seq_lens || !out ||
+      !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_sf) ||
+      !aligned16(v_sf) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(num_seqs) * num_q_heads > INT_MAX - 64) return PA_ERR_UNSUPPORTED;
+  if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX - 64)
+    return PA_ERR_UNSUPPORTED;
+  DecodeParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.block_tables = block_tables;
+  p.seq_lens = seq_lens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.group = group;
+  p.block_size = block_size;
+  p.log2_bs = ilog2(block_size);
+  p.max_blocks = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  Fp4Args f;
+  f.q = static_cast<const __nv_bfloat16*>(q);
+  f.k = static_cast<const uint8_t*>(k_cache);
+  f.v = static_cast<const uint8_t*>(v_cache);
+  f.k_sf = static_cast<const uint8_t*>(k_sf);
+  f.v_sf = static_cast<const uint8_t*>(v_sf);
+  f.k_gs = k_gscale;
+  f.v_gs = v_gscale;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (head_dim == 128)
+    return launch_fp4_decode<128>(p, f, workspace, workspace_bytes, num_splits, s);
+  return launch_fp4_decode<64>(p, f, workspace, workspace_bytes, num_splits, s);
 }

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_PKG, "libpa.so")
 
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_OUT_OF_BLOCKS, PA_ERR_BAD_BLOCK_ID = 0, 1, 2, 3
 PA_ERR_CUDA, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE = 4, 5, 6
-PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1
+PA_KV_BF16, PA_KV_FP8_E4M3, PA_KV_NVFP4 = 0, 1, 2
 
 DEVERR_BAD_BLOCK_ID, DEVERR_BAD_SEQ_LEN, DEVERR_BAD_SLOT = 0x1, 0x2, 0x4
 DEVERR_BAD_PAIR, DEVERR_TIMEOUT, DEVERR_LAUNCH = 0x8, 0x10, 0x20
@@ -68,6 +68,13 @@ SIGNATURES = {
     "pa_decode_noalloc": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr,
                                    _c_int, _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int,
                                    _c_int, ctypes.c_float, _c_ptr, _c_int, _c_ptr]),
+    "pa_cache_write_nvfp4": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_ptr,
+                                      _c_ptr, ctypes.c_float, ctypes.c_float, _c_int, _c_int,
+                                      _c_int, _c_int, _c_ptr]),
+    "pa_decode_nvfp4": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, ctypes.c_float,
+                                 ctypes.c_float, _c_ptr, _c_int, _c_ptr, _c_int, _c_int, _c_int,
+                                 _c_int, _c_int, _c_int, ctypes.c_float, _c_ptr, _c_ptr,
+                                 _c_size, _c_int, _c_ptr]),
     "pa_allocator_create": (_c_int, [_c_int, ctypes.POINTER(_c_ptr)]),
     "pa_allocator_destroy": (None, [_c_ptr]),
     "pa_block_alloc": (_c_int, [_c_ptr, _c_int, _c_ptr]),
@@ -308,6 +315,60 @@ def pa_decode_append_fp8(q, k_new, v_new, slot_mapping, k_cache, v_cache, k_scal
         _ptr(k_scale), _ptr(v_scale), _ptr(block_tables), block_tables.shape[1],
         _ptr(seq_lens), B, hq, hkv, d, bs, nb, float(scale), _ptr(out), _ptr(workspace),
         ws_bytes, num_splits, _stream(stream)))
+
+
+# ----------------------------------------------------------------- NVFP4 ---
+def nvfp4_empty_cache(num_blocks, num_kv_heads, block_size, head_dim, device="cuda"):
+    """Zeroed NVFP4 pools (k, k_sf, v, v_sf), uint8, in the layout of
+    include/pa.h: k [nb, Hkv, bs, d/2], k_sf [nb, Hkv, bs, d/16],
+    v [nb, Hkv, bs/2, d], v_sf [nb, Hkv, d/16, bs]."""
+    nb, h, bs, d = num_blocks, num_kv_heads, block_size, head_dim
+    z = lambda *shape: torch.zeros(shape, dtype=torch.uint8, device=device)
+    return z(nb, h, bs, d // 2), z(nb, h, bs, d // 16), z(nb, h, bs // 2, d), z(nb, h, d // 16, bs)
+
+
+def _nvfp4_dims(cache):
+    k, k_sf, v, v_sf = cache
+    for t, n in zip(cache, ("k", "k_sf", "v", "v_sf")):
+        _need(t, torch.uint8, n, 4)
+    nb, hkv, bs, d2 = k.shape
+    d = 2 * d2
+    if tuple(k_sf.shape) != (nb, hkv, bs, d // 16) or tuple(v.shape) != (nb, hkv, bs // 2, d) \
+            or tuple(v_sf.shape) != (nb, hkv, d // 16, bs):
+        raise ValueError("NVFP4 cache: inconsistent pool shapes")
+    return nb, hkv, bs, d
+
+
+def pa_cache_write_nvfp4(k_new, v_new, slot_mapping, cache, k_gscale, v_gscale, stream=None):
+    """Quantise k_new/v_new [T, Hkv, d] (bf16) into the NVFP4 pools
+    cache = (k, k_sf, v, v_sf) at slot_mapping[T] with tensor scales
+    k_gscale / v_gscale."""
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    nb, hkv, bs, d = _nvfp4_dims(cache)
+    k, k_sf, v, v_sf = cache
+    _check("pa_cache_write_nvfp4", lib().pa_cache_write_nvfp4(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), k_new.shape[0], _ptr(k), _ptr(v),
+        _ptr(k_sf), _ptr(v_sf), float(k_gscale), float(v_gscale), nb, hkv, bs, d,
+        _stream(stream)))
+
+
+def pa_decode_nvfp4(q, cache, k_gscale, v_gscale, block_tables, seq_lens, scale, out,
+                    workspace=None, num_splits=0, stream=None):
+    """Paged decode attention over NVFP4 pools cache = (k, k_sf, v, v_sf)."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    nb, hkv, bs, d = _nvfp4_dims(cache)
+    k, k_sf, v, v_sf = cache
+    B, hq, dq = q.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_nvfp4", lib().pa_decode_nvfp4(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(k_sf), _ptr(v_sf), float(k_gscale), float(v_gscale),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dq, bs, nb,
+        float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
 
 
 def pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,

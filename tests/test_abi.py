@@ -85,6 +85,29 @@ def test_host_validation_without_gpu(palib):
                                None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
     assert L.pa_decode_cascade(None, None, None, None, 8, None, 1, 4, 2, 64, 32, 8, 16, 1.0,
                                None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
+    # NVFP4: tensor scales must be positive and finite; block_size >= 16
+    nan, inf = float("nan"), float("inf")
+    for gs in (0.0, -1.0, nan, inf):
+        assert L.pa_cache_write_nvfp4(None, None, None, 1, None, None, None, None, gs, 1.0, 8,
+                                      2, 16, 64, None) == palib.PA_ERR_INVALID_ARG
+        assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, gs, None, 1, None, 1, 4, 2,
+                                 64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_cache_write_nvfp4(None, None, None, 1, None, None, None, None, 1.0, 1.0, 8, 2,
+                                  8, 64, None) == palib.PA_ERR_UNSUPPORTED
+    assert L.pa_cache_write_nvfp4(None, None, None, 1, None, None, None, None, 1.0, 1.0, 8, 2,
+                                  16, 96, None) == palib.PA_ERR_UNSUPPORTED
+    assert L.pa_cache_write_nvfp4(None, None, None, 0, None, None, None, None, 1.0, 1.0, 8, 2,
+                                  16, 64, None) == palib.PA_OK
+    assert L.pa_cache_write_nvfp4(None, None, None, 3, None, None, None, None, 1.0, 1.0, 8, 2,
+                                  16, 64, None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, 1.0, None, 1, None, 1, 32, 2,
+                             64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_UNSUPPORTED
+    assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, 1.0, None, 1, None, 1, 4, 2,
+                             64, 8, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_UNSUPPORTED
+    assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, 1.0, None, 1, None, 0, 4, 2,
+                             64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_OK
+    assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, 1.0, None, 1, None, 1, 4, 2,
+                             64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
 
 
 def _compare_models(pa, seed, steps=2000, N=48, bs=4):
