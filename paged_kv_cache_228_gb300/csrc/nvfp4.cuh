@@ -94,16 +94,18 @@ __device__ __forceinline__ void fp4_cp_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Two E2M1 values (low byte of x: low nibble, high nibble) -> f16x2 (low
-// half, high half).  Exact: every E2M1 value is an f16 value.
-__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t x) {
-  uint32_t d;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.u8.u32 t, %1;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d)
-      : "r"(x & 0xffu));
-  return d;
+// Four bytes of E2M1 pairs -> four f16x2 (byte k: low nibble -> low half,
+// high nibble -> high half).  Exact: every E2M1 value is an f16 value.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t& d0, uint32_t& d1,
+                                                uint32_t& d2, uint32_t& d3) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+      : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+      : "r"(w));
 }
 
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
@@ -233,34 +235,43 @@ __device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t 
   lds_words<TB>(st + L::kK + (gq + 8) * (D / 2) + TB * tq, k1);
   uint32_t s0[2], s1[2];
   if (D == 128) {  // groups 2tq, 2tq + 1
-    const uint32_t w0 = lds_u16(st + L::kKsf + gq * 8 + 2 * tq);
-    const uint32_t w1 = lds_u16(st + L::kKsf + (gq + 8) * 8 + 2 * tq);
-    s0[0] = sf_splat(w0 & 0xffu);
-    s0[1] = sf_splat(w0 >> 8);
-    s1[0] = sf_splat(w1 & 0xffu);
-    s1[1] = sf_splat(w1 >> 8);
+    const uint32_t p0 = e4m3x2_to_f16x2(static_cast<uint16_t>(lds_u16(st + L::kKsf + gq * 8 + 2 * tq)));
+    const uint32_t p1 =
+        e4m3x2_to_f16x2(static_cast<uint16_t>(lds_u16(st + L::kKsf + (gq + 8) * 8 + 2 * tq)));
+    s0[0] = __byte_perm(p0, 0, 0x1010);
+    s0[1] = __byte_perm(p0, 0, 0x3232);
+    s1[0] = __byte_perm(p1, 0, 0x1010);
+    s1[1] = __byte_perm(p1, 0, 0x3232);
   } else {  // group tq
     s0[0] = s0[1] = sf_splat(lds_u8(st + L::kKsf + gq * 4 + tq));
     s1[0] = s1[1] = sf_splat(lds_u8(st + L::kKsf + (gq + 8) * 4 + tq));
   }
   float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < TB / 2; ++j) {
-    const int w = j >> 1, sh = (j & 1) * 16;  // bytes 2j, 2j + 1
-    const int hsel = (D == 128) ? (j >> 2) : 0;
-    const uint32_t a0 = hmul2_u32(e2m1x2_to_f16x2(k0[w] >> sh), s0[hsel]);
-    const uint32_t a1 = hmul2_u32(e2m1x2_to_f16x2(k1[w] >> sh), s1[hsel]);
-    const uint32_t a2 = hmul2_u32(e2m1x2_to_f16x2(k0[w] >> (sh + 8)), s0[hsel]);
-    const uint32_t a3 = hmul2_u32(e2m1x2_to_f16x2(k1[w] >> (sh + 8)), s1[hsel]);
-    if (j & 1)
-      mma_f16(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
-    else
-      mma_f16(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+  for (int w = 0; w < TB / 4; ++w) {  // word w: bytes 4w..4w+3, k-steps 2w, 2w + 1
+    uint32_t r0[4], r1[4];
+    e2m1x8_to_f16x2(k0[w], r0[0], r0[1], r0[2], r0[3]);
+    e2m1x8_to_f16x2(k1[w], r1[0], r1[1], r1[2], r1[3]);
+    const int hsel = (D == 128) ? (w >> 1) : 0;  // group 2tq + (j >= 4)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int j = 2 * w + h;
+      const uint32_t a0 = hmul2_u32(r0[2 * h], s0[hsel]);
+      const uint32_t a1 = hmul2_u32(r1[2 * h], s1[hsel]);
+      const uint32_t a2 = hmul2_u32(r0[2 * h + 1], s0[hsel]);
+      const uint32_t a3 = hmul2_u32(r1[2 * h + 1], s1[hsel]);
+      if (h)
+        mma_f16(sb, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+      else
+        mma_f16(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
+    }
   }
   float x0 = (sa[0] + sb[0]) * kmul, x1 = (sa[1] + sb[1]) * kmul;
   float x2 = (sa[2] + sb[2]) * kmul, x3 = (sa[3] + sb[3]) * kmul;
-  if (gq >= valid) x0 = x1 = -INFINITY;
-  if (gq + 8 >= valid) x2 = x3 = -INFINITY;
+  if (valid < kTile) {  // the segment's last tile (warp-uniform)
+    if (gq >= valid) x0 = x1 = -INFINITY;
+    if (gq + 8 >= valid) x2 = x3 = -INFINITY;
+  }
   float alpha0, alpha1;
   uint32_t pb0, pb1;
   softmax_tile<true>(x0, x1, x2, x3, s.m, s.l, 1.f, 1.f, alpha0, alpha1, pb0, pb1);
@@ -274,21 +285,25 @@ __device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t 
   const int gv = D == 128 ? gq : (gq >> 1);
   uint32_t wa = lds_u16(st + L::kVsf + gv * 16 + 2 * tq);
   uint32_t wb = lds_u16(st + L::kVsf + gv * 16 + 2 * tq + 8);
-  if (2 * tq >= valid) wa &= 0xff00u;
-  if (2 * tq + 1 >= valid) wa &= 0x00ffu;
-  if (2 * tq + 8 >= valid) wb &= 0xff00u;
-  if (2 * tq + 9 >= valid) wb &= 0x00ffu;
+  if (valid < kTile) {
+    if (2 * tq >= valid) wa &= 0xff00u;
+    if (2 * tq + 1 >= valid) wa &= 0x00ffu;
+    if (2 * tq + 8 >= valid) wb &= 0xff00u;
+    if (2 * tq + 9 >= valid) wb &= 0x00ffu;
+  }
   const uint32_t sA = e4m3x2_to_f16x2(static_cast<uint16_t>(wa));
   const uint32_t sB = e4m3x2_to_f16x2(static_cast<uint16_t>(wb));
 #pragma unroll
-  for (int i = 0; i < TB / 2; ++i) {  // m-tile i: d = TB gq + i (+ TB/2)
-    const int lo_w = i >> 2, lo_s = (i & 3) * 8;
-    const int hi_w = (i + TB / 2) >> 2, hi_s = ((i + TB / 2) & 3) * 8;
-    const uint32_t a0 = hmul2_u32(e2m1x2_to_f16x2(v0[lo_w] >> lo_s), sA);
-    const uint32_t a1 = hmul2_u32(e2m1x2_to_f16x2(v0[hi_w] >> hi_s), sA);
-    const uint32_t a2 = hmul2_u32(e2m1x2_to_f16x2(v1[lo_w] >> lo_s), sB);
-    const uint32_t a3 = hmul2_u32(e2m1x2_to_f16x2(v1[hi_w] >> hi_s), sB);
-    mma_f16(s.acc[i], a0, a1, a2, a3, pb0, pb1);
+  for (int w = 0; w < TB / 8; ++w) {  // m-tiles 4w..4w+3: bytes 4w+b and TB/2 + 4w + b
+    uint32_t lo0[4], hi0[4], lo1[4], hi1[4];
+    e2m1x8_to_f16x2(v0[w], lo0[0], lo0[1], lo0[2], lo0[3]);
+    e2m1x8_to_f16x2(v0[w + TB / 8], hi0[0], hi0[1], hi0[2], hi0[3]);
+    e2m1x8_to_f16x2(v1[w], lo1[0], lo1[1], lo1[2], lo1[3]);
+    e2m1x8_to_f16x2(v1[w + TB / 8], hi1[0], hi1[1], hi1[2], hi1[3]);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      mma_f16(s.acc[4 * w + b], hmul2_u32(lo0[b], sA), hmul2_u32(hi0[b], sA),
+              hmul2_u32(lo1[b], sB), hmul2_u32(hi1[b], sB), pb0, pb1);
   }
 }
 
@@ -370,7 +385,14 @@ __global__ void __launch_bounds__(32, 16)
       fp4_issue<D>(p, f, ring + ls * L::kStage, lc, lblk);
       ls = ls + 1 == S ? 0 : ls + 1;
       if (++lu < hi) {
-        if (++lc.tile == lc.T) next_segment(p, lc);
+        if (++lc.tile == lc.T) {
+          next_segment(p, lc);
+          // its query rows into L1 while the tiles before it are computed
+          if ((threadIdx.x >> 2) < p.group)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(
+                f.q + (static_cast<int64_t>(lc.b) * p.num_q_heads + lc.g * p.group +
+                       (threadIdx.x >> 2)) * D + 2 * (D / 8) * (threadIdx.x & 3)));
+        }
         lblk = fp4_entry(p, lc);
       }
     }
