@@ -222,10 +222,11 @@ __device__ __forceinline__ void fp4_load_query(const DecodeParams& p, const Fp4A
   }
 }
 
-// One tile: scores, online softmax, O^T update.
+// Masked scores (log2 units) of one tile: x = (row gq, head 2tq), (gq, 2tq+1),
+// (gq+8, 2tq), (gq+8, 2tq+1).
 template <int D>
-__device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t (&qf)[D / 16][2],
-                                         float kmul, SegState<D>& s) {
+__device__ __forceinline__ void fp4_qk(uint32_t st, int valid, const uint32_t (&qf)[D / 16][2],
+                                       float kmul, float (&x)[4]) {
   using L = Fp4Layout<D>;
   constexpr int TB = L::kTB;
   const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
@@ -266,19 +267,24 @@ __device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t 
         mma_f16(sa, a0, a1, a2, a3, qf[j][0], qf[j][1]);
     }
   }
-  float x0 = (sa[0] + sb[0]) * kmul, x1 = (sa[1] + sb[1]) * kmul;
-  float x2 = (sa[2] + sb[2]) * kmul, x3 = (sa[3] + sb[3]) * kmul;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) x[q] = (sa[q] + sb[q]) * kmul;
   if (valid < kTile) {  // the segment's last tile (warp-uniform)
-    if (gq >= valid) x0 = x1 = -INFINITY;
-    if (gq + 8 >= valid) x2 = x3 = -INFINITY;
+    if (gq >= valid) x[0] = x[1] = -INFINITY;
+    if (gq + 8 >= valid) x[2] = x[3] = -INFINITY;
   }
-  float alpha0, alpha1;
-  uint32_t pb0, pb1;
-  softmax_tile<true>(x0, x1, x2, x3, s.m, s.l, 1.f, 1.f, alpha0, alpha1, pb0, pb1);
-  rescale(s, alpha0, alpha1);
-  // V pair-rows tq (tokens 2tq, 2tq+1) and tq + 4 (2tq+8, 2tq+9); the
-  // scales of those tokens in the lane's group (zero past the sequence
-  // end: those slots may hold anything, and P = 0 must meet finite V)
+}
+
+// O^T += V'^T . P^T for one tile.  V pair-rows tq (tokens 2tq, 2tq+1) and
+// tq + 4 (2tq+8, 2tq+9); the scales of those tokens in the lane's group are
+// zeroed past the sequence end (those slots may hold anything, and P = 0
+// must meet finite V).
+template <int D>
+__device__ __forceinline__ void fp4_pv(uint32_t st, int valid, uint32_t pb0, uint32_t pb1,
+                                       SegState<D>& s) {
+  using L = Fp4Layout<D>;
+  constexpr int TB = L::kTB;
+  const int lane = threadIdx.x & 31, gq = lane >> 2, tq = lane & 3;
   uint32_t v0[TB / 4], v1[TB / 4];
   lds_words<TB>(st + L::kV + fp4_vchunk<D>(tq, gq), v0);
   lds_words<TB>(st + L::kV + fp4_vchunk<D>(tq + 4, gq), v1);
@@ -305,6 +311,61 @@ __device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t 
       mma_f16(s.acc[4 * w + b], hmul2_u32(lo0[b], sA), hmul2_u32(hi0[b], sA),
               hmul2_u32(lo1[b], sB), hmul2_u32(hi1[b], sB), pb0, pb1);
   }
+}
+
+// One tile: scores, online softmax, O^T update.
+template <int D>
+__device__ __forceinline__ void fp4_tile(uint32_t st, int valid, const uint32_t (&qf)[D / 16][2],
+                                         float kmul, SegState<D>& s) {
+  float x[4];
+  fp4_qk<D>(st, valid, qf, kmul, x);
+  float alpha0, alpha1;
+  uint32_t pb0, pb1;
+  softmax_tile<true>(x[0], x[1], x[2], x[3], s.m, s.l, 1.f, 1.f, alpha0, alpha1, pb0, pb1);
+  rescale(s, alpha0, alpha1);
+  fp4_pv<D>(st, valid, pb0, pb1, s);
+}
+
+// Two consecutive tiles of one segment (the first one full): both score
+// blocks, one online-softmax update over their 32 tokens (the running max
+// moves only when a score passes it by more than 8 in log2 units, as in
+// softmax_tile), then both O^T updates.
+template <int D>
+__device__ __forceinline__ void fp4_tile2(uint32_t sta, uint32_t stb, int valid_b,
+                                          const uint32_t (&qf)[D / 16][2], float kmul,
+                                          SegState<D>& s) {
+  float xa[4], xb[4];
+  fp4_qk<D>(sta, kTile, qf, kmul, xa);
+  fp4_qk<D>(stb, valid_b, qf, kmul, xb);
+  constexpr float kSlack = 8.f;
+  float mx0 = fmaxf(fmaxf(xa[0], xa[2]), fmaxf(xb[0], xb[2]));
+  float mx1 = fmaxf(fmaxf(xa[1], xa[3]), fmaxf(xb[1], xb[3]));
+  float alpha0 = 1.f, alpha1 = 1.f;
+  if (__any_sync(0xffffffffu, mx0 > s.m[0] + kSlack || mx1 > s.m[1] + kSlack)) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(s.m[0], mx0), mn1 = fmaxf(s.m[1], mx1);
+    alpha0 = fast_exp2(s.m[0] - mn0);
+    alpha1 = fast_exp2(s.m[1] - mn1);
+    s.m[0] = mn0;
+    s.m[1] = mn1;
+  }
+  float pa[4], pb[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    pa[q] = fast_exp2(xa[q] - s.m[q & 1]);
+    pb[q] = fast_exp2(xb[q] - s.m[q & 1]);
+  }
+  s.l[0] = s.l[0] * alpha0 + ((pa[0] + pa[2]) + (pb[0] + pb[2]));
+  s.l[1] = s.l[1] * alpha1 + ((pa[1] + pa[3]) + (pb[1] + pb[3]));
+  rescale(s, alpha0, alpha1);
+  fp4_pv<D>(sta, kTile, movmatrix_t(pack_f16x2(pa[0], pa[1])),
+            movmatrix_t(pack_f16x2(pa[2], pa[3])), s);
+  fp4_pv<D>(stb, valid_b, movmatrix_t(pack_f16x2(pb[0], pb[1])),
+            movmatrix_t(pack_f16x2(pb[2], pb[3])), s);
 }
 
 // Write a finished piece (as finish_piece: the output when the piece is the
@@ -412,14 +473,29 @@ __global__ void __launch_bounds__(32, 16)
     fp4_load_query<D>(p, f, c, qf);
     seg_reset(s);
 #pragma unroll 1
-    for (int32_t tile = c.tile; tile < seg_end; ++tile) {
+    // Two tiles per step while two remain.  Each step starts with one copy
+    // issued; a pair step issues its second copy after both of its stages
+    // are read, so kStages - 2 tiles stay in flight during its math.
+    for (int32_t tile = c.tile; tile < seg_end;) {
       top_up();
-      fp4_cp_wait<S - 1>();  // tile u has landed
-      __syncwarp();
-      const int valid = min(kTile, c.n - tile * kTile);
-      fp4_tile<D>(ring + cs * L::kStage, valid, qf, kmul, s);
-      cs = cs + 1 == S ? 0 : cs + 1;
-      __syncwarp();  // the stage is read before a later copy overwrites it
+      if (tile + 1 < seg_end) {
+        fp4_cp_wait<S - 2>();  // tiles u and u + 1 have landed
+        __syncwarp();
+        const int cs2 = cs + 1 == S ? 0 : cs + 1;
+        fp4_tile2<D>(ring + cs * L::kStage, ring + cs2 * L::kStage,
+                     min(kTile, c.n - (tile + 1) * kTile), qf, kmul, s);
+        cs = cs2 + 1 == S ? 0 : cs2 + 1;
+        __syncwarp();  // both stages are read before later copies overwrite them
+        top_up();
+        tile += 2;
+      } else {
+        fp4_cp_wait<S - 1>();  // tile u has landed
+        __syncwarp();
+        fp4_tile<D>(ring + cs * L::kStage, min(kTile, c.n - tile * kTile), qf, kmul, s);
+        cs = cs + 1 == S ? 0 : cs + 1;
+        __syncwarp();
+        ++tile;
+      }
     }
     fp4_finish<D>(p, f, s, c, whole, blockIdx.x);
     if (!whole && seg_end == c.T && lane == 0)
