@@ -13,7 +13,9 @@ against the oracle's NVFP4 restatement, through the C ABI.
   including the 70B / 128K layer; unused slots and blocks hold NaN block
   scales and must never reach the output;
 * empty and ragged sequences, every work-partition count within tolerance and
-  repeated calls bit-identical, out-of-pool table entries and slots flagged.
+  repeated calls bit-identical, out-of-pool table entries and slots flagged;
+* shapes beyond the workloads: MQA over 300 sequences, MHA at block size 256,
+  a group of 3, one 256K-token sequence split across every CTA.
 """
 import numpy as np
 import pytest
@@ -72,8 +74,10 @@ def oracle_pool(snap, k_gs, v_gs):
 
 
 def assert_pool_equal(cache, ocache, ids):
+    """GPU blocks ids[i] against the oracle's local blocks i, i < len(ids)."""
     idx = torch.tensor(ids, dtype=torch.int64, device="cuda")
     for name, g, o in zip(("k", "k_sf", "v", "v_sf"), cache, ocache):
+        o = o[:len(ids)]
         got = _np(g.index_select(0, idx))
         bad = np.argwhere(got != o)
         assert bad.size == 0, f"{name}: {len(bad)} bytes differ, first at {bad[0]}"
@@ -154,7 +158,7 @@ def test_70b_128k_sampled():
     case.k_cache = case.v_cache = None  # the bf16 pool is no longer needed
     ocache = oracle_pool(snap, k_gs, v_gs)
     # the sequence's first 64 blocks, byte for byte
-    assert_pool_equal(cache, tuple(a[:64] for a in ocache), snap[0][:64])
+    assert_pool_equal(cache, ocache, snap[0][:64])
     out = run_decode(case, cache, k_gs, v_gs)
     ref = oracle_out(case, snap, ocache, k_gs, v_gs, seqs, heads=heads)
     assert_close(out, ref, TOL, "nvfp4 70b 128k")
@@ -269,4 +273,37 @@ def test_bad_table_entry_and_slot_are_flagged():
     cache[3][0, :, :, 3] = before[3][0, :, :, 3]
     for a, b in zip(cache, before):
         assert torch.equal(a, b)
+    assert pa.pa_get_device_error() == 0
+
+
+def _workload(name, B, hq, hkv, d, bs, lens, seed):
+    need = sum(-(-n // bs) for n in lens)
+    return W.Workload(name, B, hq, hkv, d, bs, seq_lens=lens,
+                      pool_blocks=int(np.ceil(1.3 * need)) + 2, seed=seed)
+
+
+def _lens(B, lo, hi, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(lo, hi + 1, (B,), generator=g).tolist()
+
+
+@pytest.mark.parametrize("name,B,hq,hkv,d,bs,lo,hi", [
+    ("mqa", 300, 8, 1, 128, 32, 1, 600),       # several 128-sequence length scans
+    ("mha_bs256", 5, 4, 4, 64, 256, 200, 1500),  # group 1, the largest block size
+    ("gqa3", 40, 6, 2, 128, 16, 1, 700),       # a group of 3
+    ("long1", 1, 8, 1, 64, 16, 262144, 262144),  # one 256K sequence over every CTA
+])
+def test_shape_parity(name, B, hq, hkv, d, bs, lo, hi):
+    case = build_case(_workload(name, B, hq, hkv, d, bs, _lens(B, lo, hi, 7), 41))
+    seqs = list(range(B))
+    snap = snapshot_blocks(case, seqs)
+    k_gs, v_gs = gscales(snap)
+    cache = gpu_pool(case, k_gs, v_gs)
+    ocache = oracle_pool(snap, k_gs, v_gs)
+    assert_pool_equal(cache, ocache, snap[0][:256])
+    poison_unused(cache, case)
+    ref = oracle_out(case, snap, ocache, k_gs, v_gs, seqs)
+    for splits in (0, 3):
+        out = run_decode(case, cache, k_gs, v_gs, num_splits=splits)
+        assert_close(out, ref, TOL, f"nvfp4 {name} splits {splits}")
     assert pa.pa_get_device_error() == 0
