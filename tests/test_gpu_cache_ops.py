@@ -12,6 +12,7 @@ import numpy as np
 import pytest
 import torch
 
+from oracle import e2m1, e4m3
 from oracle import paged_attention as OPA
 from oracle import quantize as OQ
 from paged_kv_cache_228_gb300 import pa
@@ -196,3 +197,68 @@ def test_cache_write_fp8_bad_slot_is_flagged_and_skipped():
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() & pa.DEVERR_BAD_SLOT
     assert torch.equal(kq, k0) and torch.equal(ks, s0)
+
+
+def _bf16_values(limit):
+    """Every finite bf16 value with |x| <= limit, as float32 (both zeros)."""
+    bits = torch.arange(65536, dtype=torch.int32).to(torch.int16)
+    x = bits.view(torch.bfloat16).float()
+    keep = torch.isfinite(x) & (x.abs() <= limit)
+    return x[keep]
+
+
+def test_quantize_codes_exhaustive_over_bf16():
+    # Every bf16 input in [-448, 448] through the GPU conversion: each (block,
+    # head) tile holds one 448, so its scale is exactly 1 and the code is
+    # e4m3(x); the oracle encodes the same values.
+    dev = "cuda"
+    vals = _bf16_values(448.0)
+    per = 16 * 128 - 1
+    n_tiles = -(-vals.numel() // per)
+    x = torch.zeros(n_tiles * per)
+    x[:vals.numel()] = vals
+    tiles = torch.cat([torch.full((n_tiles, 1), 448.0), x.view(n_tiles, per)], dim=1)
+    k = tiles.view(n_tiles, 1, 16, 128).to(torch.bfloat16).to(dev)
+    ids = torch.arange(n_tiles, dtype=torch.int32, device=dev)
+    valid = torch.full((n_tiles,), 16, dtype=torch.int32, device=dev)
+    kq = torch.empty(k.shape, dtype=torch.uint8, device=dev)
+    ks = torch.empty((n_tiles, 1), device=dev)
+    pa.pa_quantize_fp8(k, k, ids, valid, kq, kq.clone(), ks, ks.clone())
+    torch.cuda.synchronize()
+    assert torch.all(ks == 1.0)
+    got = kq.view(n_tiles, -1)[:, 1:].reshape(-1)[:vals.numel()].cpu().numpy()
+    ref = e4m3.encode_fast(vals.numpy())
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, (bad.size, vals[bad[:5]].tolist(), got[bad[:5]], ref[bad[:5]])
+    assert pa.pa_get_device_error() == 0
+
+
+def test_nvfp4_codes_exhaustive_over_bf16():
+    # Every bf16 input in [-6, 6] through the NVFP4 writer: each 16-value
+    # group holds one 6 and the tensor scale is 1/6, so the block scale is 6
+    # (E4M3 0x4C), the divisor 6 * (1/6) rounds to exactly 1 in fp32, and the
+    # code is e2m1(x); the oracle encodes the same values.
+    dev = "cuda"
+    vals = _bf16_values(6.0)
+    per_row = 128 - 8                                 # 8 groups of 15 values + one 6
+    rows = -(-vals.numel() // per_row)
+    x = torch.zeros(rows * per_row)
+    x[:vals.numel()] = vals
+    g = x.view(rows, 8, 15)
+    row = torch.cat([torch.full((rows, 8, 1), 6.0), g], dim=2).view(rows, 1, 128)
+    kn = row.to(torch.bfloat16).to(dev)
+    bs = 16
+    nb = -(-rows // bs)
+    cache = pa.nvfp4_empty_cache(nb, 1, bs, 128)
+    slots = torch.arange(rows, dtype=torch.int64, device=dev)
+    pa.pa_cache_write_nvfp4(kn, kn, slots, cache, 1.0 / 6.0, 1.0 / 6.0)
+    torch.cuda.synchronize()
+    k, k_sf = cache[0].cpu().numpy(), cache[1].cpu().numpy()
+    assert np.all(k_sf.reshape(-1)[:rows * 8] == 0x4C)
+    b = k.reshape(nb * bs, 64)[:rows]
+    codes = np.stack([b & 0xF, b >> 4], axis=-1).reshape(rows, 8, 16)[:, :, 1:]
+    got = codes.reshape(-1)[:vals.numel()]
+    ref = e2m1.encode(vals.numpy())
+    bad = np.flatnonzero(got != ref)
+    assert bad.size == 0, (bad.size, vals[bad[:5]].tolist(), got[bad[:5]], ref[bad[:5]])
+    assert pa.pa_get_device_error() == 0
