@@ -823,14 +823,13 @@ __device__ __forceinline__ void pv_fp8(uint32_t vb, float vmax, uint32_t pb0,
     const uint32_t u2 = __byte_perm(v2, 0, 0x3120);
     const uint32_t u3 = __byte_perm(v3, 0, 0x3120);
     float t0[4], t1[4];
-    mma_f16_zero_c(t0, e4m3x2_to_f16x2(static_cast<uint16_t>(u0)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u0 >> 16)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u1)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u1 >> 16)), pb0, pb1);
-    mma_f16_zero_c(t1, e4m3x2_to_f16x2(static_cast<uint16_t>(u2)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u2 >> 16)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u3)),
-                   e4m3x2_to_f16x2(static_cast<uint16_t>(u3 >> 16)), pb0, pb1);
+    uint32_t c[8];
+    e4m3x4_to_f16x2x2(u0, c[0], c[1]);
+    e4m3x4_to_f16x2x2(u1, c[2], c[3]);
+    e4m3x4_to_f16x2x2(u2, c[4], c[5]);
+    e4m3x4_to_f16x2x2(u3, c[6], c[7]);
+    mma_f16_zero_c(t0, c[0], c[1], c[2], c[3], pb0, pb1);
+    mma_f16_zero_c(t1, c[4], c[5], c[6], c[7], pb0, pb1);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       s.acc[2 * pp][q] = fmaf(vmax, t0[q], s.acc[2 * pp][q]);

@@ -218,6 +218,18 @@ __device__ __forceinline__ float2 unpack_f16x2(uint32_t x) {
   return __half22float2(h);
 }
 
+// Four E4M3 bytes -> two f16x2 (bytes 0, 1 -> lo; bytes 2, 3 -> hi), exact.
+// The word is split into its 16-bit halves by one unpacking move, so each
+// conversion takes its pair directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\t"
+      "mov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
 // Two E4M3 bytes (low byte first) -> f16x2, exact (every E4M3 value is an
 // f16 value).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t x) {
