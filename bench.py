@@ -313,6 +313,8 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
 
     def step(i, ev=None):
         if nvfp4:
+            # NVFP4 cache: the step's tokens written by their own launch, then
+            # the decode (measured faster than pa_decode_append_nvfp4 here)
             c, (kg, vg) = pools[i % n_pools], scales[i % n_pools]
             pa.pa_cache_write_nvfp4(kn, vn, slots, c, kg, vg, stream=stream)
             if ev is not None:
@@ -446,7 +448,7 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
         "pool_bytes": per_pool // (2 if fp8 else 1),
         "clocks": clocks if clocks is not None else (sampler.summary() if sampler else None),
         "e2e": e2e,
-        # decode (with the fused cache write) + merge; NVFP4: + the cache write
+        # decode (with the fused cache write) + merge; NVFP4: + its cache write
         "launches_per_step": 3 if nvfp4 else 2,
     }
 

@@ -369,6 +369,27 @@ pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const void* v_cach
                           void* out, void* workspace, size_t workspace_bytes,
                           int32_t num_splits, void* stream);
 
+/* pa_decode_append_nvfp4 -- the NVFP4 decode step in one launch: the same
+ * pools and output, bit for bit, as
+ *     pa_cache_write_nvfp4(k_new, v_new, slot_mapping, num_seqs, ...);
+ *     pa_decode_nvfp4(q, k_cache, v_cache, k_sf, v_sf, ...);
+ * where row b of k_new / v_new ([num_seqs][num_kv_heads][head_dim] bf16) is
+ * sequence b's new token.  The CTA that copies a (sequence, KV head)'s last
+ * tile first quantises that head's new rows into it.  Requirements as
+ * pa_decode_append: slot_mapping[b] >= 0 must be the slot of position
+ * seq_lens[b] - 1 in a block private to b; another slot, or one on an empty
+ * sequence, is not written and flags PA_DEVERR_BAD_SLOT; < 0 appends nothing.
+ * The pools are read and written; other arguments as pa_decode_nvfp4. */
+pa_status pa_decode_append_nvfp4(const void* q, const void* k_new, const void* v_new,
+                                 const int64_t* slot_mapping, void* k_cache, void* v_cache,
+                                 void* k_sf, void* v_sf, float k_gscale, float v_gscale,
+                                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                 const int32_t* seq_lens, int32_t num_seqs,
+                                 int32_t num_q_heads, int32_t num_kv_heads,
+                                 int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                 float scale, void* out, void* workspace,
+                                 size_t workspace_bytes, int32_t num_splits, void* stream);
+
 /* pa_decode_cascade -- pa_decode for a batch whose sequences all start with
  * the same prefix_len tokens in the same physical blocks (forks of one
  * prompt): "Paged Attention and KV Cache Fragmentation", section "How

@@ -177,13 +177,17 @@ pa_status fp4_plan(int dev, int* ctas_per_sm) {
   std::lock_guard<std::mutex> lk(g_mu);
   if (cached[dev] == 0) {
     const size_t smem = fp4_smem_bytes<D>();
-    if (cudaFuncSetAttribute(paged_decode_nvfp4_kernel<D>,
+    if (cudaFuncSetAttribute(paged_decode_nvfp4_kernel<D, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(paged_decode_nvfp4_kernel<D, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return PA_ERR_CUDA;
+    // the plain instantiation sets the grid; the append one launches the same
     int n = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_nvfp4_kernel<D>, 32,
-                                                      smem) != cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_nvfp4_kernel<D, false>,
+                                                      32, smem) != cudaSuccess)
       return PA_ERR_CUDA;
     if (n < 1) return PA_ERR_UNSUPPORTED;
     cached[dev] = n < kMaxCtasPerSm ? n : kMaxCtasPerSm;
@@ -956,8 +960,10 @@ pa_status launch_fp4_decode(const DecodeParams& prm_in, const Fp4Args& f, void* 
     w += static_cast<size_t>(pieces) * kMaxG * sizeof(float2);
     prm.ws_job = reinterpret_cast<int2*>(w);
   }
-  if (launch_pdl(paged_decode_nvfp4_kernel<D>, dim3(static_cast<unsigned>(P)), dim3(32),
-                 fp4_smem_bytes<D>(), stream, prm, f) != cudaSuccess)
+  if (launch_pdl(f.slot_mapping != nullptr ? paged_decode_nvfp4_kernel<D, true>
+                                           : paged_decode_nvfp4_kernel<D, false>,
+                 dim3(static_cast<unsigned>(P)), dim3(32), fp4_smem_bytes<D>(), stream, prm,
+                 f) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
                  dim3(kMaxG * D / 4), 0, stream, prm) != cudaSuccess)
@@ -1009,14 +1015,17 @@ extern "C" pa_status pa_cache_write_nvfp4(const void* k_new, const void* v_new,
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const void* v_cache,
-                                     const void* k_sf, const void* v_sf, float k_gscale,
-                                     float v_gscale, const int32_t* block_tables,
-                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
-                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                     int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                                     float scale, void* out, void* workspace,
-                                     size_t workspace_bytes, int32_t num_splits, void* stream) {
+namespace pa {
+namespace {
+
+pa_status fp4_decode_entry(const void* q, const void* k_cache, const void* v_cache,
+                           const void* k_sf, const void* v_sf, float k_gscale, float v_gscale,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs, int32_t num_q_heads,
+                           int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                           int32_t num_blocks, float scale, void* out, void* workspace,
+                           size_t workspace_bytes, int32_t num_splits, void* stream,
+                           const AppendArgs* app) {
   if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks <= 0 ||
       max_blocks_per_seq < 0 || num_splits < 0 || !(scale == scale) ||
       num_q_heads % num_kv_heads != 0 || !finite_pos(k_gscale) || !finite_pos(v_gscale))
@@ -1028,6 +1037,10 @@ extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const v
       !aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_sf) ||
       !aligned16(v_sf) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
       (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PA_ERR_INVALID_ARG;
+  if (app != nullptr &&
+      (!app->k_new || !app->v_new || !app->slot_mapping || !aligned16(app->k_new) ||
+       !aligned16(app->v_new) || (reinterpret_cast<uintptr_t>(app->slot_mapping) & 7u)))
     return PA_ERR_INVALID_ARG;
   if (static_cast<int64_t>(num_seqs) * num_q_heads > INT_MAX - 64) return PA_ERR_UNSUPPORTED;
   if (static_cast<int64_t>(max_blocks_per_seq) * block_size > INT_MAX - 64)
@@ -1046,16 +1059,55 @@ extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const v
   p.max_blocks = max_blocks_per_seq;
   p.num_blocks = num_blocks;
   p.scale_log2 = scale * 1.4426950408889634f;
+  // the merge kernel flags a new token of an empty sequence
+  if (app != nullptr) p.slot_mapping = app->slot_mapping;
   Fp4Args f;
+  std::memset(&f, 0, sizeof(f));
   f.q = static_cast<const __nv_bfloat16*>(q);
-  f.k = static_cast<const uint8_t*>(k_cache);
-  f.v = static_cast<const uint8_t*>(v_cache);
-  f.k_sf = static_cast<const uint8_t*>(k_sf);
-  f.v_sf = static_cast<const uint8_t*>(v_sf);
+  f.k = static_cast<uint8_t*>(const_cast<void*>(k_cache));
+  f.v = static_cast<uint8_t*>(const_cast<void*>(v_cache));
+  f.k_sf = static_cast<uint8_t*>(const_cast<void*>(k_sf));
+  f.v_sf = static_cast<uint8_t*>(const_cast<void*>(v_sf));
   f.k_gs = k_gscale;
   f.v_gs = v_gscale;
+  if (app != nullptr) {
+    f.k_new = static_cast<const __nv_bfloat16*>(app->k_new);
+    f.v_new = static_cast<const __nv_bfloat16*>(app->v_new);
+    f.slot_mapping = app->slot_mapping;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (head_dim == 128)
     return launch_fp4_decode<128>(p, f, workspace, workspace_bytes, num_splits, s);
   return launch_fp4_decode<64>(p, f, workspace, workspace_bytes, num_splits, s);
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const void* v_cache,
+                                     const void* k_sf, const void* v_sf, float k_gscale,
+                                     float v_gscale, const int32_t* block_tables,
+                                     int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                     float scale, void* out, void* workspace,
+                                     size_t workspace_bytes, int32_t num_splits, void* stream) {
+  return fp4_decode_entry(q, k_cache, v_cache, k_sf, v_sf, k_gscale, v_gscale, block_tables,
+                          max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                          head_dim, block_size, num_blocks, scale, out, workspace,
+                          workspace_bytes, num_splits, stream, nullptr);
+}
+
+extern "C" pa_status pa_decode_append_nvfp4(
+    const void* q, const void* k_new, const void* v_new, const int64_t* slot_mapping,
+    void* k_cache, void* v_cache, void* k_sf, void* v_sf, float k_gscale, float v_gscale,
+    const int32_t* block_tables, int32_t max_blocks_per_seq, const int32_t* seq_lens,
+    int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+    int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
+    size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const AppendArgs app{k_new, v_new, slot_mapping};
+  return fp4_decode_entry(q, k_cache, v_cache, k_sf, v_sf, k_gscale, v_gscale, block_tables,
+                          max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
+                          head_dim, block_size, num_blocks, scale, out, workspace,
+                          workspace_bytes, num_splits, stream, &app);
 }

@@ -46,11 +46,17 @@ namespace pa {
 
 struct Fp4Args {
   const __nv_bfloat16* q;  // [B][Hq][D]
-  const uint8_t* k;
-  const uint8_t* v;
-  const uint8_t* k_sf;
-  const uint8_t* v_sf;
+  uint8_t* k;              // pools; written only by the fused append
+  uint8_t* v;
+  uint8_t* k_sf;
+  uint8_t* v_sf;
   float k_gs, v_gs;  // tensor scales S_k, S_v
+  // Fused append (null when off): sequence b's new token rows
+  // k_new/v_new[b][Hkv][D] go to slot_mapping[b] (< 0: none), which must be
+  // the slot the table gives position seq_lens[b] - 1.
+  const __nv_bfloat16* k_new;
+  const __nv_bfloat16* v_new;
+  const int64_t* slot_mapping;
 };
 
 template <int D>
@@ -418,10 +424,100 @@ __device__ __forceinline__ void fp4_finish(const DecodeParams& p, const Fp4Args&
   }
 }
 
+// ------------------------------------------------------------ row writer --
+// Quantise one bf16 row x (D values) with tensor scale gs into token `off`
+// of (block, KV head) hb: the K layout (kv = 0) or the V layout (kv = 1).
+// Warp-collective: lane l quantises values [E l, E l + E), E = D / 32, with
+// the lanes of its 16-value group.  A V value is one nibble of its
+// pair-row byte, which the token's neighbour shares, so V bytes are updated
+// by word atomics on disjoint nibbles.
+template <int D>
+__device__ __forceinline__ void fp4_put_row(const __nv_bfloat16* __restrict__ x, int kv, float gs,
+                                            int64_t hb, int64_t off, int32_t block_size,
+                                            uint8_t* k, uint8_t* k_sf, uint8_t* v,
+                                            uint8_t* v_sf) {
+  constexpr int E = D / 32;    // values per lane
+  constexpr int LPG = 16 / E;  // lanes per group
+  constexpr int NG = D / 16;
+  const int lane = threadIdx.x & 31;
+  float xv[E];
+  if constexpr (E == 4) {
+    const uint2 w = *reinterpret_cast<const uint2*>(x + E * lane);
+    const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y);
+    xv[0] = a.x; xv[1] = a.y; xv[2] = b.x; xv[3] = b.y;
+  } else {
+    const float2 a = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(x + E * lane));
+    xv[0] = a.x; xv[1] = a.y;
+  }
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(xv[i]));
+#pragma unroll
+  for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const uint32_t sf = f32x2_to_e4m3x2(__fdiv_rn(amax, __fmul_rn(6.f, gs)), 0.f) & 0xffu;
+  const float sv = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(sf))).x;
+  uint32_t codes = 0;  // value i of the lane in bits 4i..4i+3
+  if (sv > 0.f) {
+    const float den = __fmul_rn(sv, gs);
+#pragma unroll
+    for (int i = 0; i < E; ++i) codes |= e2m1_rne(__fdiv_rn(xv[i], den)) << (4 * i);
+  }
+  const int grp = lane / LPG;
+  if (kv == 0) {
+    uint8_t* dst = k + (hb * block_size + off) * (D / 2) + (E / 2) * lane;
+    if constexpr (E == 4)
+      *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
+    else
+      *dst = static_cast<uint8_t>(codes);
+    if (lane % LPG == 0) k_sf[(hb * block_size + off) * NG + grp] = static_cast<uint8_t>(sf);
+  } else {
+    // bytes E*lane .. E*lane + E - 1 of pair-row off/2, nibble off & 1
+    const int nib = static_cast<int>(off & 1) * 4;
+    uint32_t val = 0, mask = 0;
+#pragma unroll
+    for (int i = 0; i < E; ++i) {
+      val |= ((codes >> (4 * i)) & 0xFu) << (8 * i + nib);
+      mask |= 0xFu << (8 * i + nib);
+    }
+    uint8_t* row = v + (hb * (block_size >> 1) + (off >> 1)) * D;
+    const int byte = E * lane;
+    const int shift = (byte & 3) * 8;
+    unsigned int* word = reinterpret_cast<unsigned int*>(row + (byte & ~3));
+    atomicAnd(word, ~(mask << shift));
+    atomicOr(word, val << shift);
+    if (lane % LPG == 0) v_sf[(hb * NG + grp) * block_size + off] = static_cast<uint8_t>(sf);
+  }
+}
+
+// The fused append: before the copy of segment c's last tile (in block
+// blk), quantise its sequence's new K and V rows of head c.g into position
+// n - 1.  A slot that is not that position's is not written and flags
+// PA_DEVERR_BAD_SLOT.  The rows are visible to the warp's copies after the
+// block-scope fence and the warp barrier.
+template <int D>
+__device__ __forceinline__ void fp4_append_new(const DecodeParams& p, const Fp4Args& f,
+                                               const Cursor& c, int32_t blk) {
+  const int64_t slot = f.slot_mapping[c.b];
+  if (slot < 0) return;
+  const int64_t off = (c.n - 1) & (p.block_size - 1);
+  if (blk < 0 || blk >= p.num_blocks ||
+      slot != static_cast<int64_t>(blk) * p.block_size + off) {
+    if ((threadIdx.x & 31) == 0) flag_error(PA_DEVERR_BAD_SLOT);
+    return;
+  }
+  const int64_t hb = static_cast<int64_t>(blk) * p.num_kv_heads + c.g;
+  const int64_t row = (static_cast<int64_t>(c.b) * p.num_kv_heads + c.g) * D;
+  fp4_put_row<D>(f.k_new + row, 0, f.k_gs, hb, off, p.block_size, f.k, f.k_sf, f.v, f.v_sf);
+  fp4_put_row<D>(f.v_new + row, 1, f.v_gs, hb, off, p.block_size, f.k, f.k_sf, f.v, f.v_sf);
+  __threadfence_block();
+  __syncwarp();
+}
+
 // One warp per CTA; tiles [lo, hi) of the flat list, kStages - 1 tiles in
 // flight ahead of the one computed.  Every cp.async group is waited for
-// before the CTA exits.
-template <int D>
+// before the CTA exits.  kAppend: the fused append (a separate
+// instantiation, so that plain decode keeps its registers).
+template <int D, bool kAppend>
 __global__ void __launch_bounds__(32, 16)
     paged_decode_nvfp4_kernel(const DecodeParams p, const Fp4Args f) {
   using L = Fp4Layout<D>;
@@ -443,16 +539,24 @@ __global__ void __launch_bounds__(32, 16)
   int ls = 0;  // stage of tile lu
   auto top_up = [&]() {
     if (lu < hi) {
+      if (kAppend && lc.tile == lc.T - 1) fp4_append_new<D>(p, f, lc, lblk);
       fp4_issue<D>(p, f, ring + ls * L::kStage, lc, lblk);
       ls = ls + 1 == S ? 0 : ls + 1;
       if (++lu < hi) {
         if (++lc.tile == lc.T) {
           next_segment(p, lc);
-          // its query rows into L1 while the tiles before it are computed
+          // its query rows (and new K/V rows) into L1 while the tiles
+          // before it are computed
           if ((threadIdx.x >> 2) < p.group)
             asm volatile("prefetch.global.L1 [%0];" ::"l"(
                 f.q + (static_cast<int64_t>(lc.b) * p.num_q_heads + lc.g * p.group +
                        (threadIdx.x >> 2)) * D + 2 * (D / 8) * (threadIdx.x & 3)));
+          if (kAppend) {
+            const int64_t row =
+                (static_cast<int64_t>(lc.b) * p.num_kv_heads + lc.g) * D + (D / 32) * lane;
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(f.k_new + row));
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(f.v_new + row));
+          }
         }
         lblk = fp4_entry(p, lc);
       }
@@ -507,11 +611,7 @@ __global__ void __launch_bounds__(32, 16)
 }
 
 // ------------------------------------------------------------ cache write --
-// One warp per (token, K or V, KV head) row: lane l quantises values
-// [E l, E l + E), E = D / 32, with the lanes of its 16-value group.  A V
-// value goes into one nibble of its pair-row byte; two tokens of a pair
-// written by one launch share bytes, so V bytes are updated by word
-// atomics on disjoint nibbles.
+// One warp per (token, K or V, KV head) row (fp4_put_row).
 template <int D>
 __global__ void __launch_bounds__(256)
     cache_write_nvfp4_kernel(const __nv_bfloat16* __restrict__ k_new,
@@ -521,9 +621,6 @@ __global__ void __launch_bounds__(256)
                              uint8_t* __restrict__ k, uint8_t* __restrict__ k_sf,
                              uint8_t* __restrict__ v, uint8_t* __restrict__ v_sf, float k_gs,
                              float v_gs) {
-  constexpr int E = D / 32;     // values per lane
-  constexpr int LPG = 16 / E;   // lanes per group
-  constexpr int NG = D / 16;
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -541,56 +638,8 @@ __global__ void __launch_bounds__(256)
       continue;
     }
     const int64_t blk = slot / block_size, off = slot - blk * block_size;
-    const __nv_bfloat16* x = (kv ? v_new : k_new) + (t * num_kv_heads + h) * D + E * lane;
-    float xv[E];
-    if constexpr (E == 4) {
-      const uint2 w = *reinterpret_cast<const uint2*>(x);
-      const float2 a = unpack_bf16x2(w.x), b = unpack_bf16x2(w.y);
-      xv[0] = a.x; xv[1] = a.y; xv[2] = b.x; xv[3] = b.y;
-    } else {
-      const float2 a = unpack_bf16x2(*reinterpret_cast<const uint32_t*>(x));
-      xv[0] = a.x; xv[1] = a.y;
-    }
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < E; ++i) amax = fmaxf(amax, fabsf(xv[i]));
-#pragma unroll
-    for (int o = 1; o < LPG; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float gs = kv ? v_gs : k_gs;
-    const uint32_t sf = f32x2_to_e4m3x2(__fdiv_rn(amax, __fmul_rn(6.f, gs)), 0.f) & 0xffu;
-    const float sv = unpack_f16x2(e4m3x2_to_f16x2(static_cast<uint16_t>(sf))).x;
-    uint32_t codes = 0;  // value i of the lane in bits 4i..4i+3
-    if (sv > 0.f) {
-      const float den = __fmul_rn(sv, gs);
-#pragma unroll
-      for (int i = 0; i < E; ++i) codes |= e2m1_rne(__fdiv_rn(xv[i], den)) << (4 * i);
-    }
-    const int grp = lane / LPG;
-    const int64_t hb = blk * num_kv_heads + h;
-    if (kv == 0) {
-      uint8_t* dst = k + (hb * block_size + off) * (D / 2) + (E / 2) * lane;
-      if constexpr (E == 4)
-        *reinterpret_cast<uint16_t*>(dst) = static_cast<uint16_t>(codes);
-      else
-        *dst = static_cast<uint8_t>(codes);
-      if (lane % LPG == 0) k_sf[(hb * block_size + off) * NG + grp] = static_cast<uint8_t>(sf);
-    } else {
-      // bytes E*lane .. E*lane + E - 1 of pair-row off/2, nibble off & 1
-      const int nib = static_cast<int>(off & 1) * 4;
-      uint32_t val = 0, mask = 0;
-#pragma unroll
-      for (int i = 0; i < E; ++i) {
-        val |= ((codes >> (4 * i)) & 0xFu) << (8 * i + nib);
-        mask |= 0xFu << (8 * i + nib);
-      }
-      uint8_t* row = v + (hb * (block_size >> 1) + (off >> 1)) * D;
-      const int byte = E * lane;
-      const int shift = (byte & 3) * 8;
-      unsigned int* word = reinterpret_cast<unsigned int*>(row + (byte & ~3));
-      atomicAnd(word, ~(mask << shift));
-      atomicOr(word, val << shift);
-      if (lane % LPG == 0) v_sf[(hb * NG + grp) * block_size + off] = static_cast<uint8_t>(sf);
-    }
+    fp4_put_row<D>((kv ? v_new : k_new) + (t * num_kv_heads + h) * D, kv, kv ? v_gs : k_gs,
+                   blk * num_kv_heads + h, off, block_size, k, k_sf, v, v_sf);
   }
 }
 

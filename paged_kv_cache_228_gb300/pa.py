@@ -75,6 +75,11 @@ SIGNATURES = {
                                  ctypes.c_float, _c_ptr, _c_int, _c_ptr, _c_int, _c_int, _c_int,
                                  _c_int, _c_int, _c_int, ctypes.c_float, _c_ptr, _c_ptr,
                                  _c_size, _c_int, _c_ptr]),
+    "pa_decode_append_nvfp4": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr, _c_ptr,
+                                        _c_ptr, ctypes.c_float, ctypes.c_float, _c_ptr, _c_int,
+                                        _c_ptr, _c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                        ctypes.c_float, _c_ptr, _c_ptr, _c_size, _c_int,
+                                        _c_ptr]),
     "pa_allocator_create": (_c_int, [_c_int, ctypes.POINTER(_c_ptr)]),
     "pa_allocator_destroy": (None, [_c_ptr]),
     "pa_block_alloc": (_c_int, [_c_ptr, _c_int, _c_ptr]),
@@ -369,6 +374,33 @@ def pa_decode_nvfp4(q, cache, k_gscale, v_gscale, block_tables, seq_lens, scale,
         _ptr(q), _ptr(k), _ptr(v), _ptr(k_sf), _ptr(v_sf), float(k_gscale), float(v_gscale),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, hq, hkv, dq, bs, nb,
         float(scale), _ptr(out), _ptr(workspace), ws_bytes, num_splits, _stream(stream)))
+
+
+def pa_decode_append_nvfp4(q, k_new, v_new, slot_mapping, cache, k_gscale, v_gscale,
+                           block_tables, seq_lens, scale, out, workspace=None, num_splits=0,
+                           stream=None):
+    """The NVFP4 decode step in one launch: pa_cache_write_nvfp4 of row b of
+    k_new / v_new at slot_mapping[b], then pa_decode_nvfp4, bit for bit."""
+    _need(q, torch.bfloat16, "q", 3)
+    _need(k_new, torch.bfloat16, "k_new", 3)
+    _need(v_new, torch.bfloat16, "v_new", 3)
+    _need(slot_mapping, torch.int64, "slot_mapping", 1)
+    _need(out, torch.bfloat16, "out", 3)
+    _need(block_tables, torch.int32, "block_tables", 2)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    nb, hkv, bs, d = _nvfp4_dims(cache)
+    k, k_sf, v, v_sf = cache
+    B, hq, dq = q.shape
+    if tuple(k_new.shape) != (B, hkv, dq) or tuple(v_new.shape) != (B, hkv, dq) or \
+            slot_mapping.shape[0] != B:
+        raise ValueError("pa_decode_append_nvfp4: k_new/v_new must be [B, Hkv, d], "
+                         "slot_mapping [B]")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("pa_decode_append_nvfp4", lib().pa_decode_append_nvfp4(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(k), _ptr(v), _ptr(k_sf),
+        _ptr(v_sf), float(k_gscale), float(v_gscale), _ptr(block_tables), block_tables.shape[1],
+        _ptr(seq_lens), B, hq, hkv, dq, bs, nb, float(scale), _ptr(out), _ptr(workspace),
+        ws_bytes, num_splits, _stream(stream)))
 
 
 def pa_decode_cascade_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,

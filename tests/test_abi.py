@@ -108,6 +108,13 @@ def test_host_validation_without_gpu(palib):
                              64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_OK
     assert L.pa_decode_nvfp4(None, None, None, None, None, 1.0, 1.0, None, 1, None, 1, 4, 2,
                              64, 16, 8, 1.0, None, None, 0, 0, None) == palib.PA_ERR_INVALID_ARG
+    # fused NVFP4 append: the new-token buffers are required
+    assert L.pa_decode_append_nvfp4(None, None, None, None, None, None, None, None, 1.0, 1.0,
+                                    None, 1, None, 1, 4, 2, 64, 16, 8, 1.0, None, None, 0, 0,
+                                    None) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_decode_append_nvfp4(None, None, None, None, None, None, None, None, 1.0, 1.0,
+                                    None, 1, None, 0, 4, 2, 64, 16, 8, 1.0, None, None, 0, 0,
+                                    None) == palib.PA_OK
 
 
 def _compare_models(pa, seed, steps=2000, N=48, bs=4):

@@ -307,3 +307,60 @@ def test_shape_parity(name, B, hq, hkv, d, bs, lo, hi):
         out = run_decode(case, cache, k_gs, v_gs, num_splits=splits)
         assert_close(out, ref, TOL, f"nvfp4 {name} splits {splits}")
     assert pa.pa_get_device_error() == 0
+
+
+# ------------------------------------------------------ fused NVFP4 append --
+def _fp4_two_ways(case, cache0, k_gs, v_gs, slots, splits):
+    """(out, pools) of pa_cache_write_nvfp4 + pa_decode_nvfp4 and of
+    pa_decode_append_nvfp4, each on its own copy of the pools."""
+    w = case.w
+    c1 = tuple(a.clone() for a in cache0)
+    c2 = tuple(a.clone() for a in cache0)
+    n = pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads, w.num_kv_heads, w.head_dim,
+                                    splits)
+    ws = torch.full((max(n, 16),), 255, dtype=torch.uint8, device="cuda")
+    o1 = torch.full((w.num_seqs, w.num_q_heads, w.head_dim), float("nan"),
+                    dtype=torch.bfloat16, device="cuda")
+    o2 = o1.clone()
+    pa.pa_cache_write_nvfp4(case.k_new, case.v_new, slots, c1, k_gs, v_gs)
+    pa.pa_decode_nvfp4(case.q, c1, k_gs, v_gs, case.table_t, case.lens_t, w.scale, o1, ws,
+                       num_splits=splits)
+    pa.pa_decode_append_nvfp4(case.q, case.k_new, case.v_new, slots, c2, k_gs, v_gs,
+                              case.table_t, case.lens_t, w.scale, o2, ws, num_splits=splits)
+    torch.cuda.synchronize()
+    return (o1, c1), (o2, c2)
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3.2-1b", "llama3.1-8b", "shared_prefix_bs32"])
+@pytest.mark.parametrize("splits", [0, 7])
+def test_fused_append_equals_write_then_decode(name, splits):
+    case = build_case(W.WORKLOADS[name]())
+    k_gs, v_gs = 0.0029, 0.0031
+    cache0 = gpu_pool(case, k_gs, v_gs)
+    (o1, c1), (o2, c2) = _fp4_two_ways(case, cache0, k_gs, v_gs, case.slots_t, splits)
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16)), name
+    for a, b in zip(c1, c2):
+        assert torch.equal(a, b), name
+    assert pa.pa_get_device_error() == 0
+
+
+def test_fused_append_skips_and_flags_slots():
+    # slot -1: nothing appended for that sequence; a slot other than the
+    # last position's: flagged, not written; the rest as write-then-decode
+    case = build_case(W.llama32_1b(24))
+    k_gs, v_gs = 0.0029, 0.0031
+    cache0 = gpu_pool(case, k_gs, v_gs)
+    slots = case.slots_t.clone()
+    slots[3] = -1
+    good = slots.clone()
+    slots[5] = slots[5] ^ 1  # the neighbouring slot of the same block
+    good[5] = -1
+    (o1, c1), (o2, c2) = _fp4_two_ways(case, cache0, k_gs, v_gs, slots, 0)
+    err = pa.pa_get_device_error()
+    assert err & pa.DEVERR_BAD_SLOT
+    # the reference: write only the good slots, then decode
+    (r1, rc1), _ = _fp4_two_ways(case, cache0, k_gs, v_gs, good, 0)
+    pa.pa_get_device_error()
+    assert torch.equal(o2.view(torch.int16), r1.view(torch.int16))
+    for a, b in zip(c2, rc1):
+        assert torch.equal(a, b)
