@@ -1233,7 +1233,7 @@ __global__ void __launch_bounds__(32, 16)
 }
 
 // ----------------------------------------------------------------- merge --
-// Launched with one CTA per decode CTA.  Writes the sequences the decode
+// Launched with one CTA per decode CTA, G * D / 4 threads each.  Writes the sequences the decode
 // grid had no tile of (one thread per sequence): zeros for empty ones, the
 // normalised prefix partial for a cascade sequence that ends at the prefix.
 // Then CTA c merges the split segment decode CTA c finished, if any: thread

@@ -279,7 +279,7 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
                  tq, tk, tv, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
-                 dim3(kMaxG * D / 4), 0, stream, prm) != cudaSuccess)
+                 dim3(prm.group * D / 4), 0, stream, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
@@ -966,7 +966,7 @@ pa_status launch_fp4_decode(const DecodeParams& prm_in, const Fp4Args& f, void* 
                  f) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
-                 dim3(kMaxG * D / 4), 0, stream, prm) != cudaSuccess)
+                 dim3(prm.group * D / 4), 0, stream, prm) != cudaSuccess)
     return PA_ERR_CUDA;
   return PA_OK;
 }
