@@ -599,6 +599,14 @@ def oracle_sample_all_cores(name, budget_s):
     return total / max(r[2] for r in res) / 1e9, sum(r[1] for r in res), n
 
 
+def workload_config(w):
+    """The workload's identity, shared by both arms' JSON lines."""
+    return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
+            "block_size": w.block_size, "kv_bytes_per_step": kv_bytes(w),
+            "mean_seq_len": sum(w.seq_lens) / w.num_seqs}
+
+
 def run_reference(args, w):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -619,7 +627,8 @@ def run_reference(args, w):
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name}, "cpu_baseline": cpu,
+            "config": {**workload_config(w), "parallelism": "host cores (oracle)"},
+            "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -785,10 +794,7 @@ def main():
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V, Q; scattered blocks)",
             "config": {
-                "workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
-                "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
-                "block_size": w.block_size, "kv_bytes_per_step": nbytes,
-                "mean_seq_len": sum(w.seq_lens) / w.num_seqs,
+                **workload_config(w),
                 "l2": f"inputs larger than L2: {res['n_pools']} rotating layer pools of "
                       f"{res['pool_bytes'] / 1e9:.2f} GB",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
