@@ -35,6 +35,14 @@
  *   - The library allocates no device memory in any entry point except that
  *     the CUDA runtime lazily creates its context.  The only host memory it
  *     owns is the opaque pa_allocator.
+ *   - Kernels launch as programmatic dependents of the work before them in
+ *     the stream and wait for it on the device before touching its data,
+ *     with one exception: the decode kernels read seq_lens to split the work
+ *     before that wait.  No kernel of this library writes seq_lens; a kernel
+ *     of the caller's that produces seq_lens and lets dependents start early
+ *     (griddepcontrol.launch_dependents) must not directly precede a decode
+ *     call.  Ordinary stream order (copies, kernels without that trigger)
+ *     needs nothing.
  *   - Layouts are dense, row-major (last index fastest):
  *       k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
  *                          bf16 (PA_KV_BF16) or E4M3 bytes (PA_KV_FP8_E4M3)

@@ -1132,17 +1132,31 @@ __device__ __forceinline__ bool carve(const DecodeParams& p, uint8_t* smem_raw, 
 // This CTA's range [lo, hi) of the flat tile list (W tiles over P
 // participating CTAs); false if it has none.  With fewer tiles than CTAs
 // only the first W CTAs take part, so that every participating CTA owns at
-// least one tile.  The math warp's lane 0 first clears the CTA's merge job.
+// least one tile.  Reads only seq_lens.
 __device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& W, int32_t& P,
                                          int64_t& lo, int64_t& hi) {
-  if (p.ws_job != nullptr && threadIdx.x == blockDim.x - 32)
-    p.ws_job[blockIdx.x] = make_int2(-1, -1);
   W = total_tiles(p);
   if (W == 0) return false;
   P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
   if (static_cast<int32_t>(blockIdx.x) >= P) return false;
   cta_range(W, P, blockIdx.x, lo, hi);
   return true;
+}
+
+// The CTA's work split, before the programmatic-dependency wait: it reads
+// only seq_lens (and the loader's first segment), which no kernel of this
+// library writes, so it overlaps the tail of the grid before.  After the
+// wait the math warp's lane 0 clears the CTA's merge job (the previous
+// merge grid may still read the job words until then).
+__device__ __forceinline__ bool split_then_wait(const DecodeParams& p, int64_t& W, int32_t& P,
+                                                int64_t& lo, int64_t& hi, Loader& ld) {
+  const bool mine = my_range(p, W, P, lo, hi);
+  if (mine) loader_init(p, lo, hi, ld);
+  pdl_wait();
+  pdl_trigger();
+  if (p.ws_job != nullptr && threadIdx.x == blockDim.x - 32)
+    p.ws_job[blockIdx.x] = make_int2(-1, -1);
+  return mine;
 }
 
 // Two warps: warp 0 copies, warp 1 computes.
@@ -1171,15 +1185,12 @@ __global__ void __launch_bounds__(64, 8)
     tma_prefetch_desc(&tm_v);
   }
   __syncthreads();
-  // Launched as a programmatic dependent: nothing above reads an input;
-  // wait for the previous grid before anything below does.
-  pdl_wait();
-  pdl_trigger();
+  // Launched as a programmatic dependent: only the work split runs before
+  // the wait for the previous grid.
   int64_t W, lo, hi;
   int32_t P;
-  if (!my_range(p, W, P, lo, hi)) return;
   Loader ld;
-  loader_init(p, lo, hi, ld);
+  if (!split_then_wait(p, W, P, lo, hi, ld)) return;
   if (threadIdx.x < 32) {
     produce<D, FP8>(p, tm, sb, ld, hi);
   } else {
@@ -1211,13 +1222,10 @@ __global__ void __launch_bounds__(32, 16)
     tma_prefetch_desc(&tm_v);
   }
   __syncwarp();
-  pdl_wait();  // as in the two-warp kernel
-  pdl_trigger();
-  int64_t W, lo, hi;
+  int64_t W, lo, hi;  // as in the two-warp kernel
   int32_t P;
-  if (!my_range(p, W, P, lo, hi)) return;
   Loader ld;
-  loader_init(p, lo, hi, ld);
+  if (!split_then_wait(p, W, P, lo, hi, ld)) return;
   uint32_t used, qread;
   run_math<D, FP8, true, kAppend || !FP8>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used,
                                            qread);

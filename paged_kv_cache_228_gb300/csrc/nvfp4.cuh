@@ -525,13 +525,17 @@ __global__ void __launch_bounds__(32, 16)
   extern __shared__ __align__(128) uint8_t fp4_smem[];
   const uint32_t ring = smem_addr(fp4_smem);
   const int lane = threadIdx.x & 31;
-  pdl_wait();  // launched as a programmatic dependent: inputs are ready
-  pdl_trigger();
+  // the work split reads only seq_lens: before the programmatic-dependency
+  // wait (as in the other decode kernels); the merge job after it
   int64_t W, lo, hi;
   int32_t P;
-  if (!my_range(p, W, P, lo, hi)) return;
+  const bool mine = my_range(p, W, P, lo, hi);
   Cursor c;
-  locate(p, lo, c);
+  if (mine) locate(p, lo, c);
+  pdl_wait();
+  pdl_trigger();
+  if (p.ws_job != nullptr && lane == 0) p.ws_job[blockIdx.x] = make_int2(-1, -1);
+  if (!mine) return;
   // load side: cursor lc at flat index lu, its block id prefetched
   Cursor lc = c;
   int64_t lu = lo;
