@@ -7,6 +7,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -23,6 +25,15 @@ namespace pa {
 namespace {
 
 constexpr int kMaxDevices = 64;
+
+// An NVTX range named after the entry point around its host work and
+// launches (a profiler shows it; without one it costs a no-op call).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 inline bool aligned16(const void* p) {
   return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
@@ -318,6 +329,7 @@ extern "C" pa_status pa_cache_write(const void* k_new, const void* v_new,
                                     void* k_cache, void* v_cache, int32_t num_blocks,
                                     int32_t num_kv_heads, int32_t block_size,
                                     int32_t head_dim, pa_kv_dtype kv_dtype, void* stream) {
+  const NvtxRange nvtx_range("pa_cache_write");
   if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 ||
       head_dim <= 0 || head_dim % 8 != 0)
     return PA_ERR_INVALID_ARG;
@@ -350,6 +362,7 @@ extern "C" pa_status pa_cache_write_fp8(const void* k_new, const void* v_new,
                                         float* v_scale, int32_t num_blocks,
                                         int32_t num_kv_heads, int32_t block_size,
                                         int32_t head_dim, void* stream) {
+  const NvtxRange nvtx_range("pa_cache_write_fp8");
   if (num_tokens < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0)
     return PA_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return PA_ERR_UNSUPPORTED;
@@ -386,6 +399,7 @@ extern "C" pa_status pa_copy_blocks(void* k_cache, void* v_cache, float* k_scale
                                     int32_t num_blocks, int32_t num_kv_heads,
                                     int32_t block_size, int32_t head_dim,
                                     pa_kv_dtype kv_dtype, void* stream) {
+  const NvtxRange nvtx_range("pa_copy_blocks");
   if (num_pairs < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 || head_dim <= 0)
     return PA_ERR_INVALID_ARG;
   int esz;
@@ -480,6 +494,7 @@ extern "C" pa_status pa_swap_out(const void* k_cache, const void* v_cache, const
                                  float* host_v_scale, int32_t num_blocks, int32_t num_kv_heads,
                                  int32_t block_size, int32_t head_dim, pa_kv_dtype kv_dtype,
                                  void* stream) {
+  const NvtxRange nvtx_range("pa_swap_out");
   return swap_blocks(const_cast<void*>(k_cache), const_cast<void*>(v_cache),
                      const_cast<float*>(k_scale), const_cast<float*>(v_scale), block_ids,
                      num_ids, host_k, host_v, host_k_scale, host_v_scale, num_blocks,
@@ -492,6 +507,7 @@ extern "C" pa_status pa_swap_in(const void* host_k, const void* host_v,
                                 void* v_cache, float* k_scale, float* v_scale,
                                 int32_t num_blocks, int32_t num_kv_heads, int32_t block_size,
                                 int32_t head_dim, pa_kv_dtype kv_dtype, void* stream) {
+  const NvtxRange nvtx_range("pa_swap_in");
   return swap_blocks(k_cache, v_cache, k_scale, v_scale, block_ids, num_ids,
                      const_cast<void*>(host_k), const_cast<void*>(host_v),
                      const_cast<float*>(host_k_scale), const_cast<float*>(host_v_scale),
@@ -504,6 +520,7 @@ extern "C" pa_status pa_quantize_fp8(const void* k_src, const void* v_src,
                                      float* k_scale, float* v_scale, int32_t num_blocks,
                                      int32_t num_kv_heads, int32_t block_size,
                                      int32_t head_dim, void* stream) {
+  const NvtxRange nvtx_range("pa_quantize_fp8");
   if (num_ids < 0 || num_blocks < 0 || num_kv_heads <= 0 || block_size <= 0 ||
       head_dim <= 0 || head_dim % 16 != 0)
     return PA_ERR_INVALID_ARG;
@@ -739,6 +756,7 @@ extern "C" pa_status pa_decode(const void* q, const void* k_cache, const void* v
                                int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                float scale, void* out, void* workspace,
                                size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode");
   return decode_entry(q, k_cache, v_cache, k_scale, v_scale, kv_dtype, block_tables,
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                       head_dim, block_size, num_blocks, scale, out, workspace, workspace_bytes,
@@ -755,6 +773,7 @@ extern "C" pa_status pa_decode_append_fp8(const void* q, const void* k_new, cons
                                           int32_t num_blocks, float scale, void* out,
                                           void* workspace, size_t workspace_bytes,
                                           int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_append_fp8");
   const AppendArgs app{k_new, v_new, slot_mapping};
   return decode_entry(q, k_cache, v_cache, k_scale, v_scale, PA_KV_FP8_E4M3, block_tables,
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
@@ -770,6 +789,7 @@ extern "C" pa_status pa_decode_append(const void* q, const void* k_new, const vo
                                       int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                       float scale, void* out, void* workspace,
                                       size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_append");
   const AppendArgs app{k_new, v_new, slot_mapping};
   return decode_entry(q, k_cache, v_cache, nullptr, nullptr, PA_KV_BF16, block_tables,
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
@@ -809,6 +829,7 @@ extern "C" pa_status pa_decode_cascade(const void* q, const void* k_cache, const
                                        int32_t prefix_len, float scale, void* out,
                                        void* workspace, size_t workspace_bytes,
                                        int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_cascade");
   if (prefix_len < 0 || num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
       block_size <= 0 || max_blocks_per_seq < 0 || num_q_heads % num_kv_heads != 0)
     return PA_ERR_INVALID_ARG;
@@ -911,6 +932,7 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_cache, const
                                        int32_t num_kv_heads, int32_t head_dim,
                                        int32_t block_size, int32_t num_blocks, float scale,
                                        void* out, int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_noalloc");
   void* scratch = nullptr;
   const pa_status st = pa::noalloc_scratch(&scratch);
   if (st != PA_OK) return st;
@@ -980,6 +1002,7 @@ extern "C" pa_status pa_cache_write_nvfp4(const void* k_new, const void* v_new,
                                           float k_gscale, float v_gscale, int32_t num_blocks,
                                           int32_t num_kv_heads, int32_t block_size,
                                           int32_t head_dim, void* stream) {
+  const NvtxRange nvtx_range("pa_cache_write_nvfp4");
   if (num_tokens < 0 || num_blocks <= 0 || num_kv_heads <= 0 || !finite_pos(k_gscale) ||
       !finite_pos(v_gscale))
     return PA_ERR_INVALID_ARG;
@@ -1092,6 +1115,7 @@ extern "C" pa_status pa_decode_nvfp4(const void* q, const void* k_cache, const v
                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                      float scale, void* out, void* workspace,
                                      size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_nvfp4");
   return fp4_decode_entry(q, k_cache, v_cache, k_sf, v_sf, k_gscale, v_gscale, block_tables,
                           max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
                           head_dim, block_size, num_blocks, scale, out, workspace,
@@ -1105,6 +1129,7 @@ extern "C" pa_status pa_decode_append_nvfp4(
     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
     int32_t block_size, int32_t num_blocks, float scale, void* out, void* workspace,
     size_t workspace_bytes, int32_t num_splits, void* stream) {
+  const NvtxRange nvtx_range("pa_decode_append_nvfp4");
   const AppendArgs app{k_new, v_new, slot_mapping};
   return fp4_decode_entry(q, k_cache, v_cache, k_sf, v_sf, k_gscale, v_gscale, block_tables,
                           max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,
