@@ -15,7 +15,10 @@ against the oracle's NVFP4 restatement, through the C ABI.
 * empty and ragged sequences, every work-partition count within tolerance and
   repeated calls bit-identical, out-of-pool table entries and slots flagged;
 * shapes beyond the workloads: MQA over 300 sequences, MHA at block size 256,
-  a group of 3, one 256K-token sequence split across every CTA.
+  a group of 3, one 256K-token sequence split across every CTA, and 2048
+  sequences of 1..70 tokens;
+* the fused append (pa_decode_append_nvfp4) equals write then decode bit for
+  bit, and skips or flags slots as pa_decode_append does.
 """
 import numpy as np
 import pytest
@@ -364,3 +367,19 @@ def test_fused_append_skips_and_flags_slots():
     assert torch.equal(o2.view(torch.int16), r1.view(torch.int16))
     for a, b in zip(c2, rc1):
         assert torch.equal(a, b)
+
+
+def test_many_short_sequences():
+    # 2048 sequences of 1..70 tokens: dozens of whole segments per CTA
+    B = 2048
+    case = build_case(_workload("short", B, 16, 4, 128, 16, _lens(B, 1, 70, 11), 25))
+    seqs = list(range(0, B, 41))
+    snap = snapshot_blocks(case, seqs)
+    k_gs, v_gs = gscales(snap)
+    cache = gpu_pool(case, k_gs, v_gs)
+    ocache = oracle_pool(snap, k_gs, v_gs)
+    assert_pool_equal(cache, ocache, snap[0][:128])
+    poison_unused(cache, case)
+    out = run_decode(case, cache, k_gs, v_gs)
+    assert_close(out, oracle_out(case, snap, ocache, k_gs, v_gs, seqs), TOL, "nvfp4 short")
+    assert pa.pa_get_device_error() == 0

@@ -6,7 +6,9 @@ against the fp64 oracle (bf16 1e-2, FP8 5e-2):
 * MHA: group 1, block size 256 (the largest), d = 64;
 * a group of 3 (not a power of two), block size 8;
 * one 256K-token sequence on one KV head, split across every CTA (sampled
-  heads checked), bf16 and FP8.
+  heads checked), bf16 and FP8;
+* 2048 sequences of 1..70 tokens (dozens of whole segments per CTA, query
+  slots reused many times, 16 passes of the length scan), bf16 and FP8.
 """
 import math
 
@@ -109,4 +111,34 @@ def test_one_256k_sequence_bf16_and_fp8():
                  k_scale=ks, v_scale=vs)
     torch.cuda.synchronize()
     assert_close(out8, ref, 5e-2, "256K fp8")
+    assert pa.pa_get_device_error() == 0
+
+
+def test_many_short_sequences_bf16_fp8():
+    # 2048 sequences of 1..70 tokens: every CTA walks dozens of whole
+    # segments (query-slot reuse, segment hand-over in the copy warp), and
+    # the length scan takes 16 passes of 128.
+    B = 2048
+    w = _workload("short", B, 16, 4, 128, 16, _lens(B, 1, 70, 11), 25)
+    case = build_case(w, poison_unused=True)
+    seqs = list(range(0, B, 41))
+    snap = snapshot_blocks(case, seqs)
+    out = _run(case)
+    assert_close(out, oracle_decode(case, snap, seqs), 1e-2, "short bf16")
+    assert pa.pa_get_device_error() == 0
+    ref, (blocks, vl, ids) = oracle_decode_fp8(case, snapshot_blocks(case, seqs), seqs)
+    phys = torch.tensor([ids[b] for b in blocks], dtype=torch.int32, device="cuda")
+    kq = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device="cuda")
+    vq = torch.zeros_like(kq)
+    ks = torch.ones((w.pool_blocks, w.num_kv_heads), device="cuda")
+    vs = torch.ones_like(ks)
+    pa.pa_quantize_fp8(case.k_cache, case.v_cache, phys,
+                       torch.tensor(vl, dtype=torch.int32, device="cuda"), kq, vq, ks, vs)
+    out8 = torch.full_like(out, float("nan"))
+    nws = pa.pa_decode_workspace_size(B, 16, 4, 128)
+    ws = torch.full((max(16, nws),), 255, dtype=torch.uint8, device="cuda")
+    pa.pa_decode(case.q, kq, vq, case.table_t, case.lens_t, w.scale, out8, ws,
+                 k_scale=ks, v_scale=vs)
+    torch.cuda.synchronize()
+    assert_close(out8, ref, 5e-2, "short fp8")
     assert pa.pa_get_device_error() == 0
