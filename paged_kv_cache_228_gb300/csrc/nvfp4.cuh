@@ -26,7 +26,8 @@
 // 16-token tiles over persistent CTAs, log-sum-exp merge).  A tile's bytes
 // go to shared memory with per-lane cp.async into a ring of kStages stages
 // (each lane copies what it will read itself; the scale bytes are copied
-// by 16 lanes and read after a warp barrier).  Math on the f16 tensor-core
+// by D/8 lanes and read after a warp barrier), two tiles per loop step
+// while two remain.  Math on the f16 tensor-core
 // MMA, fp32 accumulate, in the same fragment layout as the other kernels
 // (tokens on M, the query heads of the group on N):
 //   S^T = K' . Q^T with K' = e2m1 * e4m3 block scale, formed exactly in f16
@@ -37,7 +38,9 @@
 //   O^T += V'^T . P^T with V' from the pair-rows, again exact in f16; lane gq
 //         owns d in [(D/8) gq, (D/8)(gq + 1)) of every m-tile, one group.
 // The tensor scales fold in after the MMA: S_k into the score multiplier,
-// S_v into the final normalisation.
+// S_v into the final normalisation.  A second instantiation fuses the
+// step's append: the warp that copies a segment's last tile first writes
+// that head's new rows into it (fp4_append_new).
 #pragma once
 
 #include "decode.cuh"
