@@ -306,3 +306,16 @@ def test_workspace_too_small_is_rejected():
         pa.pa_decode(case.q, case.k_cache, case.v_cache, case.table_t, case.lens_t, w.scale,
                      out, torch.empty(16, dtype=torch.uint8, device="cuda"), num_splits=4)
     assert e.value.status == pa.PA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("splits", [1, 5, 37, 2000])
+def test_more_partitions_than_tiles(splits):
+    # The tiny batch has 2 * (1 + 2 + 3 + 4) = 20 tiles: with more partitions
+    # than tiles only the first W CTAs take part, one tile each, and nearly
+    # every segment goes through the merge.
+    case = build_case(W.tiny(), poison_unused=True)
+    seqs = range(case.w.num_seqs)
+    snap = snapshot_blocks(case, seqs)
+    out = run_step(case, num_splits=splits)
+    assert_close(out, oracle_decode(case, snap, seqs), TOL_BF16, f"tiny splits={splits}")
+    assert pa.pa_get_device_error() == 0

@@ -383,3 +383,18 @@ def test_many_short_sequences():
     out = run_decode(case, cache, k_gs, v_gs)
     assert_close(out, oracle_out(case, snap, ocache, k_gs, v_gs, seqs), TOL, "nvfp4 short")
     assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("splits", [1, 5, 37, 2000])
+def test_more_partitions_than_tiles(splits):
+    case = build_case(W.tiny())
+    seqs = list(range(case.w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
+    k_gs, v_gs = gscales(snap)
+    cache = gpu_pool(case, k_gs, v_gs)
+    ocache = oracle_pool(snap, k_gs, v_gs)
+    poison_unused(cache, case)
+    out = run_decode(case, cache, k_gs, v_gs, num_splits=splits)
+    assert_close(out, oracle_out(case, snap, ocache, k_gs, v_gs, seqs), TOL,
+                 f"nvfp4 tiny splits={splits}")
+    assert pa.pa_get_device_error() == 0
