@@ -13,9 +13,11 @@
 // ------------
 // * Work unit: a 16-token tile of one (sequence b, KV head g) "segment".
 //   All tiles of all segments form one flat list of W tiles, ordered
-//   (b, g, tile); persistent CTA c of P owns tiles [W*c/P, W*(c+1)/P).  This
-//   balances ragged lengths to within one tile per CTA and splits long
-//   contexts into at most P pieces in total (split-K).  A piece that covers
+//   (b, g, tile), and each persistent CTA of P owns a contiguous run of it.
+//   The runs balance cost, not tiles: a segment costs its tiles plus a
+//   fixed charge for its query copy, first table batch and finish, so a
+//   CTA that meets many short segments takes fewer tiles.  Long contexts
+//   split into at most P pieces in total (split-K).  A piece that covers
 //   a whole segment writes the output directly; otherwise it writes an
 //   unnormalised partial (o, m, l) that the merge kernel combines by
 //   log-sum-exp.  Split points depend only on seq_lens, so the output does
@@ -81,6 +83,7 @@ struct DecodeParams {
   int32_t rows_total;  // num_blocks * num_kv_heads * block_size
   float scale_log2;    // softmax scale * log2(e)
   int32_t num_ctas;    // P
+  int32_t seg_cost;    // work split: units charged per segment (a tile is kUnit)
   int32_t stages;      // ring depth
 };
 
@@ -139,51 +142,6 @@ struct Cursor {
   int32_t b, g, tile, T, n;
 };
 
-// Warp-collective: find the segment holding flat tile u (< W).  The
-// lengths of 128 sequences are loaded at once.
-__device__ __forceinline__ void locate(const DecodeParams& p, int64_t u,
-                                       Cursor& c) {
-  const int lane = threadIdx.x & 31;
-  int64_t base = 0;
-  for (int32_t b00 = 0; b00 < p.num_seqs; b00 += 128) {
-    int32_t nk[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int32_t b = b00 + 32 * k + lane;
-      nk[k] = b < p.num_seqs ? clamp_len(p, p.seq_lens[b]) : 0;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int32_t b0 = b00 + 32 * k;
-      const int32_t n = nk[k];
-      const int64_t w = static_cast<int64_t>(p.num_kv_heads) * seg_tiles(p, n);
-      int64_t incl = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int64_t t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      const int64_t total = __shfl_sync(0xffffffffu, incl, 31);
-      if (base + total > u) {
-        const unsigned m = __ballot_sync(0xffffffffu, base + incl > u);
-        const int L = __ffs(m) - 1;
-        const int64_t excl = __shfl_sync(0xffffffffu, incl - w, L);
-        const int32_t nn = __shfl_sync(0xffffffffu, n, L);
-        const int64_t rem = u - (base + excl);
-        c.b = b0 + L;
-        c.n = nn;
-        c.T = seg_tiles(p, nn);
-        c.g = static_cast<int32_t>(rem / c.T);
-        c.tile = static_cast<int32_t>(rem % c.T);
-        return;
-      }
-      base += total;
-    }
-  }
-  c.b = p.num_seqs;  // unreachable for u < W
-  c.g = c.tile = c.T = c.n = 0;
-}
-
 // Move to the first tile of the next non-empty segment.
 __device__ __forceinline__ void next_segment(const DecodeParams& p, Cursor& c) {
   c.tile = 0;
@@ -196,28 +154,153 @@ __device__ __forceinline__ void next_segment(const DecodeParams& p, Cursor& c) {
   } while (c.T == 0);
 }
 
-// Flat-list range of CTA c of P (P <= W, so every range is non-empty).
-__device__ __forceinline__ void cta_range(int64_t W, int32_t P, int32_t c,
-                                          int64_t& lo, int64_t& hi) {
-  lo = W * c / P;
-  hi = W * (c + 1) / P;
+// The cost-weighted split.  A tile costs kUnit units and every segment
+// (b, g) seg_cost more, charged just before its first tile: the query
+// copy, the first table batch and the finish are paid once per segment.
+// So tile t of segment s = b*Hkv + g has its first unit at
+//   kUnit * (flat index of the tile) + seg_cost * (s + 1),
+// and the list holds U = kUnit * W + seg_cost * B * Hkv units.  CTA c of P
+// takes the units [U*c/P, U*(c+1)/P) and with them the tiles whose first
+// unit lies there, a contiguous run [lo, hi) of the flat list.  With
+// P <= W every range spans at least kUnit units, so a CTA strictly inside
+// a split segment always holds some of its tiles; a range that falls in
+// the units charged between two segments holds none.
+constexpr int kUnit = 8;
+
+// a / b for non-negative a, b > 0, in 32 bits when both fit.
+__device__ __forceinline__ int64_t div_nn(int64_t a, int64_t b) {
+  if (((a | b) >> 31) == 0)
+    return static_cast<uint32_t>(a) / static_cast<uint32_t>(b);
+  return a / b;
 }
 
-// Index of the CTA whose range holds flat tile u.
-__device__ __forceinline__ int32_t cta_of(int64_t W, int32_t P, int64_t u) {
-  return static_cast<int32_t>(((u + 1) * P - 1) / W);
+// a * c / P for a >= 0 and 0 <= c <= P (no 64-bit division when a fits in
+// 31 bits and P is small): a = qP + r, so a*c/P = q*c + r*c/P.
+__device__ __forceinline__ int64_t mul_div(int64_t a, int32_t c, int32_t P) {
+  if ((a >> 31) == 0 && P <= 46340) {
+    const uint32_t u = static_cast<uint32_t>(a), pp = static_cast<uint32_t>(P),
+                   cc = static_cast<uint32_t>(c);
+    return static_cast<int64_t>(u / pp) * cc + (u % pp) * cc / pp;
+  }
+  return a * c / P;
 }
 
-// Warp-collective total tile count W.
-__device__ __forceinline__ int64_t total_tiles(const DecodeParams& p) {
+// Warp-collective: 128 sequences from b00, lane l holding b00 + 4l + k.
+struct Chunk {
+  int32_t n[4];  // clamped lengths (0 past the batch)
+  int64_t excl;  // tiles (all heads) of the chunk's sequences before this lane's
+  int64_t sum;   // tiles of this lane's four
+  int64_t total; // tiles of the chunk
+};
+
+__device__ __forceinline__ void load_chunk(const DecodeParams& p, int32_t b00, Chunk& ch) {
   const int lane = threadIdx.x & 31;
-  int64_t w = 0;
-#pragma unroll 4
-  for (int32_t b = lane; b < p.num_seqs; b += 32)
-    w += seg_tiles(p, clamp_len(p, p.seq_lens[b]));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
-  return w * p.num_kv_heads;
+  for (int k = 0; k < 4; ++k) {
+    const int32_t b = b00 + 4 * lane + k;
+    ch.n[k] = b < p.num_seqs ? clamp_len(p, p.seq_lens[b]) : 0;
+  }
+  int64_t s = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) s += seg_tiles(p, ch.n[k]);
+  s *= p.num_kv_heads;
+  int64_t incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if ((threadIdx.x & 31) >= o) incl += y;
+  }
+  ch.sum = s;
+  ch.excl = incl - s;
+  ch.total = __shfl_sync(0xffffffffu, incl, 31);
+}
+
+// Warp-collective: if unit x lies in chunk ch (base = tiles before it),
+// the number of tiles whose first unit is below x, and, if want, the
+// segment cursor there (before any move past a segment's end).
+__device__ __forceinline__ bool find_in_chunk(const DecodeParams& p, const Chunk& ch,
+                                              int32_t b00, int64_t base, int64_t x,
+                                              int64_t& t, Cursor* c) {
+  const int lane = threadIdx.x & 31;
+  const int64_t A = p.seg_cost;
+  const int32_t H = p.num_kv_heads;
+  const int32_t b0 = b00 + 4 * lane;
+  const int32_t nthrough = min(b0 + 4, p.num_seqs);  // sequences through this lane's
+  const int64_t uthrough = kUnit * (base + ch.excl + ch.sum) + A * H * nthrough;
+  const unsigned m = __ballot_sync(0xffffffffu, b0 < p.num_seqs && uthrough > x);
+  if (m == 0u) return false;
+  const int L = __ffs(m) - 1;
+  int64_t before = base + __shfl_sync(0xffffffffu, ch.excl, L);
+  int32_t n[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) n[k] = __shfl_sync(0xffffffffu, ch.n[k], L);
+  int32_t b = b00 + 4 * L;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int32_t T = seg_tiles(p, n[k]);
+    const int64_t seg = kUnit * static_cast<int64_t>(T) + A;  // units of one head
+    const int64_t rem = x - (kUnit * before + A * H * b);
+    if (k == 3 || rem < seg * H) {
+      const int64_t g = div_nn(rem, seg);
+      const int64_t r = rem - g * seg;
+      const int64_t j = r <= A ? 0 : (r - A + kUnit - 1) / kUnit;
+      t = before + g * T + j;
+      if (c != nullptr) {
+        c->b = b;
+        c->n = n[k];
+        c->T = T;
+        c->g = T == 0 ? H - 1 : static_cast<int32_t>(g);  // an empty sequence: past its last head
+        c->tile = T == 0 ? 0 : static_cast<int32_t>(j);
+      }
+      return true;
+    }
+    before += static_cast<int64_t>(H) * T;
+    ++b;
+  }
+  return true;  // not reached
+}
+
+// This CTA's range [lo, hi) of the flat tile list and the cursor at lo
+// (U units over P participating CTAs); false if it holds no tile.  With
+// fewer tiles than CTAs only the first W CTAs take part.  Reads only
+// seq_lens: once for up to 128 sequences.
+__device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& U, int32_t& P,
+                                         int64_t& lo, int64_t& hi, Cursor& c) {
+  Chunk ch;
+  load_chunk(p, 0, ch);
+  int64_t W = ch.total;
+  for (int32_t b00 = 128; b00 < p.num_seqs; b00 += 128) {
+    Chunk more;
+    load_chunk(p, b00, more);
+    W += more.total;
+  }
+  if (W == 0) return false;
+  U = kUnit * W + static_cast<int64_t>(p.seg_cost) * p.num_kv_heads * p.num_seqs;
+  P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
+  const int32_t cta = static_cast<int32_t>(blockIdx.x);
+  if (cta >= P) return false;
+  const int64_t x0 = mul_div(U, cta, P), x1 = mul_div(U, cta + 1, P);
+  bool f0 = false, f1 = false;
+  lo = hi = W;  // a bound past every sequence's units
+  int64_t base = 0;
+  for (int32_t b00 = 0; b00 < p.num_seqs && !(f0 && f1); b00 += 128) {
+    if (b00 > 0) load_chunk(p, b00, ch);
+    if (!f0) f0 = find_in_chunk(p, ch, b00, base, x0, lo, &c);
+    if (!f1) f1 = find_in_chunk(p, ch, b00, base, x1, hi, nullptr);
+    base += ch.total;
+  }
+  if (lo >= hi) return false;
+  // a bound at a segment's end (or in an empty sequence) opens the next one
+  if (c.T == 0 || c.tile == c.T) next_segment(p, c);
+  return true;
+}
+
+// Index of the CTA holding the first tile of segment (b, g), flat tile f.
+__device__ __forceinline__ int32_t first_cta(const DecodeParams& p, int64_t U, int32_t P,
+                                             int64_t f, int32_t b, int32_t g) {
+  const int64_t F = kUnit * f + static_cast<int64_t>(p.seg_cost) *
+                                    (static_cast<int64_t>(b) * p.num_kv_heads + g + 1);
+  return static_cast<int32_t>(((F + 1) * P - 1) / U);
 }
 
 // ---------------------------------------------------------- issue side ---
@@ -559,10 +642,10 @@ __device__ __forceinline__ void issue_tile(const DecodeParams& p, const Maps& tm
   }
 }
 
-// Warp-collective: the loader at flat tile lo of a CTA owning [lo, hi).
-__device__ __forceinline__ void loader_init(const DecodeParams& p, int64_t lo, int64_t hi,
+// The loader at flat tile lo (cursor c) of a CTA owning [lo, hi).
+__device__ __forceinline__ void loader_init(int64_t lo, int64_t hi, const Cursor& c,
                                             Loader& ld) {
-  locate(p, lo, ld.c);
+  ld.c = c;
   ld.u = lo;
   ld.seg_end = static_cast<int32_t>(min(static_cast<int64_t>(ld.c.T), ld.c.tile + (hi - lo)));
   ld.tb = -1;
@@ -1027,7 +1110,7 @@ __device__ __forceinline__ void finish_piece(const DecodeParams& p, SegState<D>&
 // query slots consumed.
 template <int D, bool FP8, bool kFused, bool kAppend = true>
 __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, const Bufs& sb,
-                                         Loader& ld, Cursor c, int64_t W, int32_t P,
+                                         Loader& ld, Cursor c, int64_t U, int32_t P,
                                          int64_t lo, int64_t hi, int32_t cta, uint32_t& used,
                                          uint32_t& qread) {
   using L = Smem<D, FP8>;
@@ -1096,7 +1179,8 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
     // kernel's CTA of the same index (at most one per CTA: only the first
     // segment of a range can have started in an earlier CTA).
     if (!whole && seg_end == c.T && lane == 0)
-      p.ws_job[cta] = make_int2(c.b * p.num_kv_heads + c.g, cta_of(W, P, u - c.tile));
+      p.ws_job[cta] =
+          make_int2(c.b * p.num_kv_heads + c.g, first_cta(p, U, P, u - c.tile, c.b, c.g));
     u += seg_end - c.tile;
     if (u < hi) next_segment(p, c);
   }
@@ -1129,29 +1213,16 @@ __device__ __forceinline__ bool carve(const DecodeParams& p, uint8_t* smem_raw, 
   return true;
 }
 
-// This CTA's range [lo, hi) of the flat tile list (W tiles over P
-// participating CTAs); false if it has none.  With fewer tiles than CTAs
-// only the first W CTAs take part, so that every participating CTA owns at
-// least one tile.  Reads only seq_lens.
-__device__ __forceinline__ bool my_range(const DecodeParams& p, int64_t& W, int32_t& P,
-                                         int64_t& lo, int64_t& hi) {
-  W = total_tiles(p);
-  if (W == 0) return false;
-  P = static_cast<int32_t>(min(static_cast<int64_t>(p.num_ctas), W));
-  if (static_cast<int32_t>(blockIdx.x) >= P) return false;
-  cta_range(W, P, blockIdx.x, lo, hi);
-  return true;
-}
-
 // The CTA's work split, before the programmatic-dependency wait: it reads
-// only seq_lens (and the loader's first segment), which no kernel of this
-// library writes, so it overlaps the tail of the grid before.  After the
-// wait the math warp's lane 0 clears the CTA's merge job (the previous
-// merge grid may still read the job words until then).
-__device__ __forceinline__ bool split_then_wait(const DecodeParams& p, int64_t& W, int32_t& P,
+// only seq_lens, which no kernel of this library writes, so it overlaps
+// the tail of the grid before.  After the wait the math warp's lane 0
+// clears the CTA's merge job (the previous merge grid may still read the
+// job words until then).
+__device__ __forceinline__ bool split_then_wait(const DecodeParams& p, int64_t& U, int32_t& P,
                                                 int64_t& lo, int64_t& hi, Loader& ld) {
-  const bool mine = my_range(p, W, P, lo, hi);
-  if (mine) loader_init(p, lo, hi, ld);
+  Cursor c;
+  const bool mine = my_range(p, U, P, lo, hi, c);
+  if (mine) loader_init(lo, hi, c, ld);
   pdl_wait();
   pdl_trigger();
   if (p.ws_job != nullptr && threadIdx.x == blockDim.x - 32)
@@ -1187,15 +1258,15 @@ __global__ void __launch_bounds__(64, 8)
   __syncthreads();
   // Launched as a programmatic dependent: only the work split runs before
   // the wait for the previous grid.
-  int64_t W, lo, hi;
+  int64_t U, lo, hi;
   int32_t P;
   Loader ld;
-  if (!split_then_wait(p, W, P, lo, hi, ld)) return;
+  if (!split_then_wait(p, U, P, lo, hi, ld)) return;
   if (threadIdx.x < 32) {
     produce<D, FP8>(p, tm, sb, ld, hi);
   } else {
     uint32_t used, qread;
-    run_math<D, FP8, false>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used, qread);
+    run_math<D, FP8, false>(p, tm, sb, ld, ld.c, U, P, lo, hi, blockIdx.x, used, qread);
   }
 }
 
@@ -1222,12 +1293,12 @@ __global__ void __launch_bounds__(32, 16)
     tma_prefetch_desc(&tm_v);
   }
   __syncwarp();
-  int64_t W, lo, hi;  // as in the two-warp kernel
+  int64_t U, lo, hi;  // as in the two-warp kernel
   int32_t P;
   Loader ld;
-  if (!split_then_wait(p, W, P, lo, hi, ld)) return;
+  if (!split_then_wait(p, U, P, lo, hi, ld)) return;
   uint32_t used, qread;
-  run_math<D, FP8, true, kAppend || !FP8>(p, tm, sb, ld, ld.c, W, P, lo, hi, blockIdx.x, used,
+  run_math<D, FP8, true, kAppend || !FP8>(p, tm, sb, ld, ld.c, U, P, lo, hi, blockIdx.x, used,
                                            qread);
   // No copy may still target shared memory when the CTA exits.  On the
   // normal path every issued copy has been waited for already.

@@ -207,6 +207,14 @@ pa_status fp4_plan(int dev, int* ctas_per_sm) {
   return PA_OK;
 }
 
+// What the work split charges per (sequence, KV head) segment, in units
+// of kUnit = 8 per tile: the segment's query copy, first table batch and
+// finish.  Two tiles' worth was the best of 8..24 on every kernel shape
+// on the Llama-3.1-8B-shaped layer (~837 tokens a sequence).
+constexpr int32_t kSegCostBf16 = 16;
+constexpr int32_t kSegCostFp8 = 16;
+constexpr int32_t kSegCostFp4 = 16;
+
 // Workspace for P decode CTAs over `segs` segments: P + segs partial
 // slots (a CTA's pieces never collide: piece = cta + segment), then P
 // merge jobs.
@@ -237,6 +245,7 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
 
   DecodeParams prm = prm_in;
   prm.num_ctas = P;
+  prm.seg_cost = FP8 ? kSegCostFp8 : kSegCostBf16;
   prm.stages = stages;
   prm.ws_o = nullptr;
   prm.ws_ml = nullptr;
@@ -970,6 +979,7 @@ pa_status launch_fp4_decode(const DecodeParams& prm_in, const Fp4Args& f, void* 
     return PA_ERR_WORKSPACE;
   DecodeParams prm = prm_in;
   prm.num_ctas = P;
+  prm.seg_cost = kSegCostFp4;
   prm.ws_o = nullptr;
   prm.ws_ml = nullptr;
   prm.ws_job = nullptr;

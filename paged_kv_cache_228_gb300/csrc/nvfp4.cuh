@@ -530,11 +530,10 @@ __global__ void __launch_bounds__(32, 16)
   const int lane = threadIdx.x & 31;
   // the work split reads only seq_lens: before the programmatic-dependency
   // wait (as in the other decode kernels); the merge job after it
-  int64_t W, lo, hi;
+  int64_t U, lo, hi;
   int32_t P;
-  const bool mine = my_range(p, W, P, lo, hi);
   Cursor c;
-  if (mine) locate(p, lo, c);
+  const bool mine = my_range(p, U, P, lo, hi, c);
   pdl_wait();
   pdl_trigger();
   if (p.ws_job != nullptr && lane == 0) p.ws_job[blockIdx.x] = make_int2(-1, -1);
@@ -610,7 +609,8 @@ __global__ void __launch_bounds__(32, 16)
     }
     fp4_finish<D>(p, f, s, c, whole, blockIdx.x);
     if (!whole && seg_end == c.T && lane == 0)
-      p.ws_job[blockIdx.x] = make_int2(c.b * p.num_kv_heads + c.g, cta_of(W, P, useg));
+      p.ws_job[blockIdx.x] =
+          make_int2(c.b * p.num_kv_heads + c.g, first_cta(p, U, P, useg, c.b, c.g));
     u += seg_end - c.tile;
     if (u < hi) next_segment(p, c);
   }
