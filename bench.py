@@ -616,6 +616,25 @@ def _oracle_part(args):
     return gbs * secs * 1e9, segs, secs
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the
+    cpu_baseline record."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def oracle_sample_all_cores(name, budget_s):
     """The oracle on every host core: one spawned process per core, each on
     its share of the sequences (single-threaded BLAS in each); returns
@@ -650,6 +669,7 @@ def run_reference(args, w):
             segs = n
     value = statistics.mean(vals)
     cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "cpu_model": cpu_model(),
            "sample": f"{segs} whole (sequence, KV head) segments of {w.name} per step, "
                      f"fp64 numpy, single-threaded BLAS"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
@@ -808,6 +828,7 @@ def main():
     if rank == 0:
         v, segs, secs = oracle_sample(w, "cpu", args.cpu_budget)
         cpu = {"value": v, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{segs} whole (sequence, KV head) segments of {w.name}, "
                          f"the batch repeated ({secs:.1f} s of oracle time), fp64 numpy, "
                          f"single-threaded BLAS"}
