@@ -570,28 +570,40 @@ def run_e2e(w, pool, scale, tab, lens, slots, q, kn, vn, ws, fp8, stream, steps,
 
 
 # ------------------------------------------------------------ oracle arm ---
+_ORACLE_INPUTS = {}
+
+
+def _oracle_inputs(w, b, device):
+    """Sequence b's blocks and queries for the oracle, as float arrays: the
+    ceil(n_b / block_size) blocks it owns, generated from b's own seeds (the
+    oracle gathers through its local ids 0, 1, 2, ...).  Generated once per
+    process and kept, so the timed samples spend their time in the oracle."""
+    key = (w.name, b)
+    if key not in _ORACLE_INPUTS:
+        from paged_kv_cache_228_gb300 import workloads as W
+        nblk = -(-w.seq_lens[b] // w.block_size)
+        shape = (nblk, w.num_kv_heads, w.block_size, w.head_dim)
+        kk = W.normal_bf16(shape, w.seed * 1000 + b, device).float().cpu().numpy()
+        vv = W.normal_bf16(shape, w.seed * 1000 + b + 500, device).float().cpu().numpy()
+        qq = W.normal_bf16((w.num_q_heads, w.head_dim), w.seed * 1000 + b + 900,
+                           device).double().cpu().numpy()
+        _ORACLE_INPUTS[key] = (kk, vv, qq, np.arange(nblk))
+    return _ORACLE_INPUTS[key]
+
+
 def oracle_sample(w, device, budget_s, part=(0, 1)):
     """Time the fp64 oracle (as it stands) on whole (sequence, KV head)
     segments of this workload -- the sequences b with b % part[1] ==
     part[0], repeated -- until about ``budget_s`` seconds of oracle time;
-    returns (GB/s, segments, seconds)."""
+    returns (GB/s, segments, seconds).  Runs on the host alone: the inputs
+    come from the seeded generators, the lengths from the workload."""
     from oracle import paged_attention as OPA
-    from paged_kv_cache_228_gb300 import workloads as W
-    tables, _, _, _, _ = step_inputs(w, "cpu")
-    shape = (w.pool_blocks, w.num_kv_heads, w.block_size, w.head_dim)
     done_bytes, done, t_used = 0, 0, 0.0
     G = w.group
     mine = [b for b in range(w.num_seqs) if b % part[1] == part[0]]
     while mine:
         for b in mine:
-            # only this sequence's blocks are materialised on the host
-            kb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b, device)
-            vb = W.normal_bf16((len(tables[b]),) + shape[1:], w.seed * 1000 + b + 500, device)
-            kk = kb.float().cpu().numpy()
-            vv = vb.float().cpu().numpy()
-            qq = W.normal_bf16((w.num_q_heads, w.head_dim), w.seed * 1000 + b + 900,
-                               device).double().cpu().numpy()
-            local = np.arange(len(tables[b]))
+            kk, vv, qq, local = _oracle_inputs(w, b, device)
             for gk in range(w.num_kv_heads):
                 t0 = time.perf_counter()
                 kc = OPA.gather_sequence(kk[:, gk:gk + 1], local, w.seq_lens[b],
@@ -647,12 +659,14 @@ def oracle_sample_all_cores(name, budget_s):
     return total / max(r[2] for r in res) / 1e9, sum(r[1] for r in res), n
 
 
-def workload_config(w):
-    """The workload's identity, shared by both arms' JSON lines."""
+def workload_config(w, world_size=1):
+    """The workload's identity, the same dict in both arms' JSON lines (how
+    each arm ran goes in its own keys)."""
     return {"workload": w.name, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim,
             "block_size": w.block_size, "kv_bytes_per_step": kv_bytes(w),
-            "mean_seq_len": sum(w.seq_lens) / w.num_seqs}
+            "mean_seq_len": sum(w.seq_lens) / w.num_seqs,
+            "parallelism": f"{world_size} independent replicas" if world_size > 1 else "none"}
 
 
 def run_reference(args, w):
@@ -661,12 +675,13 @@ def run_reference(args, w):
         return
     # about 10x the cpu_baseline budget over the whole run (120 s by default)
     budget = 10.0 * args.cpu_budget / max(1, args.steps + args.warmup)
-    vals = []
+    vals, secs = [], []
     segs = 0
     for i in range(args.warmup + args.steps):
-        v, n, _ = oracle_sample(w, "cpu", budget)
+        v, n, t = oracle_sample(w, "cpu", budget)
         if i >= args.warmup:
             vals.append(v)
+            secs.append(t)
             segs = n
     value = statistics.mean(vals)
     cpu = {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -675,9 +690,14 @@ def run_reference(args, w):
                      f"fp64 numpy, single-threaded BLAS"}
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            # each step is a bounded sample of the workload (above), not the
+            # whole batch: its oracle time
+            "ms_per_step": 1e3 * statistics.mean(secs),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64", "data": "synthetic",
-            "config": {**workload_config(w), "parallelism": "host cores (oracle)"},
+            "config": workload_config(w),
+            "setup": {"arm": "the fp64 CPU oracle on host cores",
+                      "step": f"a bounded sample of {budget:.2f} s of oracle time"},
             "cpu_baseline": cpu,
             "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -845,11 +865,10 @@ def main():
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic (seeded N(0,1) bf16 K/V, Q; scattered blocks)",
-            "config": {
-                **workload_config(w),
+            "config": workload_config(w, ws),
+            "setup": {
                 "l2": f"inputs larger than L2: {res['n_pools']} rotating layer pools of "
                       f"{res['pool_bytes'] / 1e9:.2f} GB",
-                "parallelism": "replicas" if ws > 1 else "single GPU",
                 "step": "pa_decode_append: cache write fused into the decode launch, "
                         "+ merge launch",
                 "timing": "the timed steps launched back to back on one stream (no event "

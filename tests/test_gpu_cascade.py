@@ -9,15 +9,13 @@ head_dim 64; a cascade prefix shorter than the shared one; sequences that
 end exactly at the prefix (prefix partial alone) and one shorter than it
 (zeros, flagged); agreement with pa_decode on the same inputs.
 """
-import numpy as np
 import pytest
 import torch
 
-from oracle import paged_attention as OPA
 from paged_kv_cache_228_gb300 import pa
 from paged_kv_cache_228_gb300 import workloads as W
 
-from cases import _to_np64, assert_close, build_case, oracle_decode, snapshot_blocks
+from cases import assert_close, build_case, oracle_decode, snapshot_blocks
 
 pytestmark = pytest.mark.gpu
 
@@ -66,16 +64,19 @@ def test_cascade_parity_shared_prefix(bs, splits):
 def test_cascade_agrees_with_decode_and_shorter_prefix():
     case = build_case(W.shared_prefix(16, num_seqs=48, prefix=512))
     w = case.w
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
     pa.pa_cache_write(case.k_new, case.v_new, case.slots_t, case.k_cache, case.v_cache)
-    ref = _out(w)
+    ref = oracle_decode(case, snap, seqs)
+    dec = _out(w)
     ws = torch.empty(max(16, pa.pa_decode_workspace_size(w.num_seqs, w.num_q_heads,
                                                           w.num_kv_heads, w.head_dim)),
                      dtype=torch.uint8, device="cuda")
-    pa.pa_decode(case.q, case.k_cache, case.v_cache, case.table_t, case.lens_t, w.scale, ref, ws)
+    pa.pa_decode(case.q, case.k_cache, case.v_cache, case.table_t, case.lens_t, w.scale, dec, ws)
+    torch.cuda.synchronize()
+    assert_close(dec, ref, TOL, "plain decode of the forked batch")
     for prefix_len in (512, 256, 16):   # any whole-block part of the shared prefix
-        out = _cascade(case, prefix_len)
-        d = (out.float() - ref.float()).abs()
-        assert torch.all(d <= TOL + TOL * ref.float().abs()), (prefix_len, d.max().item())
+        assert_close(_cascade(case, prefix_len), ref, TOL, f"cascade prefix {prefix_len}")
     assert pa.pa_get_device_error() == 0
 
 
@@ -86,20 +87,15 @@ def test_cascade_head_dim_64_and_sequences_at_the_prefix():
     w = W.Workload("cascade_d64", 12, 4, 2, 64, 16, seq_lens=base.seq_lens,
                    pool_blocks=base.pool_blocks, seed=9, shared_prefix=64)
     case = build_case(w)
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)  # before any library kernel writes the pool
     pa.pa_cache_write(case.k_new, case.v_new, case.slots_t, case.k_cache, case.v_cache)
     lens = list(w.seq_lens)
     lens[0] = lens[5] = 64
     lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = _cascade(case, 64, lens=lens_t)
-    ids = sorted({x for t in case.tables for x in t})
-    local = {x: i for i, x in enumerate(ids)}
-    idx = torch.tensor(ids, dtype=torch.int64, device="cuda")
-    kk = case.k_cache.index_select(0, idx).float().cpu().numpy()
-    vv = case.v_cache.index_select(0, idx).float().cpu().numpy()
-    tab = -np.ones((w.num_seqs, max(len(t) for t in case.tables)), dtype=np.int64)
-    for b, t in enumerate(case.tables):
-        tab[b, :len(t)] = [local[x] for x in t]
-    ref = OPA.decode(_to_np64(case.q), kk, vv, tab, np.array(lens), w.scale)
+    # the oracle applies the append to the snapshot and attends over `lens`
+    ref = oracle_decode(case, snap, seqs, lens=lens)
     assert_close(out, ref, TOL, "cascade d64 with sequences at the prefix")
     assert pa.pa_get_device_error() == 0
     # a sequence shorter than the prefix: zeros and a flag

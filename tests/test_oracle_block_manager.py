@@ -161,3 +161,39 @@ def test_usage_closed_forms():
     assert u["tokens_logical"] == 4 * 32 + 39
     assert u["live_blocks"] == 2 + (1 + 1 + 2 + 1)
     assert u["slots_reserved"] == u["live_blocks"] * bs
+
+
+def test_footprint_fp8_scale_bytes_closed_forms():
+    # The FP8 branch: codes at one byte per value plus two fp32 scales (K, V)
+    # per (block, KV head) a sequence touches.  70B layer at 128K, 8
+    # sequences: 2^31 code bytes and 2 * 8192 blocks * 8 heads * 4 B * 8.
+    n = [131072] * 8
+    assert footprint.decode_step_kv_bytes(n, 8, 128, 1, 16, 4) == 2 ** 31 + 2 * 8 * 8192 * 8 * 4
+    assert footprint.decode_step_kv_bytes(n, 8, 128, 1, 16, 4) == 2151677952
+    # worked by hand: 17 tokens in 16-token blocks touch 2 blocks; 2 heads,
+    # d = 64: 17 * 2 * 2 * 64 = 4352 code bytes + 2 * 2 * 2 * 4 = 32 scale bytes
+    assert footprint.decode_step_kv_bytes([17], 2, 64, 1, 16, 4) == 4384
+    # an exact block multiple adds no partial block; length 0 touches none
+    assert footprint.decode_step_kv_bytes([32, 0], 2, 64, 1, 16, 4) == 32 * 256 + 2 * 2 * 2 * 4
+    # without scales the branch is the plain footprint
+    assert footprint.decode_step_kv_bytes([17], 2, 64, 1, 16, 0) == 4352
+
+
+def test_bench_byte_counts_equal_the_oracle_footprint():
+    # bench.py restates the algorithmic byte counts (the product must not
+    # import the oracle); they must equal the pinned oracle functions on
+    # every workload and format.
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    from paged_kv_cache_228_gb300 import workloads as W
+    for name, make in W.WORKLOADS.items():
+        w = make()
+        H, d, bs = w.num_kv_heads, w.head_dim, w.block_size
+        assert bench.kv_bytes(w) == footprint.decode_step_kv_bytes(w.seq_lens, H, d, 2), name
+        assert bench.kv_bytes(w, 1, 4) == footprint.decode_step_kv_bytes(
+            w.seq_lens, H, d, 1, bs, 4), name
+        assert bench.kv_bytes_nvfp4(w) == sum(w.seq_lens) * footprint.nvfp4_bytes_per_token(
+            1, H, d), name
+    assert bench.kv_bytes(W.llama31_70b_128k(), 1, 4) == 2151677952
