@@ -255,6 +255,43 @@ def kv_bytes(w, bytes_per_scalar=2, scale_bytes=0):
     return total
 
 
+def block_size_sweep(args, device, peak):
+    """The shared-prefix batch (256 forks of a 2048-token prompt, private
+    suffixes of 1..512 tokens) at block sizes 8, 16 and 32, each through the
+    plain paged decode and the cascade: time per step and per decode call,
+    logical KV bytes (the prefix counted once per sequence) and unique KV
+    bytes (every stored token once: the least DRAM traffic a step can
+    have), and the paging waste of the host block manager's layout."""
+    from paged_kv_cache_228_gb300 import workloads as W
+    out = {}
+    for bs in (8, 16, 32):
+        wl = W.shared_prefix(bs)
+        frag = fragmentation_report(wl, 2048 + 512)
+        unique = frag["tokens_stored"] * 2 * wl.num_kv_heads * wl.head_dim * 2
+        nb = kv_bytes(wl)
+        for casc in (False, True):
+            r = run_native(wl, max(50, args.steps // 20), max(3, args.warmup // 10), device,
+                           profile_only=True, cascade=casc)
+            dec_s = r["decode_ms_mean"] / 1e3
+            out[wl.name + ("_cascade" if casc else "")] = {
+                "block_size": bs,
+                "kv_bytes_per_step": nb,
+                "unique_kv_bytes_per_step": unique,
+                "us_per_step": r["ms_per_step"] * 1e3,
+                "decode_us": dec_s * 1e6,
+                "decode_GB_per_s": nb / dec_s / 1e9,
+                "unique_GB_per_s": unique / dec_s / 1e9,
+                "unique_frac_of_measured_hbm": unique / dec_s / 1e9 / peak,
+                "paged_waste": frag["paged_waste"],
+                "dram_bytes_per_launch": ncu_traffic(wl.name + ("_cascade" if casc else "")),
+                "call": "pa_decode_cascade (the prefix's attention once for all sequences, "
+                        "suffixes paged), after pa_cache_write" if casc else "pa_decode_append "
+                        "(every sequence walks the shared prefix blocks through its own "
+                        "table)",
+            }
+    return out
+
+
 # ----------------------------------------------------------- native arm ---
 def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=None,
                profile_only=False, cascade=False, nvfp4=False):
@@ -784,8 +821,7 @@ def main():
     if rank == 0 and not args.no_secondary and args.workload == "llama3.1-8b":
         # paging tax: the same batch with contiguous physical blocks; the
         # other report-only shapes (decode kernel pair only, logical bytes)
-        for wl, casc in ((W.contiguous(w), False), (W.llama32_1b(), False),
-                         (W.shared_prefix(16), False), (W.shared_prefix(16), True)):
+        for wl, casc in ((W.contiguous(w), False), (W.llama32_1b(), False)):
             r = run_native(wl, max(50, args.steps // 20), max(3, args.warmup // 10), device,
                            profile_only=True, cascade=casc)
             nb = kv_bytes(wl)
@@ -795,6 +831,7 @@ def main():
                 "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
                 "us_per_step": r["ms_per_step"] * 1e3,
             }
+        secondary.update(block_size_sweep(args, device, peak))
         r = run_native(w, max(50, args.steps // 20), max(3, args.warmup // 10), device,
                        nvfp4=True)
         nb = kv_bytes_nvfp4(w)
@@ -812,21 +849,14 @@ def main():
         secondary["offload"]["note"] = (
             "pa_swap_out / pa_swap_in of every block the 8B batch uses, between HBM and "
             "pinned host memory read and written in place by the kernel")
-        secondary["fragmentation"] = {
-            w.name: fragmentation_report(w, 4096),
-            W.shared_prefix(16).name: fragmentation_report(W.shared_prefix(16), 2048 + 512),
-        }
+        secondary["fragmentation"] = {w.name: fragmentation_report(w, 4096)}
+        for bs in (8, 16, 32):
+            secondary["fragmentation"][W.shared_prefix(bs).name] = fragmentation_report(
+                W.shared_prefix(bs), 2048 + 512)
         c = secondary[W.contiguous(w).name]["decode_GB_per_s"]
         secondary["paging_tax"] = {
             "scattered_decode_GB_per_s": achieved, "contiguous_decode_GB_per_s": c,
             "tax": 1.0 - achieved / c}
-        secondary[W.shared_prefix(16).name]["note"] = (
-            "logical bytes: the 2048-token prefix is counted once per sequence; "
-            "its blocks are read from L2 after the first")
-        secondary[W.shared_prefix(16).name + "_cascade"]["note"] = (
-            "pa_decode_cascade: the prefix's attention computed once for all 256 sequences "
-            "(tensor-core product of all query rows with the prefix), suffixes paged; "
-            "logical bytes as above")
     if rank == 0 and not args.no_secondary and args.workload != "llama3.1-70b-128k":
         wl = W.llama31_70b_128k()
         for fmt in ("bf16", "fp8", "nvfp4"):
@@ -834,7 +864,17 @@ def main():
             r = run_native(wl, max(20, args.steps // 50), max(3, args.warmup // 10), device,
                            fp8=fp8, n_pools=1, nvfp4=fp4)
             nb = kv_bytes_nvfp4(wl) if fp4 else kv_bytes(wl, 1 if fp8 else 2, 4 if fp8 else 0)
+            dec_gbs = nb / (r["decode_ms_mean"] / 1e3) / 1e9
             secondary["llama3.1-70b-128k_" + fmt] = {
+                "roofline": {
+                    "bound": "hbm", "achieved": dec_gbs, "peak": peak, "unit": "GB/s",
+                    "frac": dec_gbs / peak,
+                    "traffic": ncu_traffic(wl.name if fmt == "bf16" else f"{wl.name}_{fmt}"),
+                    "kernel": {"bf16": "paged_decode_ws_kernel<128,bf16>",
+                               "fp8": "paged_decode_kernel<128,fp8>",
+                               "nvfp4": "paged_decode_nvfp4_kernel<128>"}[fmt] + " + merge "
+                              "(per launch pair, CUDA events around each call)",
+                    "peak_source": peak_kind},
                 "kv_bytes_per_step": nb,
                 "us_per_step": r["ms_per_step"] * 1e3,
                 "GB_per_s": nb / (r["ms_per_step"] / 1e3) / 1e9,

@@ -448,9 +448,13 @@ pa_status pa_decode_cascade(const void* q, const void* k_cache,
  *   - The first call on each device looks up that device's address of the
  *     array (with the device current); make that first call before any
  *     stream capture on the device.
- *   - Requests whose workspace (pa_decode_workspace_size with the same
- *     num_splits) exceeds PA_NOALLOC_SCRATCH_BYTES are rejected with
- *     PA_ERR_WORKSPACE and nothing is enqueued.
+ *   - The limit applies to the workspace this call itself needs: that of
+ *     its own KV format at its partition count (num_splits, or with 0 the
+ *     format's automatic count, one partition per resident decode CTA).  A
+ *     call needing more than PA_NOALLOC_SCRATCH_BYTES is rejected with
+ *     PA_ERR_WORKSPACE and nothing is enqueued.  pa_decode_workspace_size
+ *     with num_splits = 0 returns the largest automatic size over all
+ *     formats, so as a pre-check it can only over-predict a refusal.
  *   - All calls on a device share the one array, which keeps whatever the
  *     last call left in it.  Nothing in it needs to start at zero: every
  *     partial result a call reads was written earlier by the same call.

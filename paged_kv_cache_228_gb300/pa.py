@@ -5,10 +5,21 @@ the same name; torch tensors are used only as device (or host) memory and
 their current CUDA stream.  No computation of the method happens in Python:
 if ``libpa.so`` is missing, importing the functions raises instead of
 falling back to anything else.
+
+Ordering of ``seq_lens``: every decode call (pa_decode*, pa_decode_cascade,
+pa_decode_noalloc) launches as a programmatic dependent of the work before
+it on the stream and reads ``seq_lens`` to split its work BEFORE it waits
+for that work.  Nothing in this library writes ``seq_lens``.  If a kernel of
+yours writes ``seq_lens`` and calls ``griddepcontrol.launch_dependents``
+(lets its dependents start early), do not launch a decode call directly
+after it on the same stream: put a copy or any kernel
+without that trigger in between.  Ordinary stream order (torch ops, copies)
+needs nothing.
 """
 from __future__ import annotations
 
 import ctypes
+import itertools
 import os
 import time
 
@@ -253,7 +264,9 @@ def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
 
 def pa_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, out, workspace=None,
               k_scale=None, v_scale=None, num_splits=0, stream=None):
-    """Paged decode attention: out[B, Hq, d] (bf16) from q[B, Hq, d] (bf16)."""
+    """Paged decode attention: out[B, Hq, d] (bf16) from q[B, Hq, d] (bf16).
+    ``seq_lens`` is read before the wait for the preceding kernel (see the
+    module docstring)."""
     _need(q, torch.bfloat16, "q", 3)
     _need(out, torch.bfloat16, "out", 3)
     _need(block_tables, torch.int32, "block_tables", 2)
@@ -517,8 +530,8 @@ class Allocator:
                                        slots, cow, ctypes.byref(ncow))
         if st != PA_OK:
             return st, None, None
-        want = -(-(length + n) // block_size)
-        table[:] = list(tab[:want])
+        # the call filled the -1 padded table up to the sequence's new end
+        table[:] = list(itertools.takewhile(lambda x: x >= 0, tab))
         pairs = [tuple(cow[:3])] if ncow.value else []
         return st, list(slots[:n]), pairs
 
