@@ -29,7 +29,7 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
 
 SOURCES = ["libpa.cu", "block_manager.cpp"]
 DEPS = ["libpa.cu", "block_manager.cpp", "decode.cuh", "cache_ops.cuh", "cascade.cuh", "nvfp4.cuh",
-        "pa_device.cuh"]
+        "pa_device.cuh", "umma.cuh"]
 
 
 def _nvcc() -> str:

@@ -7,311 +7,513 @@
 // the log-sum-exp merge of attention over any split of its tokens, so the
 // prefix part can be computed once for every sequence's queries: for KV
 // head g it is a dense product of all B*G query rows with the prefix keys
-// and values, S = Q_g K_p^T, online softmax, O = P V_p -- a contraction
-// with many rows, run here on the tensor pipe (mma.sync m16n8k16, queries
-// on M, tokens on N for QK and on K for PV).  The result is one partial
-// (o unnormalised, m in log2 units, l) per (sequence, query head); the
-// suffix decode and its merge fold it in.
+// and values, S = Q_g K_p^T, online softmax, O = P V_p.  The result is one
+// partial (o unnormalised, m in log2 units, l) per (sequence, query head);
+// the suffix decode and its merge fold it in.
 //
-// CTA = 4 warps on 64 query rows of one KV head and one of S token ranges
-// of the prefix (S splits keep ~3 CTAs per SM busy).  The CTA streams its
-// range in 32-token chunks through a 3-stage cp.async ring that all 4
-// warps read (each chunk's K and V are fetched once per 64 rows); warp w
-// computes rows 16w .. 16w+15.  Chunk rows use the decode kernels' 128-byte
-// slab layout with the chunk index XOR-swizzled by row, and the range's
-// block ids are staged in shared memory first.  Each split writes its own
-// partial; the consumers fold in all S.
+// GB300 design: the two products run on the fifth-generation tensor cores
+// (tcgen05.mma, kind::f16, M = 128 query rows, fp32 accumulators in tensor
+// memory), operands in shared memory in the 128-byte-swizzled layout the
+// TMA writes.  What bounds this pass is how fast an SM takes in K and V
+// (the TMA delivers about 55 GB/s per SM, L2 or HBM alike), so a CTA makes
+// each byte serve two 128-row query tiles: it owns 256 query rows of one KV
+// head and one of S token ranges of the prefix, walked in 64-token chunks.
+// Eleven warps:
+//   warps 0/10 TMA producers of K and of V (one 2D box per block and
+//              64-column slab) into a 3-stage K ring and a 4-stage V ring;
+//   warp 1     owns the tensor memory; lane 0 issues the MMAs, for each
+//              query tile t:
+//                S_t   = Q_t . K_j^T                 (A, B K-major; N = 64)
+//                O_t  += P_t,j-1 . V_j-1              (P K-major, V MN-major)
+//              the S of chunk j two chunks ahead of the products (into one of
+//              two S buffers per tile), so a tile's next scores are ready
+//              when its softmax finishes a chunk;
+//   warps 2-9  softmax, four warps per query tile, one row per thread (the
+//              warp's quarter of the tensor-memory lanes): online softmax in
+//              fp32 -- the running max moves, and O_t in tensor memory is
+//              rescaled, only when a score exceeds it by more than 8 in
+//              log2 units -- P rounded to bf16 into the tile's shared P
+//              buffer (rewritten once the previous product of the tile is
+//              done), and l sums those rounded weights.
+// Each split writes its own partial per row (staged through shared memory
+// so the global stores are coalesced); prefix_merge_kernel folds the S of
+// them together.
 #pragma once
 
 #include "pa_device.cuh"
+#include "umma.cuh"
 
 namespace pa {
 
 struct PrefixParams {
-  const uint8_t* q;        // [num_seqs][num_q_heads][D] bf16
-  const uint8_t* k_cache;  // [num_blocks][num_kv_heads][block_size][D] bf16
-  const uint8_t* v_cache;
+  const uint8_t* q;             // [num_seqs][num_q_heads][D] bf16
   const int32_t* prefix_table;  // the prefix's block ids (sequence 0's table)
   float* pf_o;                  // [splits][num_seqs * num_q_heads][D]
   float2* pf_ml;                // [splits][num_seqs * num_q_heads]
   int32_t num_seqs, num_q_heads, num_kv_heads, group, block_size, log2_bs, num_blocks;
+  int32_t rows_total;     // num_blocks * num_kv_heads * block_size (rows of the K/V maps)
   int32_t prefix_tokens;
-  int32_t prefix_chunks;  // ceil(prefix_tokens / 32)
+  int32_t prefix_chunks;  // ceil(prefix_tokens / kPfChunk)
   int32_t splits;         // S
   float scale_log2;
 };
 
-constexpr int kPfWarps = 4;
-constexpr int kPfRows = 64;     // query rows per CTA (16 per warp)
-constexpr int kPfChunk = 32;    // tokens per stage
-constexpr int kPfStages = 3;
-constexpr int kPfMaxBlocks = 1024;  // block ids of one split staged in shared memory
+constexpr int kPfRows = 128;    // query rows per tile (the MMA's M)
+constexpr int kPfTiles = 2;     // query tiles per CTA sharing each K/V chunk
+constexpr int kPfChunk = 64;    // prefix tokens per chunk
+constexpr int kPfKStages = 3;   // K ring depth
+constexpr int kPfVStages = 4;   // V ring depth (V waits a whole softmax longer)
+constexpr int kPfSoftWarps = 4 * kPfTiles;
+constexpr int kPfThreads = 96 + 32 * kPfSoftWarps;  // K and V producers, MMA, softmax
+constexpr int kPfVWarp = 2 + kPfSoftWarps;
+constexpr int kPfTmemCols = 512;
+constexpr int kPfMaxSplits = 8;
 
 template <int D>
 struct PfSmem {
-  static constexpr int kRows128 = 128;                   // bytes per slab row
-  static constexpr int kKV = (D / 64) * kPfChunk * 128;  // K (or V) of a chunk
-  static constexpr int kStage = 2 * kKV;
-  static constexpr int kQ = (D / 64) * kPfRows * 128;
-  static constexpr int kIds = kPfMaxBlocks * 4;
-  static constexpr int kBytes = kQ + kPfStages * kStage + kIds;
+  static constexpr int kSlab = kPfChunk * 128;        // 64 columns of one chunk
+  static constexpr int kKV = (D / 64) * kSlab;        // K (or V) of a chunk
+  static constexpr int kQ = (D / 64) * kPfRows * 128; // one query tile
+  static constexpr int kP = kPfRows * kPfChunk * 2;   // one tile's P (one 128-byte slab)
+  static constexpr int kOffK = kPfTiles * kQ;
+  static constexpr int kOffV = kOffK + kPfKStages * kKV;
+  static constexpr int kOffP = kOffV + kPfVStages * kKV;
+  static constexpr int kOffBar = kOffP + kPfTiles * kP;
+  static constexpr int kBytes = kOffBar + 256;
+  // the epilogue stages one tile's partial in the (free) V ring, and the
+  // per-row (m, l) in the (free) K ring
+  static_assert(kPfRows * D * 4 <= kPfVStages * kKV, "epilogue staging");
+  static_assert(kPfTiles * kPfRows * 8 <= kPfKStages * kKV, "epilogue (m, l)");
+  static_assert(kP == kPfRows * 128, "P is one slab");
 };
 
+struct PfBars {
+  uint64_t k_full[kPfKStages], k_empty[kPfKStages];
+  uint64_t v_full[kPfVStages], v_empty[kPfVStages];
+  uint64_t s_full[kPfTiles][2], s_empty[kPfTiles][2];
+  uint64_t p_full[kPfTiles];  // P of the tile's current chunk written
+  uint64_t o_done[kPfTiles];  // the tile's product with that P complete
+  uint64_t mma_done;
+  uint32_t tmem;
+};
+static_assert(sizeof(PfBars) <= 256, "barrier block");
+
 // Byte offset of 16-byte chunk c (along the row's D * 2 bytes) of row r in
-// a tile of `rows` rows stored as 128-byte slabs.
+// a tile of `rows` rows stored as 128-byte slabs (128-byte swizzle).
 __device__ __forceinline__ uint32_t pf_chunk(int rows, int r, int c) {
   return (c >> 3) * (rows * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-// Wait until at most n (0..2) of this thread's copy groups are in flight.
-__device__ __forceinline__ void cp_async_wait_upto(int n) {
-  if (n >= 2)
-    asm volatile("cp.async.wait_group 2;" ::: "memory");
-  else if (n == 1)
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-  else
-    asm volatile("cp.async.wait_group 0;" ::: "memory");
+// Producer lane i's block of chunk ch: the id of the block holding tokens
+// [ch * kPfChunk + i * box_rows, + box_rows), or -1 past the prefix (and
+// for lanes past the chunk's blocks).
+__device__ __forceinline__ int32_t pf_block_id(const PrefixParams& p, int32_t ch) {
+  const int lane = threadIdx.x & 31;
+  const int box_rows = p.block_size < kPfChunk ? p.block_size : kPfChunk;
+  const int32_t tok = ch * kPfChunk + lane * box_rows;
+  if (lane >= kPfChunk / box_rows || tok >= p.prefix_tokens) return -1;
+  return p.prefix_table[tok >> p.log2_bs];
 }
 
-// CTA: K and V rows of prefix chunk ch (its block ids in `ids`, indexed
-// from the split's first block) into a stage.  Invalid ids read as zeros.
+// Producer lanes: the K (or V) rows of chunk ch into one ring stage, block i
+// of the chunk (boxes of min(bs, 64) rows, one per 64-column slab) by lane
+// i.  Blocks past the prefix, or with an invalid id, read rows past the
+// tensor, which the TMA fills with zeros.
 template <int D>
-__device__ __forceinline__ void pf_issue(const PrefixParams& p, int32_t g, int32_t ch,
-                                         int32_t first_tok, const int32_t* ids,
-                                         uint32_t kdst) {
-  constexpr int kCpr = D * 2 / 16;  // chunks per row
-  for (int idx = threadIdx.x; idx < kPfChunk * kCpr; idx += kPfWarps * 32) {
-    const int r = idx / kCpr, c = idx % kCpr;
-    const int32_t tok = ch * kPfChunk + r;
-    // rows past the prefix (a last chunk of 16) read as zeros
-    const int32_t blk = tok < p.prefix_tokens ? ids[(tok - first_tok) >> p.log2_bs] : -1;
-    const bool ok = blk >= 0 && blk < p.num_blocks;
-    const int64_t row = (static_cast<int64_t>(blk) * p.num_kv_heads + g) * p.block_size +
-                        (tok & (p.block_size - 1));
-    const int64_t byte = ok ? row * (D * 2) + c * 16 : 0;
-    const uint32_t d = kdst + pf_chunk(kPfChunk, r, c);
-    cp_async16(d, p.k_cache + byte, ok ? 16u : 0u);
-    cp_async16(d + PfSmem<D>::kKV, p.v_cache + byte, ok ? 16u : 0u);
+__device__ __forceinline__ void pf_copy_chunk(const PrefixParams& p, const CUtensorMap* map,
+                                              int32_t g, int32_t ch, int32_t blk, uint32_t dst,
+                                              uint32_t bar) {
+  const int lane = threadIdx.x & 31;
+  const int box_rows = p.block_size < kPfChunk ? p.block_size : kPfChunk;
+  if (lane == 0) mbar_arrive_expect_tx(bar, PfSmem<D>::kKV);
+  __syncwarp();
+  if (lane < kPfChunk / box_rows) {
+    const int32_t tok = ch * kPfChunk + lane * box_rows;
+    int32_t row = p.rows_total;
+    if (tok < p.prefix_tokens) {
+      if (blk >= 0 && blk < p.num_blocks)
+        row = (blk * p.num_kv_heads + g) * p.block_size + (tok & (p.block_size - 1));
+      else
+        flag_error(PA_DEVERR_BAD_BLOCK_ID);
+    }
+#pragma unroll
+    for (int sl = 0; sl < D / 64; ++sl)
+      tma_load_2d(dst + sl * PfSmem<D>::kSlab + lane * box_rows * 128, map, sl * 64, row, bar);
   }
 }
 
 template <int D>
-__global__ void __launch_bounds__(kPfWarps * 32)
-    prefix_attention_kernel(const PrefixParams p) {
+__global__ void __launch_bounds__(kPfThreads, 1)
+    prefix_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const PrefixParams p) {
   using L = PfSmem<D>;
   extern __shared__ __align__(1024) uint8_t pf_smem[];
-  pdl_wait();  // launched as a programmatic dependent: inputs ready below
-  pdl_trigger();
   const uint32_t base = smem_addr(pf_smem);
-  const uint32_t qs = base, ring = base + L::kQ;
-  int32_t* ids = reinterpret_cast<int32_t*>(pf_smem + L::kQ + kPfStages * L::kStage);
+  if (base & 1023u) {  // the same for every CTA of the launch
+    if (threadIdx.x == 0) flag_error(PA_DEVERR_LAUNCH);
+    return;
+  }
+  PfBars* bars = reinterpret_cast<PfBars*>(pf_smem + L::kOffBar);
+  const uint32_t sq = base, sk = base + L::kOffK, sv = base + L::kOffV, sp = base + L::kOffP;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gq = lane >> 2, tq = lane & 3;
   const int32_t g = blockIdx.y, split = blockIdx.z;
-  const int64_t R = static_cast<int64_t>(p.num_seqs) * p.group;  // query rows of head g
-  const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kPfRows;
-  // this split's chunks [c0, c1) and their block ids
+  const uint32_t G = static_cast<uint32_t>(p.group);
+  const uint32_t R = static_cast<uint32_t>(p.num_seqs) * G;  // query rows of head g
+  const uint32_t row0 = blockIdx.x * (kPfTiles * kPfRows);
   const int32_t c0 = static_cast<int32_t>(static_cast<int64_t>(p.prefix_chunks) * split / p.splits);
   const int32_t c1 = static_cast<int32_t>(static_cast<int64_t>(p.prefix_chunks) * (split + 1) / p.splits);
-  const int32_t first_tok = c0 * kPfChunk;
-  const int32_t first_blk = first_tok >> p.log2_bs;
-  const int32_t last_tok = min(c1 * kPfChunk, p.prefix_tokens) - 1;
-  const int32_t nblk = ((last_tok >> p.log2_bs) - first_blk) + 1;
-  for (int i = threadIdx.x; i < nblk; i += blockDim.x) {
-    const int32_t e = p.prefix_table[first_blk + i];
-    if (!(e >= 0 && e < p.num_blocks)) flag_error(PA_DEVERR_BAD_BLOCK_ID);
-    ids[i] = e;
-  }
-  // first_tok is block-aligned only when bs <= 32; index ids from the
-  // split's first block
-  const int32_t id_tok0 = first_blk << p.log2_bs;
-  // ---- 64 query rows (zeros past R): row r -> sequence (row0+r) / G, head g*G + (row0+r) % G
-  {
-    constexpr int kCpr = D * 2 / 16;
-    for (int idx = threadIdx.x; idx < kPfRows * kCpr; idx += blockDim.x) {
-      const int r = idx / kCpr, c = idx % kCpr;
-      const int64_t gr = row0 + r;
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (gr < R) {
-        const int64_t b = gr / p.group, j = gr % p.group;
-        v = *reinterpret_cast<const uint4*>(
-            p.q + ((b * p.num_q_heads + g * p.group + j) * D) * 2 + c * 16);
-      }
-      asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(qs + pf_chunk(kPfRows, r, c)),
-                   "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
-    }
-  }
-  __syncthreads();  // ids and Q staged
-  // prologue: the first two chunks
   const int32_t n = c1 - c0;
-  for (int k = 0; k < 2 && k < n; ++k) {
-    pf_issue<D>(p, g, c0 + k, id_tok0, ids, ring + k * L::kStage);
-    cp_async_commit();
+  // q / partial row of CTA row r (r < R - row0): sequence b, head g*G + j
+  auto head_row = [&](uint32_t r) -> int64_t {
+    const uint32_t gr = row0 + r, b = gr / G, j = gr - b * G;
+    return static_cast<int64_t>(b) * p.num_q_heads + g * p.group + j;
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kPfKStages; ++i) {
+      mbar_init(smem_addr(&bars->k_full[i]), 1);
+      mbar_init(smem_addr(&bars->k_empty[i]), 1);
+    }
+    for (int i = 0; i < kPfVStages; ++i) {
+      mbar_init(smem_addr(&bars->v_full[i]), 1);
+      mbar_init(smem_addr(&bars->v_empty[i]), 1);
+    }
+    for (int t = 0; t < kPfTiles; ++t) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_addr(&bars->s_full[t][i]), 1);
+        mbar_init(smem_addr(&bars->s_empty[t][i]), 4);
+      }
+      mbar_init(smem_addr(&bars->p_full[t]), 4);
+      mbar_init(smem_addr(&bars->o_done[t]), 1);
+    }
+    mbar_init(smem_addr(&bars->mma_done), 1);
+    mbar_fence_init();
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
-  // A fragments of this warp's 16 rows of Q
-  uint32_t qa[D / 16][4];
+  __syncthreads();  // barriers initialised
+  pdl_wait();       // launched as a programmatic dependent: inputs ready below
+  pdl_trigger();
+  bool ok = true;
+  uint32_t tmem = 0;
+  if (warp >= 1 && warp < kPfVWarp) {
+    // The tensor memory (warp 1) and the 256 query rows (softmax warps;
+    // zeros past R), then a barrier of warps 1-9.  The producers have
+    // started meanwhile.
+    if (warp == 1) {
+      tmem_alloc(smem_addr(&bars->tmem), kPfTmemCols);
+      tmem_relinquish();
+    } else {
+      constexpr int kCpr = D * 2 / 16;
+      constexpr int kSoft = 32 * kPfSoftWarps;
+      constexpr int kPer = kPfTiles * kPfRows * kCpr / kSoft;  // 16-byte chunks per thread
+      const int t = threadIdx.x - 64;
+      uint4 v[kPer];
 #pragma unroll
-  for (int ks = 0; ks < D / 16; ++ks) {
-    const int i = lane >> 3;  // matrices (rows 0-7 | 8-15) x (k lo | k hi)
-    const int r = 16 * warp + (lane & 7) + 8 * (i & 1);
-    ldsm_x4(qs + pf_chunk(kPfRows, r, 2 * ks + (i >> 1)), qa[ks][0], qa[ks][1], qa[ks][2],
-            qa[ks][3]);
+      for (int i = 0; i < kPer; ++i) {  // all loads in flight first
+        const int idx = t + kSoft * i, r = idx / kCpr, c = idx % kCpr;
+        v[i] = make_uint4(0u, 0u, 0u, 0u);
+        if (row0 + r < R)
+          v[i] = *reinterpret_cast<const uint4*>(p.q + head_row(r) * (D * 2) + c * 16);
+      }
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int idx = t + kSoft * i, r = idx / kCpr, c = idx % kCpr;
+        const uint32_t a = sq + (r / kPfRows) * L::kQ + pf_chunk(kPfRows, r % kPfRows, c);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v[i].x), "r"(v[i].y),
+                     "r"(v[i].z), "r"(v[i].w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // the MMA (async proxy) reads Q
+    }
+    tc_fence_before_sync();
+    asm volatile("bar.sync 1, %0;" ::"r"(32 * (kPfVWarp - 1)) : "memory");
+    tc_fence_after_sync();
+    tmem = bars->tmem;
   }
-  float o[D / 8][4];
-#pragma unroll
-  for (int i = 0; i < D / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};  // rows gq, gq + 8
-  for (int32_t k = 0; k < n; ++k) {
-    if (k + 2 < n) {
-      pf_issue<D>(p, g, c0 + k + 2, id_tok0, ids, ring + ((k + 2) % kPfStages) * L::kStage);
-      cp_async_commit();
+
+  if (warp == 0 || warp == kPfVWarp) {
+    // ----------------------------------------- producers: K (0), V (10) ---
+    const bool is_k = warp == 0;
+    const int S = is_k ? kPfKStages : kPfVStages;
+    const CUtensorMap* map = is_k ? &tm_k : &tm_v;
+    const uint32_t ring = is_k ? sk : sv;
+    uint64_t* full = is_k ? bars->k_full : bars->v_full;
+    uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
+    int32_t issued = 0;
+    int32_t e = pf_block_id(p, c0), en = n > 1 ? pf_block_id(p, c0 + 1) : -1;
+    for (int32_t j = 0; j < n && ok; ++j) {
+      const int st = j % S;
+      if (lane == 0 && j >= S) ok = mbar_wait(smem_addr(&empty[st]), ((j / S) - 1) & 1);
+      if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+      pf_copy_chunk<D>(p, map, g, c0 + j, e, ring + st * L::kKV, smem_addr(&full[st]));
+      issued = j + 1;
+      e = en;  // the next chunk's ids, loaded a chunk ahead
+      en = j + 2 < n ? pf_block_id(p, c0 + j + 2) : -1;
     }
-    cp_async_wait_upto(min(2, n - 1 - k));
-    __syncthreads();  // chunk k landed for every thread's copies
-    const uint32_t kb = ring + (k % kPfStages) * L::kStage;
-    // S = Q K^T, 4 blocks of 8 tokens
-    float s[4][4] = {};
+    // No copy may still target shared memory when the CTA exits: on the
+    // normal path the MMAs have consumed every one already.
+    if (lane == 0)
+      for (int32_t j = issued > S ? issued - S : 0; j < issued; ++j)
+        mbar_wait(smem_addr(&full[j % S]), (j / S) & 1, 1u << 16);
+  } else if (warp == 1) {
+    // ---------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      constexpr uint32_t kIdQK = idesc_bf16(kPfRows, kPfChunk, false, false);
+      constexpr uint32_t kIdPV = idesc_bf16(kPfRows, D, false, true);
+      auto issue_pv = [&](int32_t i) -> bool {
+        const int vs = i % kPfVStages;
+        if (!mbar_wait(smem_addr(&bars->v_full[vs]), (i / kPfVStages) & 1)) return false;
+        const uint32_t vb = sv + vs * L::kKV;
+        for (int t = 0; t < kPfTiles; ++t) {
+          if (!mbar_wait(smem_addr(&bars->p_full[t]), i & 1)) return false;
+          tc_fence_after_sync();
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks)
+          for (int k = 0; k < kPfChunk / 16; ++k)
+            umma_bf16(tmem + kPfTiles * 2 * kPfChunk + t * D,
+                      smem_desc_sw128(sp + t * L::kP + k * 32, 16, 1024),
+                      smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV, i > 0 || k > 0);
+          umma_commit(smem_addr(&bars->o_done[t]));
+        }
+        umma_commit(smem_addr(&bars->v_empty[vs]));
+        return true;
+      };
+      for (int32_t j = 0; j < n && ok; ++j) {
+        ok = mbar_wait(smem_addr(&bars->k_full[j % kPfKStages]), (j / kPfKStages) & 1);
+        const uint32_t kb = sk + (j % kPfKStages) * L::kKV;
+        for (int t = 0; t < kPfTiles && ok; ++t) {
+          if (j >= 2) ok = mbar_wait(smem_addr(&bars->s_empty[t][j & 1]), ((j - 2) >> 1) & 1);
+          if (!ok) break;
+          tc_fence_after_sync();
 #pragma unroll
-      for (int nbp = 0; nbp < 2; ++nbp) {
-        const int i = lane >> 3;  // (tokens +0-7 | +8-15) x (k lo | k hi)
-        const int r = 16 * nbp + (lane & 7) + 8 * (i >> 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + pf_chunk(kPfChunk, r, 2 * ks + (i & 1)), b0, b1, b2, b3);
-        mma_bf16(s[2 * nbp], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16(s[2 * nbp + 1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+          for (int k = 0; k < D / 16; ++k) {
+            const uint32_t off = (k >> 2) * (kPfRows * 128) + (k & 3) * 32;
+            const uint32_t koff = (k >> 2) * L::kSlab + (k & 3) * 32;
+            umma_bf16(tmem + (2 * t + (j & 1)) * kPfChunk,
+                      smem_desc_sw128(sq + t * L::kQ + off, 16, 1024),
+                      smem_desc_sw128(kb + koff, 16, 1024), kIdQK, k > 0);
+          }
+          umma_commit(smem_addr(&bars->s_full[t][j & 1]));
+        }
+        if (!ok) break;
+        umma_commit(smem_addr(&bars->k_empty[j % kPfKStages]));
+        if (j >= 2) ok = issue_pv(j - 2);
       }
-    // online softmax in log2 units; the running max moves (and O is
-    // rescaled) only when a score exceeds it by more than 8
-    const int32_t tok0 = (c0 + k) * kPfChunk;
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        s[nb][q] = tok0 + 8 * nb + 2 * tq + (q & 1) < p.prefix_tokens ? s[nb][q] * p.scale_log2
-                                                                        : -INFINITY;
-      mx0 = fmaxf(mx0, fmaxf(s[nb][0], s[nb][1]));
-      mx1 = fmaxf(mx1, fmaxf(s[nb][2], s[nb][3]));
+      for (int32_t i = n > 2 ? n - 2 : 0; i < n && ok; ++i) ok = issue_pv(i);
+      // every MMA this thread issued has completed before the tensor
+      // memory is released
+      umma_commit(smem_addr(&bars->mma_done));
+      mbar_wait(smem_addr(&bars->mma_done), 0, 1u << 16);
     }
-    if (__any_sync(0xffffffffu, mx0 > m[0] + 8.f || mx1 > m[1] + 8.f)) {
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      const float n0 = fmaxf(m[0], mx0), n1 = fmaxf(m[1], mx1);
-      const float a0 = fast_exp2(m[0] - n0), a1 = fast_exp2(m[1] - n1);
-      m[0] = n0;
-      m[1] = n1;
-      l[0] *= a0;
-      l[1] *= a1;
-#pragma unroll
-      for (int i = 0; i < D / 8; ++i) {
-        o[i][0] *= a0;
-        o[i][1] *= a0;
-        o[i][2] *= a1;
-        o[i][3] *= a1;
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------- softmax ---
+    const int tile = (warp - 2) >> 2;
+    const int quarter = warp & 3;  // tensor-memory lanes 32 * quarter ...
+    const int r = 32 * quarter + lane;  // row within the tile
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+    const uint32_t o_col = kPfTiles * 2 * kPfChunk + tile * D;
+    const uint32_t prow = sp + tile * L::kP + r * 128;  // this thread's P row
+    float m = -INFINITY, l = 0.f;
+    for (int32_t j = 0; j < n; ++j) {
+      ok = mbar_wait(smem_addr(&bars->s_full[tile][j & 1]), (j >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
       }
+      tc_fence_after_sync();
+      const uint32_t s_col = lane_base + (2 * tile + (j & 1)) * kPfChunk;
+      const int32_t valid = p.prefix_tokens - (c0 + j) * kPfChunk;  // tokens of the chunk
+      // pass 1: the chunk's max score (log2 units), 32 columns at a time;
+      // tokens past the prefix are masked after the scaling (-inf * 0 would
+      // be NaN)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int part = 0; part < kPfChunk / 32; ++part) {
+        uint32_t u[32];
+        tmem_ld32(s_col + part * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float x = __uint_as_float(u[i]) * p.scale_log2;
+          mx = fmaxf(mx, part * 32 + i < valid ? x : -INFINITY);
+        }
+      }
+      // the tile's previous product reads the P buffer and updates O_t: it
+      // must be complete before either is touched
+      if (j >= 1) {
+        ok = mbar_wait(smem_addr(&bars->o_done[tile]), (j - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+      }
+      if (j == 0) {
+        m = mx;
+      } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+        // the running max moves: O_t and l scale
+        const float mn = fmaxf(m, mx);
+        const float alpha = fast_exp2(m - mn);
+        m = mn;
+        l *= alpha;
+        tc_fence_after_sync();
+#pragma unroll 1
+        for (int part = 0; part < D / 32; ++part) {
+          uint32_t u[32];
+          const uint32_t ta = lane_base + o_col + part * 32;
+          tmem_ld32(ta, u);
+          tmem_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+          tmem_st32(ta, u);
+        }
+        tmem_wait_st();
+      }
+      // pass 2: P = 2^(s - m) rounded to bf16 into this row of the P tile,
+      // 32 columns (four 16-byte chunks) at a time
+      const float neg_m = -m;
+      float lsum = 0.f;
+#pragma unroll 1
+      for (int part = 0; part < kPfChunk / 32; ++part) {
+        uint32_t u[32];
+        tmem_ld32(s_col + part * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
+#pragma unroll
+          for (int h = 0; h < 4; ++h) {
+            const int i = 8 * c + 2 * h;
+            const float x0 = part * 32 + i < valid ? __uint_as_float(u[i]) * p.scale_log2 : -INFINITY;
+            const float x1 =
+                part * 32 + i + 1 < valid ? __uint_as_float(u[i + 1]) * p.scale_log2 : -INFINITY;
+            w[h] = pack_bf16x2(fast_exp2(x0 + neg_m), fast_exp2(x1 + neg_m));
+            const float2 f = unpack_bf16x2(w[h]);  // sum exactly the weights the MMA applies
+            lsum += f.x + f.y;
+          }
+          const int cc = part * 4 + c;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((cc ^ (r & 7)) << 4)),
+                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                       : "memory");
+        }
+      }
+      // both passes have read S: its buffer may take the scores two chunks on
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bars->s_empty[tile][j & 1]));
+      l += lsum;
+      fence_proxy_async_smem();  // the MMA (async proxy) reads P
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile]));
     }
-    // O += P V over the chunk's two 16-token halves; P rounded to bf16 as
-    // the A operand, and l sums the same rounded values
-    const uint32_t vb = kb + L::kKV;
-#pragma unroll
-    for (int kt = 0; kt < 2; ++kt) {
-      const uint32_t pa0 = pack_bf16x2(fast_exp2(s[2 * kt][0] - m[0]), fast_exp2(s[2 * kt][1] - m[0]));
-      const uint32_t pa1 = pack_bf16x2(fast_exp2(s[2 * kt][2] - m[1]), fast_exp2(s[2 * kt][3] - m[1]));
-      const uint32_t pa2 = pack_bf16x2(fast_exp2(s[2 * kt + 1][0] - m[0]), fast_exp2(s[2 * kt + 1][1] - m[0]));
-      const uint32_t pa3 = pack_bf16x2(fast_exp2(s[2 * kt + 1][2] - m[1]), fast_exp2(s[2 * kt + 1][3] - m[1]));
-      {
-        const float2 f0 = unpack_bf16x2(pa0), f1 = unpack_bf16x2(pa1);
-        const float2 f2 = unpack_bf16x2(pa2), f3 = unpack_bf16x2(pa3);
-        l[0] += (f0.x + f0.y) + (f2.x + f2.y);
-        l[1] += (f1.x + f1.y) + (f3.x + f3.y);
-      }
-#pragma unroll
-      for (int pp = 0; pp < D / 16; ++pp) {
-        const int i = lane >> 3;  // (tokens 0-7 | 8-15) x (d block 2pp | 2pp+1)
-        const int r = 16 * kt + (lane & 7) + 8 * (i & 1);
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vb + pf_chunk(kPfChunk, r, 2 * pp + (i >> 1)), v0, v1, v2, v3);
-        mma_bf16(o[2 * pp], pa0, pa1, pa2, pa3, v0, v1);
-        mma_bf16(o[2 * pp + 1], pa0, pa1, pa2, pa3, v2, v3);
-      }
-    }
-    __syncthreads();  // every warp is done with the stage before it is refilled
+    // every product of both tiles is complete (the staging below reuses the
+    // K and V rings that the other tile's last products may still read)
+    ok = mbar_wait(smem_addr(&bars->mma_done), 0) && ok;
+    ok = __all_sync(0xffffffffu, ok);
+    // (m, l) of each row into the (free) K ring
+    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] = make_float2(m, l);
   }
-  l[0] += __shfl_xor_sync(0xffffffffu, l[0], 1);
-  l[0] += __shfl_xor_sync(0xffffffffu, l[0], 2);
-  l[1] += __shfl_xor_sync(0xffffffffu, l[1], 1);
-  l[1] += __shfl_xor_sync(0xffffffffu, l[1], 2);
-  // ---- this split's partial of rows gq and gq + 8 of the warp
-  const int64_t stride = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
+  // ---- epilogue, one query tile at a time: its rows' partials (o
+  // unnormalised) are staged in the V ring (float rows of D, 16-byte chunk
+  // c of row r at chunk c ^ (r % (D/4))), then written to this split's slot
+  // with coalesced stores (softmax warp w rows w, w + 8, ...; lane l its
+  // 16-byte chunk).
+  constexpr int kCh = D / 4;
+  const uint32_t stage_addr = base + L::kOffV;
+  const int64_t slot = static_cast<int64_t>(split) * p.num_seqs * p.num_q_heads;
+  const bool soft = warp >= 2 && warp < kPfVWarp;
+  for (int t = 0; t < kPfTiles; ++t) {
+    if (soft && ((warp - 2) >> 2) == t && ok && n > 0) {
+      const int quarter = warp & 3, r = 32 * quarter + lane;
+      const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+      tc_fence_after_sync();
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int64_t gr = row0 + 16 * warp + gq + 8 * hr;
-    if (gr >= R) continue;
-    const int64_t b = gr / p.group, j = gr % p.group;
-    const int64_t hrow = split * stride + b * p.num_q_heads + g * p.group + j;
-    float* dst = p.pf_o + hrow * D;
+      for (int part = 0; part < D / 32; ++part) {
+        uint32_t u[32];
+        tmem_ld32(lane_base + kPfTiles * 2 * kPfChunk + t * D + part * 32, u);
+        tmem_wait_ld();
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i)
-      *reinterpret_cast<float2*>(dst + 8 * i + 2 * tq) = make_float2(o[i][2 * hr], o[i][2 * hr + 1]);
-    if (tq == 0) p.pf_ml[hrow] = make_float2(m[hr], l[hr]);
+        for (int i = 0; i < 8; ++i) {
+          const int c = part * 8 + i;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           stage_addr + (r * D + 4 * (c ^ (r & (kCh - 1)))) * 4),
+                       "r"(u[4 * i]), "r"(u[4 * i + 1]), "r"(u[4 * i + 2]), "r"(u[4 * i + 3])
+                       : "memory");
+        }
+      }
+      if (row0 + t * kPfRows + r < R) {
+        const float2 ml = reinterpret_cast<const float2*>(pf_smem + L::kOffK)[t * kPfRows + r];
+        p.pf_ml[slot + head_row(t * kPfRows + r)] = ml;
+      }
+    }
+    if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
+    if (soft && ok && n > 0) {
+      for (int rr = warp - 2; rr < kPfRows && row0 + t * kPfRows + rr < R; rr += kPfSoftWarps)
+        if (lane < kCh) {
+          float4 x;
+          asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                       : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                       : "r"(stage_addr + (rr * D + 4 * (lane ^ (rr & (kCh - 1)))) * 4)
+                       : "memory");
+          reinterpret_cast<float4*>(p.pf_o + (slot + head_row(t * kPfRows + rr)) * D)[lane] = x;
+        }
+    }
+    // the next tile is staged once every row of this one is out
+    if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kPfTmemCols);
   }
 }
 
 // Fold the S split partials of every (sequence, query head) row into the
 // split-0 slot: M = max m_s, o = sum 2^(m_s - M) o_s, l = sum 2^(m_s - M)
-// l_s.  One warp per row, lane l on columns 4l .. 4l+3 (and + 128 for
-// D > 128); each lane reads its own columns of split 0 before writing them.
+// l_s.  One thread per (row, 16-byte chunk of the row); its loads of all
+// splits are issued together (S <= kPfMaxSplits), and it reads split 0's
+// chunk before writing it.
 template <int D>
 __global__ void __launch_bounds__(256) prefix_merge_kernel(const PrefixParams p) {
   pdl_wait();
   pdl_trigger();
+  constexpr int kCh = D / 4;
   const int64_t rows = static_cast<int64_t>(p.num_seqs) * p.num_q_heads;
-  const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int64_t row = idx / kCh;
+  const int c = static_cast<int>(idx % kCh);
   if (row >= rows) return;
-  float M = -INFINITY;
-  for (int sp = 0; sp < p.splits; ++sp) M = fmaxf(M, p.pf_ml[sp * rows + row].x);
-  float den = 0.f;
-  float4 num[(D + 127) / 128];
+  float2 ml[kPfMaxSplits];
+  float4 x[kPfMaxSplits];
 #pragma unroll
-  for (int j = 0; j < (D + 127) / 128; ++j) num[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int sp = 0; sp < p.splits; ++sp) {
-    const float2 ml = p.pf_ml[sp * rows + row];
-    const float w = ml.x == -INFINITY ? 0.f : fast_exp2(ml.x - M);
-    den = fmaf(w, ml.y, den);
-#pragma unroll
-    for (int j = 0; j < (D + 127) / 128; ++j) {
-      const int d = 128 * j + 4 * lane;
-      if (d < D) {
-        const float4 x = *reinterpret_cast<const float4*>(p.pf_o + (sp * rows + row) * D + d);
-        num[j].x = fmaf(w, x.x, num[j].x);
-        num[j].y = fmaf(w, x.y, num[j].y);
-        num[j].z = fmaf(w, x.z, num[j].z);
-        num[j].w = fmaf(w, x.w, num[j].w);
-      }
+  for (int sp = 0; sp < kPfMaxSplits; ++sp)
+    if (sp < p.splits) {
+      ml[sp] = p.pf_ml[sp * rows + row];
+      x[sp] = reinterpret_cast<const float4*>(p.pf_o + (sp * rows + row) * D)[c];
     }
-  }
-  __syncwarp();  // every lane has read split 0's (m, l)
+  float M = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < (D + 127) / 128; ++j) {
-    const int d = 128 * j + 4 * lane;
-    if (d < D) *reinterpret_cast<float4*>(p.pf_o + row * D + d) = num[j];
-  }
-  if (lane == 0) p.pf_ml[row] = make_float2(M, den);
+  for (int sp = 0; sp < kPfMaxSplits; ++sp)
+    if (sp < p.splits) M = fmaxf(M, ml[sp].x);
+  float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll
+  for (int sp = 0; sp < kPfMaxSplits; ++sp)
+    if (sp < p.splits) {
+      const float w = fast_exp2(ml[sp].x - M);
+      den = fmaf(w, ml[sp].y, den);
+      num.x = fmaf(w, x[sp].x, num.x);
+      num.y = fmaf(w, x[sp].y, num.y);
+      num.z = fmaf(w, x[sp].z, num.z);
+      num.w = fmaf(w, x[sp].w, num.w);
+    }
+  reinterpret_cast<float4*>(p.pf_o + row * D)[c] = num;
+  // every thread of the row has read split 0's (m, l) before it changes:
+  // the row's kCh threads are consecutive, aligned lanes of one warp
+  __syncwarp(kCh == 32 ? 0xffffffffu : (((1u << kCh) - 1u) << (threadIdx.x & (32 - kCh))));
+  if (c == 0) p.pf_ml[row] = make_float2(M, den);
 }
 
 }  // namespace pa

@@ -618,23 +618,24 @@ struct CascadeArgs {
   int64_t stride;
 };
 
-// Token splits of the prefix pass: as many as one wave of CTAs allows (3
-// resident per SM), and enough that each split's block ids fit in shared
-// memory.
+// Token splits of the prefix pass: as many as one wave of CTAs (one per SM:
+// each holds ~210 KB of shared memory and the tensor memory) allows, at
+// least one chunk each, at most kPfMaxSplits (the merge holds them all in
+// registers).
 int32_t prefix_splits(int sms, int64_t num_seqs, int32_t group, int32_t num_kv_heads,
-                      int32_t block_size, int32_t prefix_len) {
+                      int32_t prefix_len) {
   const int64_t chunks = (prefix_len + kPfChunk - 1) / kPfChunk;
-  const int64_t ctas = (num_seqs * group + kPfRows - 1) / kPfRows * num_kv_heads;
-  int64_t s = 3LL * sms / ctas;
-  const int64_t per_split_max = static_cast<int64_t>(kPfMaxBlocks - 2) * block_size / kPfChunk;
-  const int64_t s_ids = (chunks + per_split_max - 1) / per_split_max;
-  if (s < s_ids) s = s_ids;
+  const int64_t ctas = (num_seqs * group + kPfTiles * kPfRows - 1) / (kPfTiles * kPfRows) *
+                       num_kv_heads;
+  int64_t s = static_cast<int64_t>(sms) / ctas;
   if (s > chunks) s = chunks;
+  if (s > kPfMaxSplits) s = kPfMaxSplits;
   if (s < 1) s = 1;
   return static_cast<int32_t>(s);
 }
 
-// Bytes of the prefix partials of a cascade, rounded up to 256.
+// Bytes of the prefix partials of a cascade (one per split and row; the
+// merge folds them into split 0's), rounded up to 256.
 size_t prefix_partial_bytes(int32_t splits, int64_t num_seqs, int32_t num_q_heads,
                             int32_t head_dim) {
   const size_t b = static_cast<size_t>(splits) * num_seqs * num_q_heads *
@@ -643,7 +644,8 @@ size_t prefix_partial_bytes(int32_t splits, int64_t num_seqs, int32_t num_q_head
 }
 
 template <int D>
-pa_status launch_prefix(const PrefixParams& pp, cudaStream_t stream) {
+pa_status launch_prefix(const PrefixParams& pp, const void* k_cache, const void* v_cache,
+                        cudaStream_t stream) {
   static bool attr_set[kMaxDevices] = {false};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
@@ -657,18 +659,26 @@ pa_status launch_prefix(const PrefixParams& pp, cudaStream_t stream) {
       attr_set[dev] = true;
     }
   }
-  const int64_t rows = static_cast<int64_t>(pp.num_seqs) * pp.group;
-  const int64_t bx = (rows + kPfRows - 1) / kPfRows;
-  if (bx > INT_MAX || pp.num_kv_heads > 65535 || pp.splits > 65535) return PA_ERR_UNSUPPORTED;
+  // K and V as 2D [rows][D] bf16, boxes of 64 columns x min(bs, 64) rows
+  const int box_rows = pp.block_size < kPfChunk ? pp.block_size : kPfChunk;
+  CUtensorMap tk, tv;
+  if (!encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k_cache, D, pp.rows_total, D * 2, 64,
+                 box_rows, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v_cache, D, pp.rows_total, D * 2, 64,
+                 box_rows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return PA_ERR_CUDA;
+  const int64_t bx = (static_cast<int64_t>(pp.num_seqs) * pp.group + kPfTiles * kPfRows - 1) /
+                     (kPfTiles * kPfRows);
+  if (bx > INT_MAX || pp.num_kv_heads > 65535 || pp.splits > kPfMaxSplits) return PA_ERR_UNSUPPORTED;
   if (launch_pdl(prefix_attention_kernel<D>,
                  dim3(static_cast<unsigned>(bx), static_cast<unsigned>(pp.num_kv_heads),
                       static_cast<unsigned>(pp.splits)),
-                 dim3(kPfWarps * 32), PfSmem<D>::kBytes, stream, pp) != cudaSuccess)
+                 dim3(kPfThreads), PfSmem<D>::kBytes, stream, tk, tv, pp) != cudaSuccess)
     return PA_ERR_CUDA;
   if (pp.splits == 1) return PA_OK;
   // one partial per row for the suffix pass
-  const int64_t warps = static_cast<int64_t>(pp.num_seqs) * pp.num_q_heads;
-  const int64_t mx = (warps * 32 + 255) / 256;
+  const int64_t threads = static_cast<int64_t>(pp.num_seqs) * pp.num_q_heads * (D / 4);
+  const int64_t mx = (threads + 255) / 256;
   if (mx > INT_MAX) return PA_ERR_UNSUPPORTED;
   return launch_pdl(prefix_merge_kernel<D>, dim3(static_cast<unsigned>(mx)), dim3(256), 0,
                     stream, pp) == cudaSuccess
@@ -823,7 +833,7 @@ extern "C" pa_status pa_decode_cascade_workspace_size(int32_t num_seqs, int32_t 
     const pa_status s2 = device_sms(&sms, nullptr);
     if (s2 != PA_OK) return s2;
     const int32_t sp = prefix_splits(sms, num_seqs, num_q_heads / num_kv_heads, num_kv_heads,
-                                     block_size, prefix_len);
+                                     prefix_len);
     pf = prefix_partial_bytes(sp, num_seqs, num_q_heads, head_dim);
   }
   *bytes = pf + dec;
@@ -863,7 +873,7 @@ extern "C" pa_status pa_decode_cascade(const void* q, const void* k_cache, const
   pa_status st = device_sms(&sms, nullptr);
   if (st != PA_OK) return st;
   const int32_t group = num_q_heads / num_kv_heads;
-  const int32_t sp = prefix_splits(sms, num_seqs, group, num_kv_heads, block_size, prefix_len);
+  const int32_t sp = prefix_splits(sms, num_seqs, group, num_kv_heads, prefix_len);
   const size_t pf = prefix_partial_bytes(sp, num_seqs, num_q_heads, head_dim);
   if (workspace_bytes < pf) return PA_ERR_WORKSPACE;
   CascadeArgs cas;
@@ -877,8 +887,6 @@ extern "C" pa_status pa_decode_cascade(const void* q, const void* k_cache, const
   PrefixParams pp;
   std::memset(&pp, 0, sizeof(pp));
   pp.q = static_cast<const uint8_t*>(q);
-  pp.k_cache = static_cast<const uint8_t*>(k_cache);
-  pp.v_cache = static_cast<const uint8_t*>(v_cache);
   pp.prefix_table = block_tables;  // sequence 0's row
   pp.pf_o = cas.pf_o;
   pp.pf_ml = cas.pf_ml;
@@ -889,12 +897,14 @@ extern "C" pa_status pa_decode_cascade(const void* q, const void* k_cache, const
   pp.block_size = block_size;
   pp.log2_bs = ilog2(block_size);
   pp.num_blocks = num_blocks;
+  pp.rows_total = num_blocks * num_kv_heads * block_size;
   pp.prefix_tokens = prefix_len;
   pp.prefix_chunks = (prefix_len + kPfChunk - 1) / kPfChunk;
   pp.splits = sp;
   pp.scale_log2 = scale * 1.4426950408889634f;
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = head_dim == 128 ? launch_prefix<128>(pp, s) : launch_prefix<64>(pp, s);
+  st = head_dim == 128 ? launch_prefix<128>(pp, k_cache, v_cache, s)
+                       : launch_prefix<64>(pp, k_cache, v_cache, s);
   if (st != PA_OK) return st;
   return decode_entry(q, k_cache, v_cache, nullptr, nullptr, PA_KV_BF16, block_tables,
                       max_blocks_per_seq, seq_lens, num_seqs, num_q_heads, num_kv_heads,

@@ -103,3 +103,19 @@ def test_cascade_head_dim_64_and_sequences_at_the_prefix():
     out = _cascade(case, 64, lens=torch.tensor(lens, dtype=torch.int32, device="cuda"))
     assert pa.pa_get_device_error() & pa.DEVERR_BAD_SEQ_LEN
     assert torch.all(out[3] == 0)
+
+
+@pytest.mark.parametrize("bs", [64, 256])
+def test_cascade_large_blocks(bs):
+    # blocks larger than a prefix chunk (256: two chunks per block, read at
+    # an offset inside it) and at half a chunk (64)
+    case = build_case(W.shared_prefix(bs, num_seqs=40, prefix=512))
+    w = case.w
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
+    pa.pa_cache_write(case.k_new, case.v_new, case.slots_t, case.k_cache, case.v_cache)
+    ref = oracle_decode(case, snap, seqs)
+    for prefix_len in (512, 256):
+        if prefix_len % bs == 0:
+            assert_close(_cascade(case, prefix_len), ref, TOL, f"cascade bs{bs} prefix {prefix_len}")
+    assert pa.pa_get_device_error() == 0
