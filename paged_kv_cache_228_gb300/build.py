@@ -44,6 +44,7 @@ def _stale() -> bool:
         return True
     t = os.path.getmtime(LIB)
     files = [os.path.join(CSRC, f) for f in DEPS] + [os.path.join(INCLUDE, "pa.h"),
+                                                      os.path.join(INCLUDE, "pa_testing.h"),
                                                       os.path.abspath(__file__)]
     return any(os.path.getmtime(f) > t for f in files)
 

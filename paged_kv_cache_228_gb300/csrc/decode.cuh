@@ -85,6 +85,11 @@ struct DecodeParams {
   int32_t num_ctas;    // P
   int32_t seg_cost;    // work split: units charged per segment (a tile is kUnit)
   int32_t stages;      // ring depth
+  // Bounded waits: polls before a pipeline wait gives up (PA_DEVERR_TIMEOUT).
+  // stall != 0 (a test hook) makes the math warp first wait on a barrier
+  // nothing arrives at, so the timeout path runs deterministically.
+  uint32_t wait_limit;
+  int32_t stall;
 };
 
 // ------------------------------------------------ shared memory layout ---
@@ -112,6 +117,7 @@ struct Header {
   uint64_t empty[kMaxStages];  // stage read (two-warp CTAs)
   uint64_t qfull[kQSlots];     // query slot landed
   uint64_t qempty[kQSlots];    // query slot read (two-warp CTAs)
+  uint64_t stall;              // never arrived at (the stall test hook waits on it)
   float4 scales[kMaxStages];  // FP8: (k_scale row g, k_scale row g+8, v_scale ...)
 };
 
@@ -690,9 +696,10 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const Maps& tm, c
   while (ld.u < hi) {
     if (lane == 0) {
       if (ld.fresh && ld.qn >= kQSlots)
-        ok = mbar_wait(smem_addr(&sb.hdr->qempty[ld.qn % kQSlots]), (ld.qn / kQSlots - 1) & 1);
+        ok = mbar_wait(smem_addr(&sb.hdr->qempty[ld.qn % kQSlots]), (ld.qn / kQSlots - 1) & 1,
+                       p.wait_limit);
       if (ok && ld.it >= S)
-        ok = mbar_wait(smem_addr(&sb.hdr->empty[ld.it % S]), (ld.it / S - 1) & 1);
+        ok = mbar_wait(smem_addr(&sb.hdr->empty[ld.it % S]), (ld.it / S - 1) & 1, p.wait_limit);
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     issue_tile<D, FP8>(p, tm, sb, ld, hi);
@@ -1123,12 +1130,16 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
   uint32_t qb[D / 16][2];
   float hm0, hm1;
   if (kFused) top_up<D, FP8, kAppend>(p, tm, sb, ld, hi, used, qread);
+  if (p.stall) {  // test hook: a wait that can only run out
+    ok = mbar_wait(smem_addr(&hdr->stall), 0, p.wait_limit);
+    ok = __all_sync(0xffffffffu, ok);
+  }
   while (u < hi && ok) {
     const int32_t seg_end = static_cast<int32_t>(
         min(static_cast<int64_t>(c.T), c.tile + (hi - u)));
     const bool whole = c.tile == 0 && seg_end == c.T;
     const uint32_t qs = qread % kQSlots;
-    ok = mbar_wait(smem_addr(&hdr->qfull[qs]), (qread / kQSlots) & 1);
+    ok = mbar_wait(smem_addr(&hdr->qfull[qs]), (qread / kQSlots) & 1, p.wait_limit);
     ok = __all_sync(0xffffffffu, ok);
     if (!ok) break;
     load_query<D, FP8>(p, sb.q + qs * L::kQBytes, qb, hm0, hm1);
@@ -1142,7 +1153,7 @@ __device__ __forceinline__ void run_math(const DecodeParams& p, const Maps& tm, 
     seg_reset(s);
     for (int32_t tile = c.tile; tile < seg_end; ++tile) {
       const uint32_t stage = used % p.stages;
-      ok = mbar_wait(smem_addr(&hdr->full[stage]), (used / p.stages) & 1);
+      ok = mbar_wait(smem_addr(&hdr->full[stage]), (used / p.stages) & 1, p.wait_limit);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       const uint32_t kb = sb.ring + stage * L::kStageBytes;
@@ -1250,6 +1261,7 @@ __global__ void __launch_bounds__(64, 8)
       mbar_init(smem_addr(&sb.hdr->qfull[st]), 1);
       mbar_init(smem_addr(&sb.hdr->qempty[st]), 1);
     }
+    mbar_init(smem_addr(&sb.hdr->stall), 1);
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -1287,6 +1299,7 @@ __global__ void __launch_bounds__(32, 16)
   if (lane == 0) {
     for (int st = 0; st < p.stages; ++st) mbar_init(smem_addr(&sb.hdr->full[st]), 1);
     for (int st = 0; st < kQSlots; ++st) mbar_init(smem_addr(&sb.hdr->qfull[st]), 1);
+    mbar_init(smem_addr(&sb.hdr->stall), 1);
     mbar_fence_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -1359,31 +1372,54 @@ __global__ void __launch_bounds__(kMaxG * D / 4, 1)
   const float2* ml = p.ws_ml + first * kMaxG + h;
   const float4* o = reinterpret_cast<const float4*>(p.ws_o + (first * kMaxG + h) * D + d4);
   constexpr int kOStride = kMaxG * D / 4;  // float4s per piece
+  // (m, l) and rows of up to kBatch pieces are loaded together, so a job
+  // costs one round trip after its job word rather than two
+  constexpr int kBatch = 8;
+  float2 v[kBatch];
+  float4 x[kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+    if (k < np) {
+      v[k] = ml[k * kMaxG];
+      x[k] = o[k * kOStride];
+    }
   float M = -INFINITY;
-#pragma unroll 8
-  for (int k = 0; k < np; ++k) M = fmaxf(M, ml[k * kMaxG].x);
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+    if (k < np) M = fmaxf(M, v[k].x);
+  for (int k = kBatch; k < np; ++k) M = fmaxf(M, ml[k * kMaxG].x);
   float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
   if (p.pf_o != nullptr) {
     // cascade: the prefix partial is one more piece
     const int64_t row = static_cast<int64_t>(b) * p.num_q_heads + g * p.group + h;
     const float2 pml = p.pf_ml[row];
-    const float4 x = *reinterpret_cast<const float4*>(p.pf_o + row * D + d4);
+    const float4 y = *reinterpret_cast<const float4*>(p.pf_o + row * D + d4);
     M = fmaxf(M, pml.x);
     const float w = fast_exp2(pml.x - M);
-    num = make_float4(w * x.x, w * x.y, w * x.z, w * x.w);
+    num = make_float4(w * y.x, w * y.y, w * y.z, w * y.w);
     den = w * pml.y;
   }
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k)
+    if (k < np) {
+      const float w = fast_exp2(v[k].x - M);
+      num.x = fmaf(w, x[k].x, num.x);
+      num.y = fmaf(w, x[k].y, num.y);
+      num.z = fmaf(w, x[k].z, num.z);
+      num.w = fmaf(w, x[k].w, num.w);
+      den = fmaf(w, v[k].y, den);
+    }
 #pragma unroll 4
-  for (int k = 0; k < np; ++k) {
-    const float2 v = ml[k * kMaxG];
-    const float4 x = o[k * kOStride];
-    const float w = fast_exp2(v.x - M);
-    num.x = fmaf(w, x.x, num.x);
-    num.y = fmaf(w, x.y, num.y);
-    num.z = fmaf(w, x.z, num.z);
-    num.w = fmaf(w, x.w, num.w);
-    den = fmaf(w, v.y, den);
+  for (int k = kBatch; k < np; ++k) {
+    const float2 vv = ml[k * kMaxG];
+    const float4 xx = o[k * kOStride];
+    const float w = fast_exp2(vv.x - M);
+    num.x = fmaf(w, xx.x, num.x);
+    num.y = fmaf(w, xx.y, num.y);
+    num.z = fmaf(w, xx.z, num.z);
+    num.w = fmaf(w, xx.w, num.w);
+    den = fmaf(w, vv.y, den);
   }
   uint2 r;
   r.x = pack_bf16x2(num.x / den, num.y / den);

@@ -9,6 +9,7 @@
 
 #include <nvtx3/nvToolsExt.h>
 
+#include <atomic>
 #include <climits>
 #include <cstdint>
 #include <cstring>
@@ -19,6 +20,7 @@
 #include "decode.cuh"
 #include "nvfp4.cuh"
 #include "pa.h"
+#include "pa_testing.h"
 
 namespace pa {
 
@@ -55,6 +57,12 @@ struct DeviceInfo {
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mu;
+
+// Polls before a decode kernel's pipeline wait gives up, and the stall test
+// hook (pa_testing_set_wait_limit).
+constexpr uint32_t kDefaultWaitLimit = 1u << 22;
+std::atomic<uint32_t> g_wait_limit{kDefaultWaitLimit};
+std::atomic<int32_t> g_wait_stall{0};
 
 pa_status device_sms(int* sms, int* dev_out) {
   int dev = 0;
@@ -247,6 +255,8 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
   prm.num_ctas = P;
   prm.seg_cost = FP8 ? kSegCostFp8 : kSegCostBf16;
   prm.stages = stages;
+  prm.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  prm.stall = g_wait_stall.load(std::memory_order_relaxed);
   prm.ws_o = nullptr;
   prm.ws_ml = nullptr;
   prm.ws_job = nullptr;
@@ -310,6 +320,18 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
 using namespace pa;
 
 extern "C" int32_t pa_abi_version(void) { return 1; }
+
+extern "C" pa_status pa_testing_set_wait_limit(uint32_t polls, int32_t stall) {
+  if (polls == 0) {
+    pa::g_wait_limit.store(pa::kDefaultWaitLimit);
+    pa::g_wait_stall.store(0);
+    return PA_OK;
+  }
+  if (stall != 0 && stall != 1) return PA_ERR_INVALID_ARG;
+  pa::g_wait_limit.store(polls);
+  pa::g_wait_stall.store(stall);
+  return PA_OK;
+}
 
 extern "C" const char* pa_status_string(pa_status s) {
   switch (s) {
@@ -990,6 +1012,8 @@ pa_status launch_fp4_decode(const DecodeParams& prm_in, const Fp4Args& f, void* 
   DecodeParams prm = prm_in;
   prm.num_ctas = P;
   prm.seg_cost = kSegCostFp4;
+  prm.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  prm.stall = g_wait_stall.load(std::memory_order_relaxed);
   prm.ws_o = nullptr;
   prm.ws_ml = nullptr;
   prm.ws_job = nullptr;

@@ -44,6 +44,7 @@ _c_size = ctypes.c_size_t
 # name -> (restype, argtypes); must match include/pa.h
 SIGNATURES = {
     "pa_abi_version": (_c_int, []),
+    "pa_testing_set_wait_limit": (_c_int, [ctypes.c_uint32, _c_int]),
     "pa_status_string": (ctypes.c_char_p, [_c_int]),
     "pa_get_device_error": (_c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "pa_cache_write": (_c_int, [_c_ptr, _c_ptr, _c_ptr, _c_int, _c_ptr, _c_ptr, _c_int,
@@ -254,6 +255,13 @@ def pa_quantize_fp8(k_src, v_src, block_ids, valid_lens, k_dst, v_dst, k_scale,
 
 
 # ---------------------------------------------------------------- decode ---
+def pa_testing_set_wait_limit(polls: int, stall: bool = False):
+    """Test hook (include/pa_testing.h): polls before a decode pipeline wait
+    gives up (0 restores the default and clears stall); stall=True makes
+    every decode CTA first wait on a barrier nothing arrives at."""
+    _check("pa_testing_set_wait_limit", lib().pa_testing_set_wait_limit(polls, int(stall)))
+
+
 def pa_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim,
                              num_splits=0) -> int:
     n = ctypes.c_size_t(0)

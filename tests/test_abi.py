@@ -1,5 +1,5 @@
 """The C ABI library builds, loads without a GPU, and exports every entry
-point ``include/pa.h`` declares; the Python binding declares each with the
+point ``include/pa.h`` and ``include/pa_testing.h`` declare; the Python binding declares each with the
 header's argument count.  The native block manager matches the oracle's
 model op for op (statuses, ids, slots, copy requests, refcounts)."""
 import os
@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "pa.h")
+HEADERS = [os.path.join(ROOT, "include", f) for f in ("pa.h", "pa_testing.h")]
 
 
 @pytest.fixture(scope="session")
@@ -20,7 +20,7 @@ def palib():
 
 
 def _declared():
-    text = open(HEADER).read()
+    text = "\n".join(open(h).read() for h in HEADERS)
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     decls = {}
     for m in re.finditer(r"\b(pa_\w+)\s*\(([^;{]*?)\)\s*;", text, flags=re.S):
@@ -245,3 +245,12 @@ def test_allocator_usage_matches_model(palib, name):
     m, tm, lm = BM.replay_script(ops, w.num_seqs, w.block_size, maxb, w.pool_blocks)
     a, ta, la = palib.replay_script(ops, w.num_seqs, w.block_size, maxb, w.pool_blocks)
     assert palib.allocator_usage(a, ta, la, w.block_size) == BM.usage(m, tm, lm, w.block_size)
+
+
+def test_wait_limit_hook_validates_on_the_host(palib):
+    # The bounded-wait test hook (include/pa_testing.h): host-side settings
+    # only, no CUDA call; 0 polls restores the default.
+    L = palib.lib()
+    assert L.pa_testing_set_wait_limit(100, 2) == palib.PA_ERR_INVALID_ARG
+    assert L.pa_testing_set_wait_limit(100, 1) == palib.PA_OK
+    assert L.pa_testing_set_wait_limit(0, 1) == palib.PA_OK
