@@ -386,6 +386,11 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
         if ev is not None:
             ev[1].record(stream)
 
+    # nvidia-smi samples clocks from before the warm-up to after the timed
+    # region, so that no idle gap precedes the timed steps
+    sampler = sample_clocks() if sample_clocks else None
+    if sampler:
+        time.sleep(0.3)  # let nvidia-smi start sampling
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize()
@@ -396,16 +401,11 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     if torch.distributed.is_initialized():
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler = sample_clocks() if sample_clocks else None
-    if sampler:
-        time.sleep(0.3)  # let nvidia-smi start sampling
     t_start.record(stream)
     for i in range(steps):
         step(i, evs[i])
     t_end.record(stream)
     torch.cuda.synchronize()
-    if sampler:
-        sampler.stop()
     if torch.distributed.is_initialized():
         torch.distributed.barrier()
     total_ms = t_start.elapsed_time(t_end)
@@ -414,18 +414,18 @@ def run_native(w, steps, warmup, device, fp8=False, n_pools=None, sample_clocks=
     if err:
         raise RuntimeError(f"device error word 0x{err:x} during the benchmark")
     if profile_only:
+        if sampler:
+            sampler.stop()
         return {"ms_per_step": total_ms / steps, "decode_ms_mean": statistics.mean(dec_ms)}
 
     # The headline timed region: exactly `steps` steps launched back to back
     # on one stream with no event between them, so that each step's
     # programmatic dependent launches overlap its start with the previous
-    # step's tail, as consecutive calls do in use.
+    # step's tail, as consecutive calls do in use.  It follows the loop
+    # above directly (the GPU does not idle in between).
     if torch.distributed.is_initialized():
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    sampler = sample_clocks() if sample_clocks else None
-    if sampler:
-        time.sleep(0.3)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     a.record(stream)

@@ -5,7 +5,7 @@
  *
  * Every pipeline wait inside the bf16 and FP8 decode kernels (a consumer
  * waiting for a copy to land, a producer waiting for a stage to be freed)
- * is bounded: after a fixed number of polls it gives up, sets
+ * is bounded: after a number of polls it gives up, sets
  * PA_DEVERR_TIMEOUT in the device error word, lets the CTA's own copies in
  * flight land (those waits keep their own bound), and returns.  A correct
  * pipeline never comes near the bound, so tests need a way to make a wait
@@ -25,8 +25,10 @@ extern "C" {
 /* pa_testing_set_wait_limit -- process-wide; applies to decode calls
  * (pa_decode, pa_decode_append, pa_decode_append_fp8, pa_decode_cascade's
  * suffix pass, pa_decode_noalloc) launched after it returns.
- *   polls  polls before a pipeline wait gives up; 0 restores the default
- *          (2^22) and clears `stall`
+ *   polls  polls before a wait of the math warp (the only warp of an FP8
+ *          CTA) gives up; 0 restores the default (2^22) and clears
+ *          `stall`.  The copy warp of a bf16 CTA always uses the default,
+ *          so after a stalled math warp it gives up later.
  *   stall  1: the math warp of every decode CTA first waits on a barrier
  *          that nothing arrives at, with the limit above, so that wait runs
  *          out deterministically: the CTA sets PA_DEVERR_TIMEOUT, drains its

@@ -85,9 +85,11 @@ struct DecodeParams {
   int32_t num_ctas;    // P
   int32_t seg_cost;    // work split: units charged per segment (a tile is kUnit)
   int32_t stages;      // ring depth
-  // Bounded waits: polls before a pipeline wait gives up (PA_DEVERR_TIMEOUT).
-  // stall != 0 (a test hook) makes the math warp first wait on a barrier
-  // nothing arrives at, so the timeout path runs deterministically.
+  // Bounded waits: polls before a math-warp wait gives up (PA_DEVERR_TIMEOUT;
+  // the copy warp's waits keep the fixed default bound: a run-time bound
+  // there slowed the block-size-8 decode by 47%, measured).  stall != 0 (a
+  // test hook) makes the math warp first wait on a barrier nothing arrives
+  // at, so the timeout path runs deterministically.
   uint32_t wait_limit;
   int32_t stall;
 };
@@ -696,10 +698,9 @@ __device__ __forceinline__ void produce(const DecodeParams& p, const Maps& tm, c
   while (ld.u < hi) {
     if (lane == 0) {
       if (ld.fresh && ld.qn >= kQSlots)
-        ok = mbar_wait(smem_addr(&sb.hdr->qempty[ld.qn % kQSlots]), (ld.qn / kQSlots - 1) & 1,
-                       p.wait_limit);
+        ok = mbar_wait(smem_addr(&sb.hdr->qempty[ld.qn % kQSlots]), (ld.qn / kQSlots - 1) & 1);
       if (ok && ld.it >= S)
-        ok = mbar_wait(smem_addr(&sb.hdr->empty[ld.it % S]), (ld.it / S - 1) & 1, p.wait_limit);
+        ok = mbar_wait(smem_addr(&sb.hdr->empty[ld.it % S]), (ld.it / S - 1) & 1);
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     issue_tile<D, FP8>(p, tm, sb, ld, hi);
