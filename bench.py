@@ -80,9 +80,16 @@ def peaks():
 
 
 def kernel_source_hash():
+    """Hash of every kernel and launch source (csrc/*, include/*.h): a DRAM
+    traffic figure counts only while it was captured on these sources."""
     h = hashlib.sha256()
-    for f in ("decode.cuh", "pa_device.cuh", "libpa.cu"):
-        h.update(open(os.path.join(ROOT, "paged_kv_cache_228_gb300", "csrc", f), "rb").read())
+    csrc = os.path.join(ROOT, "paged_kv_cache_228_gb300", "csrc")
+    inc = os.path.join(ROOT, "include")
+    for d in (csrc, inc):
+        for f in sorted(os.listdir(d)):
+            if f.endswith((".cu", ".cuh", ".cpp", ".h")):
+                h.update(f.encode())
+                h.update(open(os.path.join(d, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -283,7 +290,7 @@ def block_size_sweep(args, device, peak):
                 "unique_GB_per_s": unique / dec_s / 1e9,
                 "unique_frac_of_measured_hbm": unique / dec_s / 1e9 / peak,
                 "paged_waste": frag["paged_waste"],
-                "dram_bytes_per_launch": ncu_traffic(wl.name + ("_cascade" if casc else "")),
+                "dram_bytes_per_step": ncu_traffic(wl.name + ("_cascade" if casc else "")),
                 "call": "pa_decode_cascade (the prefix's attention once for all sequences, "
                         "suffixes paged), after pa_cache_write" if casc else "pa_decode_append "
                         "(every sequence walks the shared prefix blocks through its own "
