@@ -20,7 +20,7 @@
 // head and one of S token ranges of the prefix, walked in 64-token chunks.
 // Eleven warps:
 //   warps 0/10 TMA producers of K and of V (one 2D box per block and
-//              64-column slab) into a 3-stage K ring and a 4-stage V ring;
+//              64-column slab) into 3-stage K and V rings;
 //   warp 1     owns the tensor memory; lane 0 issues the MMAs, for each
 //              query tile t:
 //                S_t   = Q_t . K_j^T                 (A, B K-major; N = 64)
@@ -32,9 +32,9 @@
 //              warp's quarter of the tensor-memory lanes): online softmax in
 //              fp32 -- the running max moves, and O_t in tensor memory is
 //              rescaled, only when a score exceeds it by more than 8 in
-//              log2 units -- P rounded to bf16 into the tile's shared P
-//              buffer (rewritten once the previous product of the tile is
-//              done), and l sums those rounded weights.
+//              log2 units -- P rounded to bf16 into one of the tile's two
+//              shared P buffers (so softmax need not wait for the previous
+//              chunk's product), and l sums those rounded weights.
 // Each split writes its own partial per row (staged through shared memory
 // so the global stores are coalesced); prefix_merge_kernel folds the S of
 // them together.
@@ -62,7 +62,7 @@ constexpr int kPfRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kPfTiles = 2;     // query tiles per CTA sharing each K/V chunk
 constexpr int kPfChunk = 64;    // prefix tokens per chunk
 constexpr int kPfKStages = 3;   // K ring depth
-constexpr int kPfVStages = 4;   // V ring depth (V waits a whole softmax longer)
+constexpr int kPfVStages = 3;   // V ring depth
 constexpr int kPfSoftWarps = 4 * kPfTiles;
 constexpr int kPfThreads = 96 + 32 * kPfSoftWarps;  // K and V producers, MMA, softmax
 constexpr int kPfVWarp = 2 + kPfSoftWarps;
@@ -78,11 +78,11 @@ struct PfSmem {
   static constexpr int kOffK = kPfTiles * kQ;
   static constexpr int kOffV = kOffK + kPfKStages * kKV;
   static constexpr int kOffP = kOffV + kPfVStages * kKV;
-  static constexpr int kOffBar = kOffP + kPfTiles * kP;
+  static constexpr int kOffBar = kOffP + 2 * kPfTiles * kP;  // P double-buffered per tile
   static constexpr int kBytes = kOffBar + 256;
-  // the epilogue stages one tile's partial in the (free) V ring, and the
+  // the epilogue stages one tile's partial in the (free) P buffers, and the
   // per-row (m, l) in the (free) K ring
-  static_assert(kPfRows * D * 4 <= kPfVStages * kKV, "epilogue staging");
+  static_assert(kPfRows * D * 4 <= 2 * kPfTiles * kP, "epilogue staging");
   static_assert(kPfTiles * kPfRows * 8 <= kPfKStages * kKV, "epilogue (m, l)");
   static_assert(kP == kPfRows * 128, "P is one slab");
 };
@@ -91,8 +91,8 @@ struct PfBars {
   uint64_t k_full[kPfKStages], k_empty[kPfKStages];
   uint64_t v_full[kPfVStages], v_empty[kPfVStages];
   uint64_t s_full[kPfTiles][2], s_empty[kPfTiles][2];
-  uint64_t p_full[kPfTiles];  // P of the tile's current chunk written
-  uint64_t o_done[kPfTiles];  // the tile's product with that P complete
+  uint64_t p_full[kPfTiles][2];  // P of a chunk written, per tile and P buffer
+  uint64_t o_done[kPfTiles][2];  // the tile's product with that P complete
   uint64_t mma_done;
   uint32_t tmem;
 };
@@ -183,8 +183,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         mbar_init(smem_addr(&bars->s_full[t][i]), 1);
         mbar_init(smem_addr(&bars->s_empty[t][i]), 4);
       }
-      mbar_init(smem_addr(&bars->p_full[t]), 4);
-      mbar_init(smem_addr(&bars->o_done[t]), 1);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(smem_addr(&bars->p_full[t][i]), 4);
+        mbar_init(smem_addr(&bars->o_done[t][i]), 1);
+      }
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
     mbar_fence_init();
@@ -266,14 +268,14 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         if (!mbar_wait(smem_addr(&bars->v_full[vs]), (i / kPfVStages) & 1)) return false;
         const uint32_t vb = sv + vs * L::kKV;
         for (int t = 0; t < kPfTiles; ++t) {
-          if (!mbar_wait(smem_addr(&bars->p_full[t]), i & 1)) return false;
+          if (!mbar_wait(smem_addr(&bars->p_full[t][i & 1]), (i >> 1) & 1)) return false;
           tc_fence_after_sync();
+          const uint32_t pb = sp + (2 * t + (i & 1)) * L::kP;
 #pragma unroll
           for (int k = 0; k < kPfChunk / 16; ++k)
-            umma_bf16(tmem + kPfTiles * 2 * kPfChunk + t * D,
-                      smem_desc_sw128(sp + t * L::kP + k * 32, 16, 1024),
+            umma_bf16(tmem + kPfTiles * 2 * kPfChunk + t * D, smem_desc_sw128(pb + k * 32, 16, 1024),
                       smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV, i > 0 || k > 0);
-          umma_commit(smem_addr(&bars->o_done[t]));
+          umma_commit(smem_addr(&bars->o_done[t][i & 1]));
         }
         umma_commit(smem_addr(&bars->v_empty[vs]));
         return true;
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int r = 32 * quarter + lane;  // row within the tile
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
     const uint32_t o_col = kPfTiles * 2 * kPfChunk + tile * D;
-    const uint32_t prow = sp + tile * L::kP + r * 128;  // this thread's P row
+    const uint32_t prow0 = sp + 2 * tile * L::kP + r * 128;  // this thread's P row, buffer 0
     float m = -INFINITY, l = 0.f;
     for (int32_t j = 0; j < n; ++j) {
       ok = mbar_wait(smem_addr(&bars->s_full[tile][j & 1]), (j >> 1) & 1);
@@ -339,10 +341,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           mx = fmaxf(mx, part * 32 + i < valid ? x : -INFINITY);
         }
       }
-      // the tile's previous product reads the P buffer and updates O_t: it
-      // must be complete before either is touched
-      if (j >= 1) {
-        ok = mbar_wait(smem_addr(&bars->o_done[tile]), (j - 1) & 1);
+      // P_j goes to buffer j & 1, which the tile's product of chunk j - 2
+      // reads: that product must be complete
+      if (j >= 2) {
+        ok = mbar_wait(smem_addr(&bars->o_done[tile][j & 1]), ((j - 2) >> 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
@@ -351,11 +353,17 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (j == 0) {
         m = mx;
       } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
-        // the running max moves: O_t and l scale
+        // the running max moves: O_t and l scale, once the tile's product
+        // of chunk j - 1 has updated O_t
         const float mn = fmaxf(m, mx);
         const float alpha = fast_exp2(m - mn);
         m = mn;
         l *= alpha;
+        ok = mbar_wait(smem_addr(&bars->o_done[tile][(j - 1) & 1]), ((j - 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
         tc_fence_after_sync();
 #pragma unroll 1
         for (int part = 0; part < D / 32; ++part) {
@@ -392,7 +400,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             lsum += f.x + f.y;
           }
           const int cc = part * 4 + c;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(prow + ((cc ^ (r & 7)) << 4)),
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           prow0 + (j & 1) * L::kP + ((cc ^ (r & 7)) << 4)),
                        "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
                        : "memory");
         }
@@ -405,7 +414,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       fence_proxy_async_smem();  // the MMA (async proxy) reads P
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile]));
+      if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile][j & 1]));
     }
     // every product of both tiles is complete (the staging below reuses the
     // K and V rings that the other tile's last products may still read)
@@ -415,12 +424,12 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] = make_float2(m, l);
   }
   // ---- epilogue, one query tile at a time: its rows' partials (o
-  // unnormalised) are staged in the V ring (float rows of D, 16-byte chunk
+  // unnormalised) are staged in the P buffers (float rows of D, 16-byte chunk
   // c of row r at chunk c ^ (r % (D/4))), then written to this split's slot
   // with coalesced stores (softmax warp w rows w, w + 8, ...; lane l its
   // 16-byte chunk).
   constexpr int kCh = D / 4;
-  const uint32_t stage_addr = base + L::kOffV;
+  const uint32_t stage_addr = base + L::kOffP;
   const int64_t slot = static_cast<int64_t>(split) * p.num_seqs * p.num_q_heads;
   const bool soft = warp >= 2 && warp < kPfVWarp;
   for (int t = 0; t < kPfTiles; ++t) {
