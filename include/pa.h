@@ -242,7 +242,10 @@ pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  *     s_t    = scale * <q[b][h], K_b[t]>,           0 <= t < n
  *     out[b][h] = sum_t softmax(s)_t * V_b[t]       (bf16 result)
  * with fp32 accumulation throughout.  FP8 caches dequantise as
- * decode(code) * k_scale[block][g] (likewise V).  A sequence with n == 0
+ * decode(code) * k_scale[block][g] (likewise V); the query and the softmax
+ * weights meet the E4M3 codes on the tensor cores as two-term E4M3 splits
+ * (hi + lo / 16, within about 2^-8 of each value relative to its row's
+ * largest), with fp32 products and sums.  A sequence with n == 0
  * yields zeros.  Long contexts are split over up to `num_splits` persistent
  * work partitions (0 = automatic) whose partial results are merged with a
  * log-sum-exp reduction; the split points depend only on seq_lens, so the
@@ -303,12 +306,16 @@ pa_status pa_decode_append(const void* q, const void* k_new, const void* v_new,
  * cache (codes and scales) and output as
  *     pa_cache_write_fp8(k_new, v_new, slot_mapping, num_seqs, ...);
  *     pa_decode(q, k_cache, v_cache, k_scale, v_scale, PA_KV_FP8_E4M3, ...);
- * bit for bit.  The CTA that copies sequence b's last tile first quantises
- * the new row into its block (growing the block's scale and requantising
- * its earlier rows when needed), which is exact only when that tile holds
- * the whole block: block_size must be 8 or 16 (else PA_ERR_UNSUPPORTED).
- * k_scale / v_scale are read and updated.  Other arguments and
- * requirements as pa_decode_append. */
+ * bit for bit.  head_dim 64: the CTA that copies sequence b's last tile
+ * first quantises the new row into its block (growing the block's scale
+ * and requantising its earlier rows when needed), which is exact only when
+ * that tile holds the whole block.  head_dim 128: two launches on `stream`,
+ * the FP8 cache write (with the slot check below) and then pa_decode's
+ * tensor-core kernel.  block_size must be 8 or 16 (else
+ * PA_ERR_UNSUPPORTED).  k_scale / v_scale are read and updated.  Other
+ * arguments and requirements as pa_decode_append, including its slot check:
+ * a slot that is not the one of position seq_lens[b] - 1 is not written and
+ * flags PA_DEVERR_BAD_SLOT. */
 pa_status pa_decode_append_fp8(const void* q, const void* k_new, const void* v_new,
                                const int64_t* slot_mapping, void* k_cache,
                                void* v_cache, float* k_scale, float* v_scale,

@@ -28,8 +28,8 @@ NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "-Xcompiler", "-Wall", f"-I{INCLUDE}", f"-I{CSRC}"]
 
 SOURCES = ["libpa.cu", "block_manager.cpp"]
-DEPS = ["libpa.cu", "block_manager.cpp", "decode.cuh", "cache_ops.cuh", "cascade.cuh", "nvfp4.cuh",
-        "pa_device.cuh", "umma.cuh"]
+DEPS = ["libpa.cu", "block_manager.cpp", "decode.cuh", "decode_tc.cuh", "cache_ops.cuh",
+        "cascade.cuh", "nvfp4.cuh", "pa_device.cuh", "umma.cuh"]
 
 
 def _nvcc() -> str:

@@ -164,7 +164,10 @@ __global__ void __launch_bounds__(256)
 //   otherwise:       the scale stays
 // then the row is e4m3(x / scale) (fp32 IEEE division, RNE, satfinite).
 // Tokens of one call must name distinct blocks (a block updated by two
-// warps at once ends unspecified).
+// warps at once ends unspecified).  With `tables` non-null, token t is
+// sequence t's appended token of a decode step: a slot other than the one
+// the table gives position seq_lens[t] - 1 (or any slot of an empty
+// sequence) is not written and flags PA_DEVERR_BAD_SLOT.
 template <int D>
 __global__ void __launch_bounds__(256, 1)
     cache_write_fp8_kernel(const __nv_bfloat16* __restrict__ k_new,
@@ -172,7 +175,9 @@ __global__ void __launch_bounds__(256, 1)
                            const int64_t* __restrict__ slots, int32_t num_tokens,
                            uint8_t* __restrict__ k_cache, uint8_t* __restrict__ v_cache,
                            float* __restrict__ k_scale, float* __restrict__ v_scale,
-                           int64_t num_slots, int32_t num_kv_heads, int32_t block_size) {
+                           int64_t num_slots, int32_t num_kv_heads, int32_t block_size,
+                           const int32_t* __restrict__ seq_lens,
+                           const int32_t* __restrict__ tables, int32_t max_blocks) {
   pdl_wait();  // as cache_write_kernel
   pdl_trigger();
   constexpr int E = D / 32;  // bytes (and elements) per lane per row
@@ -188,6 +193,19 @@ __global__ void __launch_bounds__(256, 1)
   if (s >= num_slots) {
     if (lane == 0 && h == 0 && kv == 0) flag_error(PA_DEVERR_BAD_SLOT);
     return;
+  }
+  if (tables != nullptr) {
+    const int32_t n = seq_lens[t];
+    bool at_end = n > 0 && static_cast<int64_t>(n) <= static_cast<int64_t>(max_blocks) * block_size;
+    if (at_end) {
+      const int32_t pos = n - 1;
+      at_end = static_cast<int64_t>(tables[t * max_blocks + pos / block_size]) * block_size +
+                   pos % block_size == s;
+    }
+    if (!at_end) {
+      if (lane == 0 && h == 0 && kv == 0) flag_error(PA_DEVERR_BAD_SLOT);
+      return;
+    }
   }
   const int64_t blk = s / block_size;
   const int32_t off = static_cast<int32_t>(s - blk * block_size);

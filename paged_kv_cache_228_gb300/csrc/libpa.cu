@@ -18,6 +18,7 @@
 #include "cache_ops.cuh"
 #include "cascade.cuh"
 #include "decode.cuh"
+#include "decode_tc.cuh"
 #include "nvfp4.cuh"
 #include "pa.h"
 #include "pa_testing.h"
@@ -188,6 +189,38 @@ pa_status decode_plan(int dev, DecodePlan* out) {
   return PA_OK;
 }
 
+// The tcgen05 FP8 decode: kTcCtasPerSm CTAs per SM (if registers allow),
+// each with the deepest ring of 32 KB chunk stages that lets them share the
+// SM's shared memory.
+constexpr int kTcCtasPerSm = 1;
+
+template <int D>
+pa_status tc_plan(int dev, DecodePlan* out) {
+  static DecodePlan cached[kMaxDevices];
+  std::lock_guard<std::mutex> lk(g_mu);
+  DecodePlan& pl = cached[dev];
+  if (pl.ctas_per_sm == 0) {
+    const size_t per_cta = kSmemPerSm / kTcCtasPerSm - kSmemReservedPerCta;
+    int s = static_cast<int>((per_cta - tc_smem_bytes<D>(0)) / TcSmem<D>::kStage);
+    if (s < 2) s = 2;
+    if (s > kTcMaxStages) s = kTcMaxStages;
+    const size_t smem = tc_smem_bytes<D>(s);
+    if (cudaFuncSetAttribute(paged_decode_tc_fp8_kernel<D>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return PA_ERR_CUDA;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_tc_fp8_kernel<D>,
+                                                      kTcThreads, smem) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (n < 1) return PA_ERR_UNSUPPORTED;
+    pl.stages = s;
+    pl.ctas_per_sm = n < kTcCtasPerSm ? n : kTcCtasPerSm;
+  }
+  *out = pl;
+  return PA_OK;
+}
+
 // NVFP4 decode: a fixed ring depth per head_dim, so the plan is the CTAs
 // per SM that registers and that ring allow (at most kMaxCtasPerSm).
 template <int D>
@@ -222,6 +255,7 @@ pa_status fp4_plan(int dev, int* ctas_per_sm) {
 constexpr int32_t kSegCostBf16 = 16;
 constexpr int32_t kSegCostFp8 = 16;
 constexpr int32_t kSegCostFp4 = 16;
+constexpr int32_t kSegCostTc = 16;
 
 // Workspace for P decode CTAs over `segs` segments: P + segs partial
 // slots (a CTA's pieces never collide: piece = cta + segment), then P
@@ -307,6 +341,61 @@ pa_status launch_decode(const DecodeParams& prm_in, const void* q,
   if (launch_pdl(decode_fn<D, FP8>(append), dim3(static_cast<unsigned>(P)),
                  dim3(DecodeShape<D, FP8>::kThreads), decode_smem_bytes<D, FP8>(stages), stream,
                  tq, tk, tv, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
+                 dim3(prm.group * D / 4), 0, stream, prm) != cudaSuccess)
+    return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+// FP8 cache, head_dim 128, plain decode: the tcgen05 kernel and the merge.
+template <int D>
+pa_status launch_decode_tc(const DecodeParams& prm_in, const void* q, const void* k_cache,
+                           const void* v_cache, void* workspace, size_t workspace_bytes,
+                           int32_t num_splits, cudaStream_t stream) {
+  int sms = 0, dev = 0;
+  pa_status st = device_sms(&sms, &dev);
+  if (st != PA_OK) return st;
+  DecodePlan plan;
+  st = tc_plan<D>(dev, &plan);
+  if (st != PA_OK) return st;
+  const int32_t P = num_splits > 0 ? num_splits : sms * plan.ctas_per_sm;
+  const int64_t segs = static_cast<int64_t>(prm_in.num_seqs) * prm_in.num_kv_heads;
+  const size_t need = P > 1 ? workspace_bytes_for(P, segs, D) : 0;
+  if (need > 0 && (workspace == nullptr || workspace_bytes < need || !aligned16(workspace)))
+    return PA_ERR_WORKSPACE;
+  DecodeParams prm = prm_in;
+  prm.num_ctas = P;
+  prm.seg_cost = kSegCostTc;
+  prm.stages = plan.stages;
+  prm.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
+  prm.stall = g_wait_stall.load(std::memory_order_relaxed);
+  prm.ws_o = nullptr;
+  prm.ws_ml = nullptr;
+  prm.ws_job = nullptr;
+  if (need > 0) {
+    const int64_t pieces = P + segs;
+    char* w = static_cast<char*>(workspace);
+    prm.ws_o = reinterpret_cast<float*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * D * sizeof(float);
+    prm.ws_ml = reinterpret_cast<float2*>(w);
+    w += static_cast<size_t>(pieces) * kMaxG * sizeof(float2);
+    prm.ws_job = reinterpret_cast<int2*>(w);
+  }
+  CUtensorMap tq, tk, tv;
+  const uint64_t qrows = static_cast<uint64_t>(prm.num_seqs) * prm.num_q_heads;
+  const uint32_t box_rows = prm.block_size < kTile ? prm.block_size : kTile;
+  const uint64_t rows = static_cast<uint64_t>(prm.rows_total);
+  if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, D, qrows, D * 2, 64, 8,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_UINT8, k_cache, D, rows, D, D, box_rows,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_UINT8, v_cache, D, rows, D, D, box_rows,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return PA_ERR_CUDA;
+  if (launch_pdl(paged_decode_tc_fp8_kernel<D>, dim3(static_cast<unsigned>(P)),
+                 dim3(kTcThreads), tc_smem_bytes<D>(plan.stages), stream, tq, tk, tv,
+                 prm) != cudaSuccess)
     return PA_ERR_CUDA;
   if (launch_pdl(paged_decode_merge_kernel<D>, dim3(static_cast<unsigned>(P)),
                  dim3(prm.group * D / 4), 0, stream, prm) != cudaSuccess)
@@ -415,13 +504,15 @@ extern "C" pa_status pa_cache_write_fp8(const void* k_new, const void* v_new,
                    s, static_cast<const __nv_bfloat16*>(k_new),
                    static_cast<const __nv_bfloat16*>(v_new), slot_mapping, num_tokens,
                    static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
-                   v_scale, num_slots, num_kv_heads, block_size);
+                   v_scale, num_slots, num_kv_heads, block_size,
+                   static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr), 0);
   else
     e = launch_pdl(cache_write_fp8_kernel<64>, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
                    s, static_cast<const __nv_bfloat16*>(k_new),
                    static_cast<const __nv_bfloat16*>(v_new), slot_mapping, num_tokens,
                    static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), k_scale,
-                   v_scale, num_slots, num_kv_heads, block_size);
+                   v_scale, num_slots, num_kv_heads, block_size,
+                   static_cast<const int32_t*>(nullptr), static_cast<const int32_t*>(nullptr), 0);
   return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -780,6 +871,28 @@ pa_status decode_entry(const void* q, const void* k_cache, const void* v_cache,
     if (head_dim == 128)
       return launch_decode<128, false>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
     return launch_decode<64, false>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);
+  }
+  if (head_dim == 128 && cas == nullptr) {
+    if (app != nullptr) {
+      // FP8 append at head_dim 128: the checked cache write, then the
+      // tcgen05 decode (its own launch: the decode kernel stores nothing)
+      const int64_t warps = 2LL * num_seqs * num_kv_heads;
+      const int64_t grid = (warps * 32 + 255) / 256;
+      if (grid > INT_MAX) return PA_ERR_UNSUPPORTED;
+      if (launch_pdl(cache_write_fp8_kernel<128>, dim3(static_cast<unsigned>(grid)), dim3(256), 0,
+                     s, static_cast<const __nv_bfloat16*>(app->k_new),
+                     static_cast<const __nv_bfloat16*>(app->v_new), app->slot_mapping, num_seqs,
+                     p.k_cache, p.v_cache, const_cast<float*>(k_scale),
+                     const_cast<float*>(v_scale), static_cast<int64_t>(num_blocks) * block_size,
+                     num_kv_heads, block_size, seq_lens, block_tables,
+                     max_blocks_per_seq) != cudaSuccess)
+        return PA_ERR_CUDA;
+      p.k_new = p.v_new = nullptr;
+      p.slot_mapping = nullptr;
+      p.k_cache = p.v_cache = nullptr;
+    }
+    return launch_decode_tc<128>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits,
+                                 s);
   }
   if (head_dim == 128)
     return launch_decode<128, true>(p, q, k_cache, v_cache, workspace, workspace_bytes, num_splits, s);

@@ -1,13 +1,15 @@
 """The bounded-wait path of the decode kernels, made to run on purpose.
 
-Every pipeline wait in the bf16 (copy warp + math warp) and FP8 (single
-warp) decode kernels gives up after a bounded number of polls, sets
-PA_DEVERR_TIMEOUT and lets the CTA's own copies land before it exits.  A
-correct pipeline never reaches the bound, so this test uses the test hook
-of include/pa_testing.h: with stall on, every CTA's math warp first waits
-on a barrier nothing arrives at, with a short limit, so that wait runs out
-deterministically (no fault, no hang: the copies the CTA issued still land
-and are waited for).  The call must return, the error word must carry
+Every pipeline wait in the bf16 (copy warp + math warp), FP8 head_dim 64
+(single warp) and FP8 head_dim 128 (tensor-core, warp-specialised) decode
+kernels gives up after a bounded number of polls, sets PA_DEVERR_TIMEOUT
+and lets the CTA's own copies land before it exits.  A correct pipeline
+never reaches the bound, so this test uses the test hook of
+include/pa_testing.h: with stall on, every CTA's math (softmax) warps first
+wait on a barrier nothing arrives at, with a short limit, so that wait runs
+out deterministically (no fault, no hang: the copies the CTA issued still
+land and are waited for, and the tensor-core kernel's MMA warps wait for
+their MMAs before the tensor memory is released).  The call must return, the error word must carry
 PA_DEVERR_TIMEOUT, and the next normal call on the same device must be
 clean and match the fp64 oracle.
 """
@@ -73,10 +75,13 @@ def test_bf16_stalled_wait_times_out_then_recovers(name, splits):
     assert_close(out, oracle_decode(case, snap, seqs), 1e-2, f"{name} after a timeout")
 
 
-def test_fp8_stalled_wait_times_out_then_recovers():
-    case = build_case(W.tiny())
+@pytest.mark.parametrize("name", ["tiny", "llama3.1-8b"])
+def test_fp8_stalled_wait_times_out_then_recovers(name):
+    # tiny: head_dim 64, the single-warp kernel; the 8B shape: head_dim 128,
+    # the tensor-core kernel
+    case = build_case(W.WORKLOADS[name]())
     w = case.w
-    seqs = list(range(w.num_seqs))
+    seqs = list(range(w.num_seqs)) if w.num_seqs <= 16 else list(range(0, w.num_seqs, 9))
     snap = snapshot_blocks(case, seqs)
     ref, (blocks, valid, ids) = oracle_decode_fp8(case, snap, seqs)
     # an FP8 cache of the same blocks, quantised by the library
@@ -101,4 +106,4 @@ def test_fp8_stalled_wait_times_out_then_recovers():
                  v_scale=vs)
     torch.cuda.synchronize()
     assert pa.pa_get_device_error() == 0
-    assert_close(out, ref, 5e-2, "fp8 after a timeout")
+    assert_close(out, ref, 5e-2, f"{name} fp8 after a timeout")
