@@ -615,11 +615,12 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
                    : "memory");
       // V rows past the sequence inside the last 32-token MMA step hold
       // stale bytes (possibly NaN codes): zero them, as P is zero there
-      // (group 0 the first half of the row, group 1 the second)
+      // (with two groups, group 0 the first half of the row, group 1 the
+      // second)
       if (!valid && t < ((nvalid + 31) & ~31)) {
-        const uint32_t vrow = ring + st * L::kStage + L::kKV + t * D + g * (D / 2);
-#pragma unroll
-        for (int o = 0; o < D / 2; o += 16)
+        const bool both = p.group > kTcGroupHeads;
+        const uint32_t vrow = ring + st * L::kStage + L::kKV + t * D + (both ? g * (D / 2) : 0);
+        for (int o = 0; o < (both ? D / 2 : D); o += 16)
           asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + o), "r"(0)
                        : "memory");
       }
@@ -703,15 +704,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(smem_addr(&hdr->full[s]), kTcCopyWarps);
       mbar_init(smem_addr(&hdr->empty[s]), 1);
     }
+    // softmax warps that take part: group 1 only when the GQA group has
+    // more than 4 heads (its heads would all be past the group)
+    const uint32_t nsoft = p.group > kTcGroupHeads ? kTcSoftWarps : kTcSoftWarps / 2;
     for (int s = 0; s < 2; ++s) {
       mbar_init(smem_addr(&hdr->qfull[s]), 1);
       mbar_init(smem_addr(&hdr->qempty[s]), 1);
       mbar_init(smem_addr(&hdr->qready[s]), 1);
       mbar_init(smem_addr(&hdr->s_full[s]), 1);
-      mbar_init(smem_addr(&hdr->s_empty[s]), kTcSoftWarps);
-      mbar_init(smem_addr(&hdr->p_full[s]), kTcSoftWarps);
+      mbar_init(smem_addr(&hdr->s_empty[s]), nsoft);
+      mbar_init(smem_addr(&hdr->p_full[s]), nsoft);
       mbar_init(smem_addr(&hdr->o_full[s]), 1);
-      mbar_init(smem_addr(&hdr->o_empty[s]), kTcSoftWarps);
+      mbar_init(smem_addr(&hdr->o_empty[s]), nsoft);
     }
     mbar_init(smem_addr(&hdr->mma_done[0]), 1);
     mbar_init(smem_addr(&hdr->mma_done[1]), 1);
@@ -751,7 +755,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_mma_qk<D>(p, ring, qbuf, q8buf, hdr, tmem, it, hi);
     } else if (warp == 10) {
       tc_mma_pv<D>(p, ring, pbuf, hdr, tmem, it, hi);
-    } else {
+    } else if (((warp - 2) >> 2) * kTcGroupHeads < p.group) {
       tc_softmax<D>(p, ring, pbuf, hdr, tmem, it, hi, U, P, (warp - 2) >> 2);
     }
   }

@@ -255,7 +255,7 @@ pa_status fp4_plan(int dev, int* ctas_per_sm) {
 constexpr int32_t kSegCostBf16 = 16;
 constexpr int32_t kSegCostFp8 = 16;
 constexpr int32_t kSegCostFp4 = 16;
-constexpr int32_t kSegCostTc = 16;
+constexpr int32_t kSegCostTc = 128;
 
 // Workspace for P decode CTAs over `segs` segments: P + segs partial
 // slots (a CTA's pieces never collide: piece = cta + segment), then P
