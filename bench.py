@@ -845,6 +845,19 @@ def main():
             }
         secondary.update(block_size_sweep(args, device, peak))
         r = run_native(w, max(50, args.steps // 20), max(3, args.warmup // 10), device,
+                       fp8=True)
+        nb = kv_bytes(w, 1, 4)
+        secondary[w.name + "_fp8"] = {
+            "kv_bytes_per_step": nb,
+            "decode_us": r["decode_ms_mean"] * 1e3,
+            "decode_GB_per_s": nb / (r["decode_ms_mean"] / 1e3) / 1e9,
+            "hbm_frac_of_measured": nb / (r["decode_ms_mean"] / 1e3) / 1e9 / peak,
+            "us_per_step": r["ms_per_step"] * 1e3,
+            "kernel": "paged_decode_tc_fp8_kernel<128> + merge",
+            "note": "pa_cache_write_fp8 of the step's tokens + pa_decode (+ merge) on an E4M3 "
+                    "cache; bytes: codes and per-(block, head) scales",
+        }
+        r = run_native(w, max(50, args.steps // 20), max(3, args.warmup // 10), device,
                        nvfp4=True)
         nb = kv_bytes_nvfp4(w)
         secondary[w.name + "_nvfp4"] = {
@@ -884,7 +897,7 @@ def main():
                     "frac": dec_gbs / peak,
                     "traffic": ncu_traffic(wl.name if fmt == "bf16" else f"{wl.name}_{fmt}"),
                     "kernel": {"bf16": "paged_decode_ws_kernel<128,bf16>",
-                               "fp8": "paged_decode_kernel<128,fp8>",
+                               "fp8": "paged_decode_tc_fp8_kernel<128>",
                                "nvfp4": "paged_decode_nvfp4_kernel<128>"}[fmt] + " + merge "
                               "(per launch pair, CUDA events around each call)",
                     "peak_source": peak_kind},

@@ -139,6 +139,7 @@ def test_decode_parity_70b_128k_fp8(long_case):
 
 
 @pytest.mark.parametrize("name,bs", [("llama3.1-8b", 16), ("shared_prefix", 8),
+                                     ("shared_prefix", 32), ("shared_prefix", 64),
                                      ("llama3.2-1b", 16)])
 def test_decode_parity_fp8(name, bs):
     w = W.shared_prefix(bs) if name == "shared_prefix" else W.WORKLOADS[name]()
@@ -318,4 +319,68 @@ def test_more_partitions_than_tiles(splits):
     snap = snapshot_blocks(case, seqs)
     out = run_step(case, num_splits=splits)
     assert_close(out, oracle_decode(case, snap, seqs), TOL_BF16, f"tiny splits={splits}")
+    assert pa.pa_get_device_error() == 0
+
+
+# ------------------------------------------------ FP8, head_dim 128 paths ---
+def _fp8_cache(case, seqs, poison=False):
+    """The oracle's FP8 reference for `seqs` and a GPU E4M3 cache of the same
+    blocks quantised by the library; with poison, every code past a block's
+    valid tokens is an E4M3 NaN (0x7F), which the kernel must never let into
+    a product."""
+    w = case.w
+    snap = snapshot_blocks(case, seqs)
+    ref, (blocks, vl, ids) = oracle_decode_fp8(case, snap, seqs)
+    phys = torch.tensor([ids[b] for b in blocks], dtype=torch.int32, device="cuda")
+    kq = torch.zeros(case.k_cache.shape, dtype=torch.uint8, device="cuda")
+    vq = torch.zeros_like(kq)
+    ks = torch.ones((w.pool_blocks, w.num_kv_heads), device="cuda")
+    vs = torch.ones_like(ks)
+    pa.pa_quantize_fp8(case.k_cache, case.v_cache, phys,
+                       torch.tensor(vl, dtype=torch.int32, device="cuda"), kq, vq, ks, vs)
+    if poison:
+        for b, n in zip(phys.tolist(), vl):
+            kq[b, :, n:, :] = 0x7F
+            vq[b, :, n:, :] = 0x7F
+    return ref, kq, vq, ks, vs
+
+
+@pytest.mark.parametrize("splits", [1, 7, 151, 2000])
+def test_fp8_partition_count_within_tolerance(splits):
+    case = build_case(W.llama31_8b())
+    ref, kq, vq, ks, vs = _fp8_cache(case, list(range(0, 128, 9)))
+    out = run_step(case, num_splits=splits, write=False, k_cache=kq, v_cache=vq, k_scale=ks,
+                   v_scale=vs)
+    assert_close(out, ref, TOL_FP8, f"fp8 splits={splits}")
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("splits", [0, 2000])
+def test_fp8_repeated_decode_is_bit_identical(splits):
+    case = build_case(W.llama31_8b())
+    _, kq, vq, ks, vs = _fp8_cache(case, list(range(0, 128, 9)))
+    outs = [run_step(case, write=False, num_splits=splits, k_cache=kq, v_cache=vq, k_scale=ks,
+                     v_scale=vs) for _ in range(6)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_fp8_empty_and_ragged_sequences_poisoned_tails(bs):
+    # lengths around the 16-token tile, the 32-token MMA step and the
+    # 128-token chunk; the codes past each sequence's end are NaN
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 127, 128, 129, 0, 255, 257, 300, 511]
+    w = W.Workload("ragged128", len(lens), 32, 8, 128, bs,
+                   seq_lens=[max(1, n) for n in lens], pool_blocks=2 * (512 // bs) * 8,
+                   seed=22)
+    case = build_case(w)
+    case.w.seq_lens = lens
+    case.lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    seqs = [b for b, n in enumerate(lens) if n > 0]
+    ref, kq, vq, ks, vs = _fp8_cache(case, seqs, poison=True)
+    out = run_step(case, write=False, k_cache=kq, v_cache=vq, k_scale=ks, v_scale=vs)
+    assert_close(out, ref, TOL_FP8, f"fp8 ragged bs{bs}")
+    assert torch.equal(out[0], torch.zeros_like(out[0]))
+    assert torch.equal(out[11], torch.zeros_like(out[11]))
     assert pa.pa_get_device_error() == 0
