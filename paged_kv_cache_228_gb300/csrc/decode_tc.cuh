@@ -554,6 +554,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
       }
       bad |= !mbar_wait(smem_addr(&hdr->full[st]), ph, wl);
       bad |= !mbar_wait(smem_addr(&hdr->s_full[j & 1]), (j >> 1) & 1, wl);
+      tc_fence_after_sync();  // the MMA's tensor-memory writes before the load
       uint32_t sr[8];  // hi of the group's 4 heads, then their lo
       tmem_ld8(tl + (j & 1) * 16, sr);
       tmem_wait_ld();
@@ -631,6 +632,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
     if (have_prev) {
       const uint32_t c = j - 1;
       bad |= !mbar_wait(smem_addr(&hdr->o_full[c & 1]), (c >> 1) & 1, wl);
+      tc_fence_after_sync();
       uint32_t orr[8];
       tmem_ld8(tl + 32 + (c & 1) * 16, orr);
       tmem_wait_ld();
