@@ -54,6 +54,15 @@
 
 namespace pa {
 
+// Every wait of this kernel: at most kTcSuspendNs per poll (the phase's
+// completion ends it earlier), so waiting warps leave the issue slots to
+// the others; p.wait_limit (default) polls bound it to about 8 s.
+constexpr uint32_t kTcSuspendNs = 2000;
+__device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity,
+                                        uint32_t limit = (1u << 22)) {
+  return mbar_wait_sleep(bar, parity, limit, kTcSuspendNs);
+}
+
 constexpr int kTcTiles = 8;               // 16-token tiles per chunk
 constexpr int kTcTok = kTcTiles * kTile;  // tokens per chunk: the QK MMA's M
 constexpr int kTcMaxStages = 6;
@@ -198,9 +207,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
   for (; it0.nt > 0; ++j) {
     bool ok = true;
     if (lane == 0) {
-      if (j >= S) ok = mbar_wait(smem_addr(&hdr->empty[st]), ph ^ 1);
+      if (j >= S) ok = tc_wait(smem_addr(&hdr->empty[st]), ph ^ 1);
       if (ok && part == 0 && it0.first && qn >= 2)
-        ok = mbar_wait(smem_addr(&hdr->qempty[qn & 1]), ((qn >> 1) - 1) & 1);
+        ok = tc_wait(smem_addr(&hdr->qempty[qn & 1]), ((qn >> 1) - 1) & 1);
     }
     if (!__shfl_sync(0xffffffffu, ok, 0)) break;
     cp_async_wait_group<1>();  // this chunk's entries (two groups back) landed
@@ -261,9 +270,9 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
   // No copy may still target shared memory when the CTA exits.
   if (lane == 0) {
     for (uint32_t k = j > S ? j - S : 0; k < j; ++k)
-      mbar_wait(smem_addr(&hdr->full[k % S]), (k / S) & 1, 1u << 16);
+      tc_wait(smem_addr(&hdr->full[k % S]), (k / S) & 1, 1u << 16);
     for (uint32_t k = qn > 2 ? qn - 2 : 0; k < qn; ++k)
-      mbar_wait(smem_addr(&hdr->qfull[k & 1]), (k >> 1) & 1, 1u << 16);
+      tc_wait(smem_addr(&hdr->qfull[k & 1]), (k >> 1) & 1, 1u << 16);
   }
   __syncwarp();
 }
@@ -372,11 +381,11 @@ __device__ __forceinline__ void tc_mma_qk(const DecodeParams& p, uint32_t ring, 
   uint32_t sg = 0;
   for (uint32_t j = 0; it.nt > 0; ++j) {
     const uint32_t st = j % S;
-    bool ok = mbar_wait(smem_addr(&hdr->full[st]), (j / S) & 1, wl);
+    bool ok = tc_wait(smem_addr(&hdr->full[st]), (j / S) & 1, wl);
     // (s_empty also means the softmax warps have read hm of the piece that
     // last used this query slot)
-    if (ok && j >= 2) ok = mbar_wait(smem_addr(&hdr->s_empty[j & 1]), ((j >> 1) - 1) & 1, wl);
-    if (ok && it.first) ok = mbar_wait(smem_addr(&hdr->qfull[sg & 1]), (sg >> 1) & 1, wl);
+    if (ok && j >= 2) ok = tc_wait(smem_addr(&hdr->s_empty[j & 1]), ((j >> 1) - 1) & 1, wl);
+    if (ok && it.first) ok = tc_wait(smem_addr(&hdr->qfull[sg & 1]), (sg >> 1) & 1, wl);
     if (!__all_sync(0xffffffffu, ok)) break;
     if (it.first) {
       const uint32_t slot = sg & 1;
@@ -405,7 +414,7 @@ __device__ __forceinline__ void tc_mma_qk(const DecodeParams& p, uint32_t ring, 
   // released
   if (lane == 0) {
     umma_commit(smem_addr(&hdr->mma_done[0]));
-    mbar_wait(smem_addr(&hdr->mma_done[0]), 0, wl);
+    tc_wait(smem_addr(&hdr->mma_done[0]), 0, wl);
   }
   __syncwarp();
 }
@@ -424,8 +433,8 @@ __device__ __forceinline__ void tc_mma_pv(const DecodeParams& p, uint32_t ring, 
   const uint64_t pd0 = smem_desc(pbuf, 128, 128, 0);
   for (uint32_t j = 0; it.nt > 0; ++j) {
     const uint32_t st = j % S;
-    bool ok = mbar_wait(smem_addr(&hdr->p_full[j & 1]), (j >> 1) & 1, wl);
-    if (ok && j >= 2) ok = mbar_wait(smem_addr(&hdr->o_empty[j & 1]), ((j >> 1) - 1) & 1, wl);
+    bool ok = tc_wait(smem_addr(&hdr->p_full[j & 1]), (j >> 1) & 1, wl);
+    if (ok && j >= 2) ok = tc_wait(smem_addr(&hdr->o_empty[j & 1]), ((j >> 1) - 1) & 1, wl);
     if (!__all_sync(0xffffffffu, ok)) break;
     tc_fence_after_sync();
     if (lane == 0) {
@@ -444,7 +453,7 @@ __device__ __forceinline__ void tc_mma_pv(const DecodeParams& p, uint32_t ring, 
   }
   if (lane == 0) {
     umma_commit(smem_addr(&hdr->mma_done[1]));
-    mbar_wait(smem_addr(&hdr->mma_done[1]), 0, wl);
+    tc_wait(smem_addr(&hdr->mma_done[1]), 0, wl);
   }
   __syncwarp();
 }
@@ -531,7 +540,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
     l[i] = lold[i] = acc[i] = 0.f;
   }
   bool bad = false;
-  if (p.stall) bad = !mbar_wait(smem_addr(&hdr->stall), 0, wl);  // test hook
+  if (p.stall) bad = !tc_wait(smem_addr(&hdr->stall), 0, wl);  // test hook
   uint32_t j = 0, sg = 0, nfin = 0, st = 0, ph = 0;
   bool have_prev = false, grew1 = false, last1 = false;
   float f1 = 0.f;  // the previous chunk's O unit
@@ -542,7 +551,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
     float f = 0.f;
     if (have) {
       if (it.first) {
-        bad |= !mbar_wait(smem_addr(&hdr->qready[sg & 1]), (sg >> 1) & 1, wl);
+        bad |= !tc_wait(smem_addr(&hdr->qready[sg & 1]), (sg >> 1) & 1, wl);
 #pragma unroll
         for (int i = 0; i < H; ++i) {
           hm[i] = hdr->hm[sg & 1][H * g + i];
@@ -552,8 +561,8 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
         }
         ++sg;
       }
-      bad |= !mbar_wait(smem_addr(&hdr->full[st]), ph, wl);
-      bad |= !mbar_wait(smem_addr(&hdr->s_full[j & 1]), (j >> 1) & 1, wl);
+      bad |= !tc_wait(smem_addr(&hdr->full[st]), ph, wl);
+      bad |= !tc_wait(smem_addr(&hdr->s_full[j & 1]), (j >> 1) & 1, wl);
       tc_fence_after_sync();  // the MMA's tensor-memory writes before the load
       uint32_t sr[8];  // hi of the group's 4 heads, then their lo
       tmem_ld8(tl + (j & 1) * 16, sr);
@@ -631,7 +640,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
     }
     if (have_prev) {
       const uint32_t c = j - 1;
-      bad |= !mbar_wait(smem_addr(&hdr->o_full[c & 1]), (c >> 1) & 1, wl);
+      bad |= !tc_wait(smem_addr(&hdr->o_full[c & 1]), (c >> 1) & 1, wl);
       tc_fence_after_sync();
       uint32_t orr[8];
       tmem_ld8(tl + 32 + (c & 1) * 16, orr);

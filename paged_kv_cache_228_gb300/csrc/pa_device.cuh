@@ -113,6 +113,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Bounded wait whose polls may each suspend the thread for up to
+// `suspend_ns` (the phase's completion wakes it earlier): a warp that waits
+// long takes few issue slots.  The bound is then at most limit * suspend_ns.
+__device__ __forceinline__ bool mbar_wait_sleep(uint32_t bar, uint32_t parity, uint32_t limit,
+                                                uint32_t suspend_ns) {
+  for (uint32_t i = 0; i < limit; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    if (ok) return true;
+  }
+  flag_error(PA_DEVERR_TIMEOUT);
+  return false;
+}
+
 // Non-blocking test of a phase.
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
