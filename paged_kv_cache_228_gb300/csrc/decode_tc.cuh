@@ -73,7 +73,17 @@ constexpr int kTcThreads = 32 * (2 + kTcSoftWarps + kTcCopyWarps);
 constexpr float kTcSlack = 4.f;    // log2 units the max may lag the scores
 constexpr float kTcPScale = 16.f;  // 2^(8 - kTcSlack): P' <= 256 < 448
 constexpr uint32_t kTcTmemCols = 64;  // S at columns 0 / 16, O at 32 / 48
-constexpr uint32_t kTcNamedBar = 1;   // + g: the four softmax warps of group g
+// Named barriers 1 and 2: the four softmax warps of group 0, resp. 1 (as
+// constants, so the kernel reserves only the barriers it names).
+__device__ __forceinline__ void tc_group_sync(int g) {
+  if (g == 0)
+    named_bar_sync<1>(128);
+  else
+    named_bar_sync<2>(128);
+}
+__device__ __forceinline__ uint32_t tc_group_popc(int g, bool pred) {
+  return g == 0 ? named_bar_popc<1>(128, pred) : named_bar_popc<2>(128, pred);
+}
 
 template <int D>
 struct TcSmem {
@@ -490,7 +500,7 @@ __device__ __forceinline__ void tc_finish(const DecodeParams& p, TcHeader* hdr, 
   if (lane == 0)
 #pragma unroll
     for (int i = 0; i < kTcGroupHeads; ++i) red[qd][i] = Lh[i];
-  named_bar_sync(kTcNamedBar + g, 128);
+  tc_group_sync(g);
 #pragma unroll
   for (int i = 0; i < kTcGroupHeads; ++i) Lh[i] = (red[0][i] + red[1][i]) + (red[2][i] + red[3][i]);
   const int G = p.group;
@@ -528,7 +538,6 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
   const int lane = threadIdx.x & 31, qd = (threadIdx.x >> 5) & 3;
   const int t = 32 * qd + lane;
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16) + 8 * g;
-  const uint32_t bar = kTcNamedBar + g;
   const int bshift = p.block_size < kTile ? 3 : 4;  // token -> box
   const uint32_t S = p.stages, wl = p.wait_limit;
   float hm[H], m[H], mt[H], l[H], lold[H];
@@ -585,8 +594,8 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
         x[i] = valid ? s * (ks * hm[i]) : -INFINITY;
         gr |= x[i] > mt[i];
       }
-      if (named_bar_popc(bar, 128, gr || bad) != 0) {
-        if (named_bar_popc(bar, 128, bad) != 0) break;  // the group's four warps leave
+      if (tc_group_popc(g, gr || bad) != 0) {
+        if (tc_group_popc(g, bad) != 0) break;  // the group's four warps leave
         // a score passed the running max by more than the slack: the
         // chunk's maxima over the 128 tokens become the new running max
         float mx[H];
@@ -595,7 +604,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
         if (lane == 0)
 #pragma unroll
           for (int i = 0; i < H; ++i) hdr->red_m[g][qd][i] = mx[i];
-        named_bar_sync(bar, 128);
+        tc_group_sync(g);
 #pragma unroll
         for (int i = 0; i < H; ++i) {
           const float mn = fmaxf(fmaxf(m[i], fmaxf(hdr->red_m[g][0][i], hdr->red_m[g][1][i])),

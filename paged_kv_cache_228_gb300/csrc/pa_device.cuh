@@ -82,21 +82,24 @@ __device__ __forceinline__ void st_shared_f32(uint32_t addr, float v) {
   asm volatile("st.shared.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
-// Named barrier `id` over `n` threads (whole warps).
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Named barrier ID over `n` threads (whole warps).  The id is a constant,
+// so the compiler reserves only the barriers a kernel names.
+template <int ID>
+__device__ __forceinline__ void named_bar_sync(uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"n"(ID), "r"(n) : "memory");
 }
 
 // Named barrier that also counts the participating threads whose `pred`
 // is true.
-__device__ __forceinline__ uint32_t named_bar_popc(uint32_t id, uint32_t n, bool pred) {
+template <int ID>
+__device__ __forceinline__ uint32_t named_bar_popc(uint32_t n, bool pred) {
   uint32_t c;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "setp.ne.u32 p, %3, 0;\n\t"
-      "bar.red.popc.u32 %0, %1, %2, p;\n\t}"
+      "setp.ne.u32 p, %2, 0;\n\t"
+      "bar.red.popc.u32 %0, %1, %3, p;\n\t}"
       : "=r"(c)
-      : "r"(id), "r"(n), "r"(static_cast<uint32_t>(pred))
+      : "n"(ID), "r"(static_cast<uint32_t>(pred)), "r"(n)
       : "memory");
   return c;
 }
