@@ -13,8 +13,11 @@
 // GB300 design
 // ------------
 // * Work: the cost-weighted split of the flat 16-token tile list that every
-//   decode kernel uses (my_range), taken in chunks of up to 8 tiles of one
-//   (sequence, KV head) segment: 128 tokens, the M of one UMMA.
+//   decode kernel uses (my_range), taken in chunks of up to 16 tiles of one
+//   (sequence, KV head) segment: 256 tokens, two M = 128 QK MMAs per K step
+//   and a K = 256 PV.  Each softmax thread takes two tokens of a chunk, so
+//   the per-chunk waits and barriers are shared by twice the data (128-token
+//   chunks measured 377 us against 329 at 128K).
 // * A CTA (one per SM) is 14 warps with fixed roles:
 //     warps 0, 11-13  copies: each chunk's K and V boxes by TMA into a ring
 //                stage (K by two warps, V by two: one warp's TMA issue is
@@ -24,26 +27,26 @@
 //     warp 1     splits the piece's query per head into two E4M3 terms,
 //                x = q * 2^s = hi + lo / 16, as the 16 rows of the B
 //                operand, then per chunk the QK MMAs
-//                  S^T[128 tok x 16] = K[128 x 128 d] . [hi; lo]^T;
+//                  S^T[2 x 128 tok x 16] = K[256 x 128 d] . [hi; lo]^T;
 //     warp 10    per chunk, once its P is written, the PV MMAs
-//                  O^T[128 d x 16]   = V^T[128 d x 128 tok] . [P_hi; P_lo]^T
+//                  O^T[128 d x 16]   = V^T[128 d x 256 tok] . [P_hi; P_lo]^T
 //                (two issuing warps, so the next chunk's QK never delays
 //                this chunk's PV), both into tensor memory (fp32);
 //     warps 2-9  two groups of four (one warp per tensor-memory lane
-//                quarter), group g taking heads 4g .. 4g + 3: one token
-//                per thread, the score s = (S_hi + S_lo / 16) * k_scale *
+//                quarter), group g taking heads 4g .. 4g + 3: two tokens
+//                per thread (t and t + 128), the score s = (S_hi + S_lo / 16) * k_scale *
 //                scale / 2^s, the online softmax, P written to shared
 //                memory as a two-term E4M3 split; then, as d = lane of the
 //                same quarter, the chunk's O^T added into fp32 registers,
 //                and at a piece's end its output.
-// * The running max of a head is shared by the 128 tokens of a chunk and
+// * The running max of a head is shared by the 256 tokens of a chunk and
 //   moves only when a score passes it by more than kTcSlack (log2 units):
 //   one barrier reduction per chunk decides that for each group.  So P <= 2^kTcSlack.
 // * V scales: P' = p * v_scale(block) / vmax(chunk) * kTcPScale <= 256, and
 //   the chunk's O^T is in units of vmax(chunk) / kTcPScale, applied when it
 //   is added to the registers.  The two-term split keeps P' to about 2^-8
 //   relative (absolute 2^-13 below the E4M3 normal range).
-// * Shared memory: [ring stages of K | V (16 KB each) | 2 query slots (bf16)
+// * Shared memory: [ring stages of K | V (32 KB each) | 2 query slots (bf16)
 //   | 2 E4M3 query operands | 2 P buffers | header].  K tiles are K-major
 //   and V tiles MN-major operands with the 128-byte swizzle the TMA writes;
 //   P is an MN-major operand without swizzle.
@@ -63,8 +66,10 @@ __device__ __forceinline__ bool tc_wait(uint32_t bar, uint32_t parity,
   return mbar_wait_sleep(bar, parity, limit, kTcSuspendNs);
 }
 
-constexpr int kTcTiles = 8;               // 16-token tiles per chunk
-constexpr int kTcTok = kTcTiles * kTile;  // tokens per chunk: the QK MMA's M
+constexpr int kTcTiles = 16;              // 16-token tiles per chunk
+constexpr int kTcTok = kTcTiles * kTile;  // tokens per chunk
+constexpr int kTcM = 128;                 // tokens per QK MMA (its M)
+constexpr int kTcHalves = kTcTok / kTcM;  // QK MMAs per K step; tokens per softmax thread
 constexpr int kTcMaxStages = 6;
 constexpr int kTcCopyWarps = 4;  // K and V boxes split over these (even)
 constexpr int kTcSoftWarps = 8;  // two per tensor-memory lane quarter
@@ -72,7 +77,12 @@ constexpr int kTcGroupHeads = 4; // heads per softmax warp (group of four warps)
 constexpr int kTcThreads = 32 * (2 + kTcSoftWarps + kTcCopyWarps);
 constexpr float kTcSlack = 4.f;    // log2 units the max may lag the scores
 constexpr float kTcPScale = 16.f;  // 2^(8 - kTcSlack): P' <= 256 < 448
-constexpr uint32_t kTcTmemCols = 64;  // S at columns 0 / 16, O at 32 / 48
+// tensor memory: S of chunk parity b at columns kTcSCols b (+ 16 per half),
+// O at kTcOCol + 16 b
+constexpr uint32_t kTcSCols = 16 * kTcHalves;
+constexpr uint32_t kTcOCol = 2 * kTcSCols;
+constexpr uint32_t kTcTmemCols = 128;
+static_assert(kTcOCol + 32 <= kTcTmemCols, "tensor memory columns");
 // Named barriers 1 and 2: the four softmax warps of group 0, resp. 1 (as
 // constants, so the kernel reserves only the barriers it names).
 __device__ __forceinline__ void tc_group_sync(int g) {
@@ -104,8 +114,8 @@ struct TcHeader {
   uint64_t o_full[2], o_empty[2];
   uint64_t mma_done[2];           // each issuing warp's MMAs complete
   uint64_t stall;                 // test hook: never arrived at
-  float sk[kTcMaxStages][16];     // K scale per box (8 or 16 tokens)
-  float sv[kTcMaxStages][16];     // V scale per box
+  float sk[kTcMaxStages][32];     // K scale per box (8 or 16 tokens)
+  float sv[kTcMaxStages][32];     // V scale per box
   int32_t ent[kTcCopyWarps][4][32];  // copy part w, lane l: entry of chunk c at [w][c & 3][l]
   float hm[2][kMaxG];             // per head: scale * log2(e) / 2^s
   float red_m[2][4][kTcGroupHeads];     // group, warp quarter: chunk maxima
@@ -381,7 +391,7 @@ __device__ __forceinline__ void tc_mma_qk(const DecodeParams& p, uint32_t ring, 
   using L = TcSmem<D>;
   const int lane = threadIdx.x & 31;
   const uint32_t S = p.stages, wl = p.wait_limit;
-  constexpr uint32_t kIdQK = idesc_e4m3(kTcTok, 2 * kMaxG, false, false);
+  constexpr uint32_t kIdQK = idesc_e4m3(kTcM, 2 * kMaxG, false, false);
   // descriptors of stage 0 and query slot 0; other buffers and every K step
   // add their byte offset >> 4 to the start-address field (shared addresses
   // are below 256 KB, so the field never carries)
@@ -412,9 +422,12 @@ __device__ __forceinline__ void tc_mma_qk(const DecodeParams& p, uint32_t ring, 
     tc_fence_after_sync();
     if (lane == 0) {
       const uint64_t kd = kd0 + (st * L::kStage >> 4);
-      const uint32_t ts = tmem + (j & 1) * 16;
+      const uint32_t ts = tmem + (j & 1) * kTcSCols;
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) umma_e4m3(ts, kd + 2 * k, qd + 2 * k, kIdQK, k > 0);
+      for (int h = 0; h < kTcHalves; ++h)
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k)
+          umma_e4m3(ts + 16 * h, kd + h * (kTcM * D >> 4) + 2 * k, qd + 2 * k, kIdQK, k > 0);
       umma_commit(smem_addr(&hdr->s_full[j & 1]));
     }
     __syncwarp();
@@ -450,7 +463,7 @@ __device__ __forceinline__ void tc_mma_pv(const DecodeParams& p, uint32_t ring, 
     if (lane == 0) {
       const uint64_t vd = vd0 + (st * L::kStage >> 4);
       const uint64_t pd = pd0 + ((j & 1) * L::kP >> 4);
-      const uint32_t to = tmem + 32 + (j & 1) * 16;
+      const uint32_t to = tmem + kTcOCol + (j & 1) * 16;
       const int ks = (tc_valid(it) + 31) >> 5;  // rows past the last valid are zero
       umma_e4m3(to, vd, pd, kIdPV, false);
       for (int k = 1; k < ks; ++k)
@@ -573,34 +586,49 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
       bad |= !tc_wait(smem_addr(&hdr->full[st]), ph, wl);
       bad |= !tc_wait(smem_addr(&hdr->s_full[j & 1]), (j >> 1) & 1, wl);
       tc_fence_after_sync();  // the MMA's tensor-memory writes before the load
-      uint32_t sr[8];  // hi of the group's 4 heads, then their lo
-      tmem_ld8(tl + (j & 1) * 16, sr);
+      // tokens t + 128 h of the chunk, h < kTcHalves: S columns 16 h on
+      uint32_t sr[kTcHalves][8];  // hi of the group's 4 heads, then their lo
+#pragma unroll
+      for (int h = 0; h < kTcHalves; ++h) tmem_ld8(tl + (j & 1) * kTcSCols + 16 * h, sr[h]);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&hdr->s_empty[j & 1]));
       const int32_t nvalid = tc_valid(it);
-      const bool valid = t < nvalid;
-      const int box = t >> bshift;
-      const float ks = hdr->sk[st][box];
-      const float vs = valid ? hdr->sv[st][box] : 0.f;
-      const uint32_t wv = __reduce_max_sync(0xffffffffu, __float_as_uint(vs));  // vs >= 0
-      if (lane == 0) hdr->red_v[j & 1][g][qd] = __uint_as_float(wv);
-      float x[H];
+      bool valid[kTcHalves];
+      float vs[kTcHalves], x[kTcHalves][H];
+      float vsm = 0.f;
       bool gr = false;
 #pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float s = fmaf(__uint_as_float(sr[H + i]), 0.0625f, __uint_as_float(sr[i]));
-        x[i] = valid ? s * (ks * hm[i]) : -INFINITY;
-        gr |= x[i] > mt[i];
+      for (int h = 0; h < kTcHalves; ++h) {
+        const int tok = t + kTcM * h;
+        valid[h] = tok < nvalid;
+        const int box = tok >> bshift;
+        const float ks = hdr->sk[st][box];
+        vs[h] = valid[h] ? hdr->sv[st][box] : 0.f;
+        vsm = fmaxf(vsm, vs[h]);
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float s =
+              fmaf(__uint_as_float(sr[h][H + i]), 0.0625f, __uint_as_float(sr[h][i]));
+          x[h][i] = valid[h] ? s * (ks * hm[i]) : -INFINITY;
+          gr |= x[h][i] > mt[i];
+        }
       }
+      const uint32_t wv = __reduce_max_sync(0xffffffffu, __float_as_uint(vsm));  // vs >= 0
+      if (lane == 0) hdr->red_v[j & 1][g][qd] = __uint_as_float(wv);
       if (tc_group_popc(g, gr || bad) != 0) {
         if (tc_group_popc(g, bad) != 0) break;  // the group's four warps leave
         // a score passed the running max by more than the slack: the
-        // chunk's maxima over the 128 tokens become the new running max
+        // chunk's maxima over its tokens become the new running max
         float mx[H];
 #pragma unroll
-        for (int i = 0; i < H; ++i) mx[i] = warp_max(x[i]);
+        for (int i = 0; i < H; ++i) {
+          float v = x[0][i];
+#pragma unroll
+          for (int h = 1; h < kTcHalves; ++h) v = fmaxf(v, x[h][i]);
+          mx[i] = warp_max(v);
+        }
         if (lane == 0)
 #pragma unroll
           for (int i = 0; i < H; ++i) hdr->red_m[g][qd][i] = mx[i];
@@ -618,30 +646,37 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
       const float4 rv = *reinterpret_cast<const float4*>(hdr->red_v[j & 1][g]);
       const float vmax = fmaxf(fmaxf(rv.x, rv.y), fmaxf(rv.z, rv.w));
       f = vmax * (1.f / kTcPScale);
-      const float r = vs * __fdividef(kTcPScale, vmax);
-      float pq[H];
+      const float rinv = __fdividef(kTcPScale, vmax);
 #pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float pp = fast_exp2(x[i] - m[i]);
-        l[i] += pp;
-        pq[i] = pp * r;
-      }
-      uint32_t h0, l0, h1, l1;
-      split_e4m3x2(pq[0], pq[1], h0, l0);
-      split_e4m3x2(pq[2], pq[3], h1, l1);
-      asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(pbuf + (j & 1) * L::kP + t * 16 + 8 * g),
-                   "r"(h0 | (h1 << 16)), "r"(l0 | (l1 << 16))
-                   : "memory");
-      // V rows past the sequence inside the last 32-token MMA step hold
-      // stale bytes (possibly NaN codes): zero them, as P is zero there
-      // (with two groups, group 0 the first half of the row, group 1 the
-      // second)
-      if (!valid && t < ((nvalid + 31) & ~31)) {
-        const bool both = p.group > kTcGroupHeads;
-        const uint32_t vrow = ring + st * L::kStage + L::kKV + t * D + (both ? g * (D / 2) : 0);
-        for (int o = 0; o < (both ? D / 2 : D); o += 16)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + o), "r"(0)
-                       : "memory");
+      for (int h = 0; h < kTcHalves; ++h) {
+        const int tok = t + kTcM * h;
+        const float r = vs[h] * rinv;
+        float pq[H];
+#pragma unroll
+        for (int i = 0; i < H; ++i) {
+          const float pp = fast_exp2(x[h][i] - m[i]);
+          l[i] += pp;
+          pq[i] = pp * r;
+        }
+        uint32_t h0, l0, h1, l1;
+        split_e4m3x2(pq[0], pq[1], h0, l0);
+        split_e4m3x2(pq[2], pq[3], h1, l1);
+        asm volatile("st.shared.v2.b32 [%0], {%1,%2};" ::"r"(pbuf + (j & 1) * L::kP + tok * 16 +
+                                                               8 * g),
+                     "r"(h0 | (h1 << 16)), "r"(l0 | (l1 << 16))
+                     : "memory");
+        // V rows past the sequence inside the last 32-token MMA step hold
+        // stale bytes (possibly NaN codes): zero them, as P is zero there
+        // (with two groups, group 0 the first half of the row, group 1 the
+        // second)
+        if (!valid[h] && tok < ((nvalid + 31) & ~31)) {
+          const bool both = p.group > kTcGroupHeads;
+          const uint32_t vrow =
+              ring + st * L::kStage + L::kKV + tok * D + (both ? g * (D / 2) : 0);
+          for (int o = 0; o < (both ? D / 2 : D); o += 16)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(vrow + o), "r"(0)
+                         : "memory");
+        }
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -652,7 +687,7 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
       bad |= !tc_wait(smem_addr(&hdr->o_full[c & 1]), (c >> 1) & 1, wl);
       tc_fence_after_sync();
       uint32_t orr[8];
-      tmem_ld8(tl + 32 + (c & 1) * 16, orr);
+      tmem_ld8(tl + kTcOCol + (c & 1) * 16, orr);
       tmem_wait_ld();
       tc_fence_before_sync();
       __syncwarp();
