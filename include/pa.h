@@ -244,8 +244,10 @@ pa_status pa_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads,
  * with fp32 accumulation throughout.  FP8 caches dequantise as
  * decode(code) * k_scale[block][g] (likewise V); the query and the softmax
  * weights meet the E4M3 codes on the tensor cores as two-term E4M3 splits
- * (hi + lo / 16, within about 2^-8 of each value relative to its row's
- * largest), with fp32 products and sums.  A sequence with n == 0
+ * (hi + lo / 16 after a power-of-two row scale: exact for a bf16 query
+ * except below about 2^-14 of its row's largest element; each softmax
+ * weight within 2^-8 of itself plus 2^-18 of the largest), with fp32
+ * products and sums.  A sequence with n == 0
  * yields zeros.  Long contexts are split over up to `num_splits` persistent
  * work partitions (0 = automatic) whose partial results are merged with a
  * log-sum-exp reduction; the split points depend only on seq_lens, so the

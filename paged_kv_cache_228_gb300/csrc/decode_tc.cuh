@@ -44,8 +44,9 @@
 //   one barrier reduction per chunk decides that for each group.  So P <= 2^kTcSlack.
 // * V scales: P' = p * v_scale(block) / vmax(chunk) * kTcPScale <= 256, and
 //   the chunk's O^T is in units of vmax(chunk) / kTcPScale, applied when it
-//   is added to the registers.  The two-term split keeps P' to about 2^-8
-//   relative (absolute 2^-13 below the E4M3 normal range).
+//   is added to the registers.  The two-term split keeps P' to 2^-8
+//   relative (absolute 2^-14 where the lo term is subnormal); a bf16 query
+//   it carries exactly above about 2^-14 of its row's largest element.
 // * Shared memory: [ring stages of K | V (32 KB each) | 2 query slots (bf16)
 //   | 2 E4M3 query operands | 2 P buffers | header].  K tiles are K-major
 //   and V tiles MN-major operands with the 128-byte swizzle the TMA writes;
