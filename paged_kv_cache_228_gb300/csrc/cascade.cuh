@@ -13,28 +13,32 @@
 //
 // GB300 design: the two products run on the fifth-generation tensor cores
 // (tcgen05.mma, kind::f16, M = 128 query rows, fp32 accumulators in tensor
-// memory), operands in shared memory in the 128-byte-swizzled layout the
-// TMA writes.  What bounds this pass is how fast an SM takes in K and V
-// (the TMA delivers about 55 GB/s per SM, L2 or HBM alike), so a CTA makes
-// each byte serve two 128-row query tiles: it owns 256 query rows of one KV
-// head and one of S token ranges of the prefix, walked in 64-token chunks.
-// Eleven warps:
+// memory).  Q, K and V sit in shared memory in the 128-byte-swizzled layout
+// the TMA writes; P stays in tensor memory, where the softmax stores it and
+// the P.V product reads it as its A operand, so it costs no shared-memory
+// bandwidth.  A CTA makes each copied byte serve two 128-row query tiles:
+// it owns 256 query rows of one KV head and one of S token ranges of the
+// prefix, walked in 64-token chunks.  Eleven warps:
 //   warps 0/10 TMA producers of K and of V (one 2D box per block and
 //              64-column slab) into 3-stage K and V rings;
-//   warp 1     owns the tensor memory; lane 0 issues the MMAs, for each
-//              query tile t:
+//   warp 1     owns the tensor memory; lane 0 issues the MMAs, per chunk j
+//              and query tile t:
 //                S_t   = Q_t . K_j^T                 (A, B K-major; N = 64)
-//                O_t  += P_t,j-1 . V_j-1              (P K-major, V MN-major)
-//              the S of chunk j two chunks ahead of the products (into one of
-//              two S buffers per tile), so a tile's next scores are ready
-//              when its softmax finishes a chunk;
+//                O_t  += P_t,j . [V_j | 1]           (P in tensor memory,
+//                                                     V MN-major; N = D + 16)
+//              S of chunk j + 1 as soon as the softmax has read S_t,j, the
+//              product of chunk j when P_t,j is written.  The 16 extra
+//              columns multiply P by a slab of ones kept beside each V
+//              stage: they accumulate the row sum l of exactly the bf16
+//              weights the product applies, rescaled with O;
 //   warps 2-9  softmax, four warps per query tile, one row per thread (the
-//              warp's quarter of the tensor-memory lanes): online softmax in
-//              fp32 -- the running max moves, and O_t in tensor memory is
-//              rescaled, only when a score exceeds it by more than 8 in
-//              log2 units -- P rounded to bf16 into one of the tile's two
-//              shared P buffers (so softmax need not wait for the previous
-//              chunk's product), and l sums those rounded weights.
+//              warp's quarter of the tensor-memory lanes): the chunk's 64
+//              scores in one read, their maximum, then 2^(s.scale - m)
+//              rounded to bf16 pairs into the tile's P columns.  The running
+//              max m moves, and O_t (with l) is rescaled in tensor memory,
+//              only when a score exceeds it by more than 8 in log2 units.
+// A negative scale is applied as its magnitude to the negated query (exact
+// in bf16), so the maximum of a chunk is that of its raw scores.
 // Each split writes its own partial per row (staged through shared memory
 // so the global stores are coalesced); prefix_merge_kernel folds the S of
 // them together.
@@ -66,33 +70,42 @@ constexpr int kPfVStages = 3;   // V ring depth
 constexpr int kPfSoftWarps = 4 * kPfTiles;
 constexpr int kPfThreads = 96 + 32 * kPfSoftWarps;  // K and V producers, MMA, softmax
 constexpr int kPfVWarp = 2 + kPfSoftWarps;
+// Tensor memory per query tile (256 columns each): O (D fp32) and its 16
+// row-sum columns, S of the chunk (64 fp32) and P (64 bf16 = 32 columns).
+constexpr int kPfTileCols = 256;
+constexpr int kPfOCol = 0;
+constexpr int kPfSCol = 160;
+constexpr int kPfPCol = 224;
 constexpr int kPfTmemCols = 512;
 constexpr int kPfMaxSplits = 8;
+constexpr uint32_t kBf16OnePair = 0x3F803F80u;  // two bf16 ones
 
 template <int D>
 struct PfSmem {
   static constexpr int kSlab = kPfChunk * 128;        // 64 columns of one chunk
   static constexpr int kKV = (D / 64) * kSlab;        // K (or V) of a chunk
+  static constexpr int kVStage = kKV + kSlab;         // V, then a slab of ones
   static constexpr int kQ = (D / 64) * kPfRows * 128; // one query tile
-  static constexpr int kP = kPfRows * kPfChunk * 2;   // one tile's P (one 128-byte slab)
   static constexpr int kOffK = kPfTiles * kQ;
   static constexpr int kOffV = kOffK + kPfKStages * kKV;
-  static constexpr int kOffP = kOffV + kPfVStages * kKV;
-  static constexpr int kOffBar = kOffP + 2 * kPfTiles * kP;  // P double-buffered per tile
+  static constexpr int kOffBar = kOffV + kPfVStages * kVStage;
   static constexpr int kBytes = kOffBar + 256;
-  // the epilogue stages one tile's partial in the (free) P buffers, and the
+  // the epilogue stages one tile's partial in the (free) V ring, and the
   // per-row (m, l) in the (free) K ring
-  static_assert(kPfRows * D * 4 <= 2 * kPfTiles * kP, "epilogue staging");
+  static_assert(kPfRows * D * 4 <= kPfVStages * kVStage, "epilogue staging");
   static_assert(kPfTiles * kPfRows * 8 <= kPfKStages * kKV, "epilogue (m, l)");
-  static_assert(kP == kPfRows * 128, "P is one slab");
+  static_assert(kPfOCol + D + 16 <= kPfSCol && kPfSCol + kPfChunk <= kPfPCol &&
+                    kPfPCol + kPfChunk / 2 <= kPfTileCols,
+                "tensor-memory columns");
+  static_assert(kBytes <= 227 * 1024, "shared memory");
 };
 
 struct PfBars {
   uint64_t k_full[kPfKStages], k_empty[kPfKStages];
   uint64_t v_full[kPfVStages], v_empty[kPfVStages];
-  uint64_t s_full[kPfTiles][2], s_empty[kPfTiles][2];
-  uint64_t p_full[kPfTiles][2];  // P of a chunk written, per tile and P buffer
-  uint64_t o_done[kPfTiles][2];  // the tile's product with that P complete
+  uint64_t s_full[kPfTiles], s_empty[kPfTiles];  // S of the tile's chunk written / read
+  uint64_t p_full[kPfTiles];                     // P of the tile's chunk written
+  uint64_t o_done[kPfTiles];                     // the tile's product of that P complete
   uint64_t mma_done;
   uint32_t tmem;
 };
@@ -142,6 +155,44 @@ __device__ __forceinline__ void pf_copy_chunk(const PrefixParams& p, const CUten
   }
 }
 
+// The largest raw score of a thread's row of the chunk (64 columns in s0,
+// s1), over the first `valid` tokens when kMask.  Four independent
+// maxima keep the dependency chain short.
+template <bool kMask>
+__device__ __forceinline__ float pf_row_max(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
+                                            int32_t valid) {
+  float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    a[0] = fmaxf(a[0], !kMask || i < valid ? __uint_as_float(s0[i]) : -INFINITY);
+    a[1] = fmaxf(a[1], !kMask || i + 1 < valid ? __uint_as_float(s0[i + 1]) : -INFINITY);
+    a[2] = fmaxf(a[2], !kMask || i + 32 < valid ? __uint_as_float(s1[i]) : -INFINITY);
+    a[3] = fmaxf(a[3], !kMask || i + 33 < valid ? __uint_as_float(s1[i + 1]) : -INFINITY);
+  }
+  return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+}
+
+// The row's weights 2^(s * sl - m) (neg = -m), rounded to bf16 pairs: w[c]
+// holds tokens 2c (low half) and 2c + 1, the layout of the P.V product's A
+// operand in tensor memory; tokens from `valid` on weigh 0 when kMask.
+template <bool kMask>
+__device__ __forceinline__ void pf_row_weights(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
+                                               int32_t valid, float sl, float neg,
+                                               uint32_t (&w)[32]) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const uint32_t x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
+    const uint32_t x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
+    float e0 = fast_exp2(fmaf(__uint_as_float(x0), sl, neg));
+    float e1 = fast_exp2(fmaf(__uint_as_float(x1), sl, neg));
+    if (kMask) {
+      e0 = 2 * c < valid ? e0 : 0.f;
+      e1 = 2 * c + 1 < valid ? e1 : 0.f;
+    }
+    w[c] = pack_bf16x2(e0, e1);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPfThreads, 1)
     prefix_attention_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -154,7 +205,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     return;
   }
   PfBars* bars = reinterpret_cast<PfBars*>(pf_smem + L::kOffBar);
-  const uint32_t sq = base, sk = base + L::kOffK, sv = base + L::kOffV, sp = base + L::kOffP;
+  const uint32_t sq = base, sk = base + L::kOffK, sv = base + L::kOffV;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t g = blockIdx.y, split = blockIdx.z;
   const uint32_t G = static_cast<uint32_t>(p.group);
@@ -179,14 +230,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       mbar_init(smem_addr(&bars->v_empty[i]), 1);
     }
     for (int t = 0; t < kPfTiles; ++t) {
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_addr(&bars->s_full[t][i]), 1);
-        mbar_init(smem_addr(&bars->s_empty[t][i]), 4);
-      }
-      for (int i = 0; i < 2; ++i) {
-        mbar_init(smem_addr(&bars->p_full[t][i]), 4);
-        mbar_init(smem_addr(&bars->o_done[t][i]), 1);
-      }
+      mbar_init(smem_addr(&bars->s_full[t]), 1);
+      mbar_init(smem_addr(&bars->s_empty[t]), 4);
+      mbar_init(smem_addr(&bars->p_full[t]), 4);
+      mbar_init(smem_addr(&bars->o_done[t]), 1);
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
     mbar_fence_init();
@@ -199,9 +246,10 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   bool ok = true;
   uint32_t tmem = 0;
   if (warp >= 1 && warp < kPfVWarp) {
-    // The tensor memory (warp 1) and the 256 query rows (softmax warps;
-    // zeros past R), then a barrier of warps 1-9.  The producers have
-    // started meanwhile.
+    // The tensor memory (warp 1); the 256 query rows (zeros past R, negated
+    // for a negative scale) and the slabs of ones beside the V stages
+    // (softmax warps); then a barrier of warps 1-9.  The producers have
+    // started meanwhile (they write only the V stages' data slabs).
     if (warp == 1) {
       tmem_alloc(smem_addr(&bars->tmem), kPfTmemCols);
       tmem_relinquish();
@@ -209,6 +257,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       constexpr int kCpr = D * 2 / 16;
       constexpr int kSoft = 32 * kPfSoftWarps;
       constexpr int kPer = kPfTiles * kPfRows * kCpr / kSoft;  // 16-byte chunks per thread
+      const uint32_t flip = p.scale_log2 < 0.f ? 0x80008000u : 0u;
       const int t = threadIdx.x - 64;
       uint4 v[kPer];
 #pragma unroll
@@ -222,11 +271,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       for (int i = 0; i < kPer; ++i) {
         const int idx = t + kSoft * i, r = idx / kCpr, c = idx % kCpr;
         const uint32_t a = sq + (r / kPfRows) * L::kQ + pf_chunk(kPfRows, r % kPfRows, c);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v[i].x), "r"(v[i].y),
-                     "r"(v[i].z), "r"(v[i].w)
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(v[i].x ^ flip),
+                     "r"(v[i].y ^ flip), "r"(v[i].z ^ flip), "r"(v[i].w ^ flip)
                      : "memory");
       }
-      fence_proxy_async_smem();  // the MMA (async proxy) reads Q
+      for (int i = t; i < kPfVStages * L::kSlab / 16; i += kSoft) {
+        const int st = i / (L::kSlab / 16), o = i % (L::kSlab / 16);
+        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(
+                         sv + st * L::kVStage + L::kKV + o * 16),
+                     "r"(kBf16OnePair)
+                     : "memory");
+      }
+      fence_proxy_async_smem();  // the MMA (async proxy) reads Q and the ones
     }
     tc_fence_before_sync();
     asm volatile("bar.sync 1, %0;" ::"r"(32 * (kPfVWarp - 1)) : "memory");
@@ -240,6 +296,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int S = is_k ? kPfKStages : kPfVStages;
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const uint32_t ring = is_k ? sk : sv;
+    const uint32_t stride = is_k ? L::kKV : L::kVStage;
     uint64_t* full = is_k ? bars->k_full : bars->v_full;
     uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
     int32_t issued = 0;
@@ -248,7 +305,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       const int st = j % S;
       if (lane == 0 && j >= S) ok = mbar_wait(smem_addr(&empty[st]), ((j / S) - 1) & 1);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      pf_copy_chunk<D>(p, map, g, c0 + j, e, ring + st * L::kKV, smem_addr(&full[st]));
+      pf_copy_chunk<D>(p, map, g, c0 + j, e, ring + st * stride, smem_addr(&full[st]));
       issued = j + 1;
       e = en;  // the next chunk's ids, loaded a chunk ahead
       en = j + 2 < n ? pf_block_id(p, c0 + j + 2) : -1;
@@ -262,46 +319,52 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---------------------------------------------------- MMA issuer ---
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kPfRows, kPfChunk, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kPfRows, D, false, true);
-      auto issue_pv = [&](int32_t i) -> bool {
-        const int vs = i % kPfVStages;
-        if (!mbar_wait(smem_addr(&bars->v_full[vs]), (i / kPfVStages) & 1)) return false;
-        const uint32_t vb = sv + vs * L::kKV;
+      constexpr uint32_t kIdPV = idesc_bf16(kPfRows, D + 16, false, true);
+      // S_t of chunk j, once the softmax has read S_t of chunk j - 1
+      auto issue_qk = [&](int32_t j) -> bool {
+        const int ks = j % kPfKStages;
+        if (!mbar_wait(smem_addr(&bars->k_full[ks]), (j / kPfKStages) & 1)) return false;
+        const uint32_t kb = sk + ks * L::kKV;
         for (int t = 0; t < kPfTiles; ++t) {
-          if (!mbar_wait(smem_addr(&bars->p_full[t][i & 1]), (i >> 1) & 1)) return false;
-          tc_fence_after_sync();
-          const uint32_t pb = sp + (2 * t + (i & 1)) * L::kP;
-#pragma unroll
-          for (int k = 0; k < kPfChunk / 16; ++k)
-            umma_bf16(tmem + kPfTiles * 2 * kPfChunk + t * D, smem_desc_sw128(pb + k * 32, 16, 1024),
-                      smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV, i > 0 || k > 0);
-          umma_commit(smem_addr(&bars->o_done[t][i & 1]));
-        }
-        umma_commit(smem_addr(&bars->v_empty[vs]));
-        return true;
-      };
-      for (int32_t j = 0; j < n && ok; ++j) {
-        ok = mbar_wait(smem_addr(&bars->k_full[j % kPfKStages]), (j / kPfKStages) & 1);
-        const uint32_t kb = sk + (j % kPfKStages) * L::kKV;
-        for (int t = 0; t < kPfTiles && ok; ++t) {
-          if (j >= 2) ok = mbar_wait(smem_addr(&bars->s_empty[t][j & 1]), ((j - 2) >> 1) & 1);
-          if (!ok) break;
+          if (j > 0 && !mbar_wait(smem_addr(&bars->s_empty[t]), (j - 1) & 1)) return false;
           tc_fence_after_sync();
 #pragma unroll
           for (int k = 0; k < D / 16; ++k) {
             const uint32_t off = (k >> 2) * (kPfRows * 128) + (k & 3) * 32;
             const uint32_t koff = (k >> 2) * L::kSlab + (k & 3) * 32;
-            umma_bf16(tmem + (2 * t + (j & 1)) * kPfChunk,
+            umma_bf16(tmem + t * kPfTileCols + kPfSCol,
                       smem_desc_sw128(sq + t * L::kQ + off, 16, 1024),
                       smem_desc_sw128(kb + koff, 16, 1024), kIdQK, k > 0);
           }
-          umma_commit(smem_addr(&bars->s_full[t][j & 1]));
+          umma_commit(smem_addr(&bars->s_full[t]));
         }
-        if (!ok) break;
-        umma_commit(smem_addr(&bars->k_empty[j % kPfKStages]));
-        if (j >= 2) ok = issue_pv(j - 2);
+        umma_commit(smem_addr(&bars->k_empty[ks]));
+        return true;
+      };
+      // O_t (and l) += P_t . [V | 1] of chunk i, once P_t is written
+      auto issue_pv = [&](int32_t i) -> bool {
+        const int vs = i % kPfVStages;
+        if (!mbar_wait(smem_addr(&bars->v_full[vs]), (i / kPfVStages) & 1)) return false;
+        const uint32_t vb = sv + vs * L::kVStage;
+        for (int t = 0; t < kPfTiles; ++t) {
+          if (!mbar_wait(smem_addr(&bars->p_full[t]), i & 1)) return false;
+          tc_fence_after_sync();
+          const uint32_t tt = tmem + t * kPfTileCols;
+#pragma unroll
+          for (int k = 0; k < kPfChunk / 16; ++k)
+            umma_bf16_ta(tt + kPfOCol, tt + kPfPCol + k * 8,
+                         smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV,
+                         i > 0 || k > 0);
+          umma_commit(smem_addr(&bars->o_done[t]));
+        }
+        umma_commit(smem_addr(&bars->v_empty[vs]));
+        return true;
+      };
+      if (n > 0) ok = issue_qk(0);
+      for (int32_t j = 0; j < n && ok; ++j) {
+        if (j + 1 < n) ok = issue_qk(j + 1);
+        if (ok) ok = issue_pv(j);
       }
-      for (int32_t i = n > 2 ? n - 2 : 0; i < n && ok; ++i) ok = issue_pv(i);
       // every MMA this thread issued has completed before the tensor
       // memory is released
       umma_commit(smem_addr(&bars->mma_done));
@@ -313,134 +376,106 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int tile = (warp - 2) >> 2;
     const int quarter = warp & 3;  // tensor-memory lanes 32 * quarter ...
     const int r = 32 * quarter + lane;  // row within the tile
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
-    const uint32_t o_col = kPfTiles * 2 * kPfChunk + tile * D;
-    const uint32_t prow0 = sp + 2 * tile * L::kP + r * 128;  // this thread's P row, buffer 0
-    float m = -INFINITY, l = 0.f;
+    const uint32_t tb =
+        tmem + (static_cast<uint32_t>(32 * quarter) << 16) + tile * kPfTileCols;
+    const float sl = fabsf(p.scale_log2);
+    float m = -INFINITY;
     for (int32_t j = 0; j < n; ++j) {
-      ok = mbar_wait(smem_addr(&bars->s_full[tile][j & 1]), (j >> 1) & 1);
+      ok = mbar_wait(smem_addr(&bars->s_full[tile]), j & 1);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
-      const uint32_t s_col = lane_base + (2 * tile + (j & 1)) * kPfChunk;
+      uint32_t s0[32], s1[32];
+      tmem_ld32(tb + kPfSCol, s0);
+      tmem_ld32(tb + kPfSCol + 32, s1);
+      tmem_wait_ld();
+      // S is in registers: its columns may take the next chunk's scores
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&bars->s_empty[tile]));
       const int32_t valid = p.prefix_tokens - (c0 + j) * kPfChunk;  // tokens of the chunk
-      // pass 1: the chunk's max score (log2 units), 32 columns at a time;
-      // tokens past the prefix are masked after the scaling (-inf * 0 would
-      // be NaN)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int part = 0; part < kPfChunk / 32; ++part) {
-        uint32_t u[32];
-        tmem_ld32(s_col + part * 32, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float x = __uint_as_float(u[i]) * p.scale_log2;
-          mx = fmaxf(mx, part * 32 + i < valid ? x : -INFINITY);
-        }
-      }
-      // P_j goes to buffer j & 1, which the tile's product of chunk j - 2
-      // reads: that product must be complete
-      if (j >= 2) {
-        ok = mbar_wait(smem_addr(&bars->o_done[tile][j & 1]), ((j - 2) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-      }
+      const bool part = valid < kPfChunk;  // the prefix's last, partial chunk
+      const float mx = (part ? pf_row_max<true>(s0, s1, valid) : pf_row_max<false>(s0, s1, valid)) * sl;
+      bool resc = false;
+      float alpha = 1.f;
       if (j == 0) {
         m = mx;
       } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
-        // the running max moves: O_t and l scale, once the tile's product
-        // of chunk j - 1 has updated O_t
         const float mn = fmaxf(m, mx);
-        const float alpha = fast_exp2(m - mn);
+        alpha = fast_exp2(m - mn);
         m = mn;
-        l *= alpha;
-        ok = mbar_wait(smem_addr(&bars->o_done[tile][(j - 1) & 1]), ((j - 1) >> 1) & 1);
+        resc = true;
+      }
+      uint32_t w[32];
+      if (part)
+        pf_row_weights<true>(s0, s1, valid, sl, -m, w);
+      else
+        pf_row_weights<false>(s0, s1, valid, sl, -m, w);
+      // P's columns are free, and O holds the product of chunk j - 1, once
+      // that product has completed
+      if (j > 0) {
+        ok = mbar_wait(smem_addr(&bars->o_done[tile]), (j - 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
+      }
+      if (resc) {  // the running max moved: O and the row sums scale by alpha
 #pragma unroll 1
-        for (int part = 0; part < D / 32; ++part) {
+        for (int c = 0; c < D / 32; ++c) {
           uint32_t u[32];
-          const uint32_t ta = lane_base + o_col + part * 32;
-          tmem_ld32(ta, u);
+          tmem_ld32(tb + kPfOCol + 32 * c, u);
           tmem_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-          tmem_st32(ta, u);
+          tmem_st32(tb + kPfOCol + 32 * c, u);
         }
-        tmem_wait_st();
-      }
-      // pass 2: P = 2^(s - m) rounded to bf16 into this row of the P tile,
-      // 32 columns (four 16-byte chunks) at a time
-      const float neg_m = -m;
-      float lsum = 0.f;
-#pragma unroll 1
-      for (int part = 0; part < kPfChunk / 32; ++part) {
-        uint32_t u[32];
-        tmem_ld32(s_col + part * 32, u);
+        uint32_t u[16];
+        tmem_ld16(tb + kPfOCol + D, u);
         tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t w[4];
-#pragma unroll
-          for (int h = 0; h < 4; ++h) {
-            const int i = 8 * c + 2 * h;
-            const float x0 = part * 32 + i < valid ? __uint_as_float(u[i]) * p.scale_log2 : -INFINITY;
-            const float x1 =
-                part * 32 + i + 1 < valid ? __uint_as_float(u[i + 1]) * p.scale_log2 : -INFINITY;
-            w[h] = pack_bf16x2(fast_exp2(x0 + neg_m), fast_exp2(x1 + neg_m));
-            const float2 f = unpack_bf16x2(w[h]);  // sum exactly the weights the MMA applies
-            lsum += f.x + f.y;
-          }
-          const int cc = part * 4 + c;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           prow0 + (j & 1) * L::kP + ((cc ^ (r & 7)) << 4)),
-                       "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
-                       : "memory");
-        }
+        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
+        tmem_st16(tb + kPfOCol + D, u);
       }
-      // both passes have read S: its buffer may take the scores two chunks on
+      tmem_st32(tb + kPfPCol, w);
+      tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bars->s_empty[tile][j & 1]));
-      l += lsum;
-      fence_proxy_async_smem();  // the MMA (async proxy) reads P
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile][j & 1]));
+      if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile]));
     }
     // every product of both tiles is complete (the staging below reuses the
     // K and V rings that the other tile's last products may still read)
     ok = mbar_wait(smem_addr(&bars->mma_done), 0) && ok;
     ok = __all_sync(0xffffffffu, ok);
-    // (m, l) of each row into the (free) K ring
-    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] = make_float2(m, l);
+    // (m, l) of each row into the (free) K ring; l from the row-sum columns
+    tc_fence_after_sync();
+    uint32_t lv[8];
+    tmem_ld8(tb + kPfOCol + D, lv);
+    tmem_wait_ld();
+    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] =
+        make_float2(m, n > 0 ? __uint_as_float(lv[0]) : 0.f);
   }
   // ---- epilogue, one query tile at a time: its rows' partials (o
-  // unnormalised) are staged in the P buffers (float rows of D, 16-byte chunk
-  // c of row r at chunk c ^ (r % (D/4))), then written to this split's slot
-  // with coalesced stores (softmax warp w rows w, w + 8, ...; lane l its
-  // 16-byte chunk).
+  // unnormalised) are staged in the (free) V ring (float rows of D, 16-byte
+  // chunk c of row r at chunk c ^ (r % (D/4))), then written to this
+  // split's slot with coalesced stores (softmax warp w rows w, w + 8, ...;
+  // lane l its 16-byte chunk).
   constexpr int kCh = D / 4;
-  const uint32_t stage_addr = base + L::kOffP;
+  const uint32_t stage_addr = sv;
   const int64_t slot = static_cast<int64_t>(split) * p.num_seqs * p.num_q_heads;
   const bool soft = warp >= 2 && warp < kPfVWarp;
   for (int t = 0; t < kPfTiles; ++t) {
     if (soft && ((warp - 2) >> 2) == t && ok && n > 0) {
       const int quarter = warp & 3, r = 32 * quarter + lane;
-      const uint32_t lane_base = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+      const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + t * kPfTileCols;
       tc_fence_after_sync();
 #pragma unroll
       for (int part = 0; part < D / 32; ++part) {
         uint32_t u[32];
-        tmem_ld32(lane_base + kPfTiles * 2 * kPfChunk + t * D + part * 32, u);
+        tmem_ld32(tb + kPfOCol + part * 32, u);
         tmem_wait_ld();
 #pragma unroll
         for (int i = 0; i < 8; ++i) {

@@ -94,9 +94,10 @@ def snapshot_blocks(case: Case, seqs):
     return ids, _to_np32(case.k_cache.index_select(0, idx)), _to_np32(case.v_cache.index_select(0, idx))
 
 
-def oracle_decode(case: Case, snap, seqs, heads=None, with_append=True, lens=None):
+def oracle_decode(case: Case, snap, seqs, heads=None, with_append=True, lens=None, scale=None):
     """fp64 oracle output [B, Hq, d] (NaN outside ``seqs``/``heads``).
-    ``lens`` overrides the workload's post-append lengths."""
+    ``lens`` overrides the workload's post-append lengths, ``scale`` its
+    softmax scale."""
     ids, kk, vv = snap
     local = {bid: i for i, bid in enumerate(ids)}
     bs = case.w.block_size
@@ -112,8 +113,8 @@ def oracle_decode(case: Case, snap, seqs, heads=None, with_append=True, lens=Non
             sl[b] = local[s // bs] * bs + s % bs
         kk, vv = OPA.cache_write(_to_np32(case.k_new), _to_np32(case.v_new), sl, kk, vv)
     lens = np.array(case.w.seq_lens if lens is None else lens)
-    return OPA.decode(_to_np64(case.q), kk, vv, tab, lens, case.w.scale,
-                      seqs=seqs, heads=heads)
+    return OPA.decode(_to_np64(case.q), kk, vv, tab, lens,
+                      case.w.scale if scale is None else scale, seqs=seqs, heads=heads)
 
 
 def oracle_decode_fp8(case: Case, snap, seqs, heads=None):

@@ -5,7 +5,8 @@ nothing of prefixes: it attends over each sequence's whole gathered cache.
 
 Cases: the shared-prefix workload (256 forks of a 2048-token prompt) at
 block sizes 8, 16 and 32 with automatic and fixed partition counts;
-head_dim 64; a cascade prefix shorter than the shared one; sequences that
+head_dim 64; negative and zero scales; a cascade prefix shorter than the
+shared one (down to a partial last chunk); sequences that
 end exactly at the prefix (prefix partial alone) and one shorter than it
 (zeros, flagged); agreement with pa_decode on the same inputs.
 """
@@ -40,11 +41,12 @@ def _out(w):
                       dtype=torch.bfloat16, device="cuda")
 
 
-def _cascade(case, prefix_len, splits=0, lens=None):
+def _cascade(case, prefix_len, splits=0, lens=None, scale=None):
     w = case.w
     out = _out(w)
     pa.pa_decode_cascade(case.q, case.k_cache, case.v_cache, case.table_t,
-                         case.lens_t if lens is None else lens, prefix_len, w.scale, out,
+                         case.lens_t if lens is None else lens, prefix_len,
+                         w.scale if scale is None else scale, out,
                          _ws(w, splits, prefix_len), num_splits=splits)
     torch.cuda.synchronize()
     return out
@@ -77,6 +79,22 @@ def test_cascade_agrees_with_decode_and_shorter_prefix():
     assert_close(dec, ref, TOL, "plain decode of the forked batch")
     for prefix_len in (512, 256, 16):   # any whole-block part of the shared prefix
         assert_close(_cascade(case, prefix_len), ref, TOL, f"cascade prefix {prefix_len}")
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("sign", [-1.0, 0.0])
+def test_cascade_negative_and_zero_scale(sign):
+    # the prefix pass applies a negative scale as its magnitude to the
+    # negated query; a zero scale weighs every token alike (also in the
+    # prefix's last, partial chunk: 528 = 8 chunks + 16 tokens)
+    case = build_case(W.shared_prefix(16, num_seqs=48, prefix=528))
+    w = case.w
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
+    pa.pa_cache_write(case.k_new, case.v_new, case.slots_t, case.k_cache, case.v_cache)
+    scale = sign * w.scale
+    ref = oracle_decode(case, snap, seqs, scale=scale)
+    assert_close(_cascade(case, 528, scale=scale), ref, TOL, f"cascade scale {scale}")
     assert pa.pa_get_device_error() == 0
 
 
