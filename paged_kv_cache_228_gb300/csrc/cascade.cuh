@@ -14,29 +14,32 @@
 // GB300 design: the two products run on the fifth-generation tensor cores
 // (tcgen05.mma, kind::f16, M = 128 query rows, fp32 accumulators in tensor
 // memory).  Q, K and V sit in shared memory in the 128-byte-swizzled layout
-// the TMA writes; P stays in tensor memory, where the softmax stores it and
-// the P.V product reads it as its A operand, so it costs no shared-memory
-// bandwidth.  A CTA makes each copied byte serve two 128-row query tiles:
-// it owns 256 query rows of one KV head and one of S token ranges of the
-// prefix, walked in 64-token chunks.  Eleven warps:
+// the TMA writes.  A CTA makes each copied byte serve two 128-row query
+// tiles: it owns 256 query rows of one KV head and one of S token ranges of
+// the prefix, walked in 128-token chunks (N = 128 per score MMA: half the
+// MMA instructions per token of 64-token chunks, and each instruction and
+// each barrier round trip has a fixed cost).  Per query tile the tensor
+// memory holds S of the chunk, overwritten in place by P (bf16, the A
+// operand of the P.V product), and O.  Eleven warps:
 //   warps 0/10 TMA producers of K and of V (one 2D box per block and
-//              64-column slab) into 3-stage K and V rings;
+//              64-column slab) into K and V rings;
 //   warp 1     owns the tensor memory; lane 0 issues the MMAs, per chunk j
-//              and query tile t:
-//                S_t   = Q_t . K_j^T                 (A, B K-major; N = 64)
-//                O_t  += P_t,j . [V_j | 1]           (P in tensor memory,
-//                                                     V MN-major; N = D + 16)
-//              S of chunk j + 1 as soon as the softmax has read S_t,j, the
-//              product of chunk j when P_t,j is written.  The 16 extra
-//              columns multiply P by a slab of ones kept beside each V
-//              stage: they accumulate the row sum l of exactly the bf16
-//              weights the product applies, rescaled with O;
+//              and query tile t, once the softmax has written P_t,j:
+//                O_t  += P_t,j . V_j                 (P in tensor memory,
+//                                                     V MN-major; N = D)
+//                S_t   = Q_t . K_j+1^T               (A, B K-major; N = 128)
+//              in that order: the tensor pipe runs them in issue order, so
+//              the scores of chunk j + 1 land in the columns of P_t,j only
+//              after the product has read it, and their completion also
+//              means the product is done;
 //   warps 2-9  softmax, four warps per query tile, one row per thread (the
-//              warp's quarter of the tensor-memory lanes): the chunk's 64
-//              scores in one read, their maximum, then 2^(s.scale - m)
-//              rounded to bf16 pairs into the tile's P columns.  The running
-//              max m moves, and O_t (with l) is rescaled in tensor memory,
-//              only when a score exceeds it by more than 8 in log2 units.
+//              warp's quarter of the tensor-memory lanes): the chunk's
+//              maximum in a first read of S, then 2^(s.scale - m) rounded to
+//              bf16 pairs, written over S 32 columns at a time, and the sum
+//              l of exactly those rounded weights.  The running max m moves,
+//              and O_t is rescaled in tensor memory, only when a score
+//              exceeds it by more than 8 in log2 units.  While one tile's
+//              softmax runs, the tensor pipe works on the other tile.
 // A negative scale is applied as its magnitude to the negated query (exact
 // in bf16), so the maximum of a chunk is that of its raw scores.
 // Each split writes its own partial per row (staged through shared memory
@@ -64,38 +67,34 @@ struct PrefixParams {
 
 constexpr int kPfRows = 128;    // query rows per tile (the MMA's M)
 constexpr int kPfTiles = 2;     // query tiles per CTA sharing each K/V chunk
-constexpr int kPfChunk = 64;    // prefix tokens per chunk
+constexpr int kPfChunk = 128;   // prefix tokens per chunk
 constexpr int kPfKStages = 3;   // K ring depth
-constexpr int kPfVStages = 3;   // V ring depth
+constexpr int kPfVStages = 2;   // V ring depth
 constexpr int kPfSoftWarps = 4 * kPfTiles;
 constexpr int kPfThreads = 96 + 32 * kPfSoftWarps;  // K and V producers, MMA, softmax
 constexpr int kPfVWarp = 2 + kPfSoftWarps;
-// Tensor memory per query tile (256 columns each): O (D fp32) and its 16
-// row-sum columns, S of the chunk (64 fp32) and P (64 bf16 = 32 columns).
+// Tensor memory per query tile (256 columns each): S of the chunk (128
+// fp32, P in its first 64 columns once written), then O (D fp32).
 constexpr int kPfTileCols = 256;
-constexpr int kPfOCol = 0;
-constexpr int kPfSCol = 160;
-constexpr int kPfPCol = 224;
+constexpr int kPfSCol = 0;
+constexpr int kPfOCol = 128;
 constexpr int kPfTmemCols = 512;
 constexpr int kPfMaxSplits = 8;
-constexpr uint32_t kBf16OnePair = 0x3F803F80u;  // two bf16 ones
 
 template <int D>
 struct PfSmem {
   static constexpr int kSlab = kPfChunk * 128;        // 64 columns of one chunk
   static constexpr int kKV = (D / 64) * kSlab;        // K (or V) of a chunk
-  static constexpr int kVStage = kKV + kSlab;         // V, then a slab of ones
   static constexpr int kQ = (D / 64) * kPfRows * 128; // one query tile
   static constexpr int kOffK = kPfTiles * kQ;
   static constexpr int kOffV = kOffK + kPfKStages * kKV;
-  static constexpr int kOffBar = kOffV + kPfVStages * kVStage;
+  static constexpr int kOffBar = kOffV + kPfVStages * kKV;
   static constexpr int kBytes = kOffBar + 256;
   // the epilogue stages one tile's partial in the (free) V ring, and the
   // per-row (m, l) in the (free) K ring
-  static_assert(kPfRows * D * 4 <= kPfVStages * kVStage, "epilogue staging");
+  static_assert(kPfRows * D * 4 <= kPfVStages * kKV, "epilogue staging");
   static_assert(kPfTiles * kPfRows * 8 <= kPfKStages * kKV, "epilogue (m, l)");
-  static_assert(kPfOCol + D + 16 <= kPfSCol && kPfSCol + kPfChunk <= kPfPCol &&
-                    kPfPCol + kPfChunk / 2 <= kPfTileCols,
+  static_assert(kPfSCol + kPfChunk <= kPfOCol && kPfOCol + D <= kPfTileCols,
                 "tensor-memory columns");
   static_assert(kBytes <= 227 * 1024, "shared memory");
 };
@@ -103,9 +102,8 @@ struct PfSmem {
 struct PfBars {
   uint64_t k_full[kPfKStages], k_empty[kPfKStages];
   uint64_t v_full[kPfVStages], v_empty[kPfVStages];
-  uint64_t s_full[kPfTiles], s_empty[kPfTiles];  // S of the tile's chunk written / read
-  uint64_t p_full[kPfTiles];                     // P of the tile's chunk written
-  uint64_t o_done[kPfTiles];                     // the tile's product of that P complete
+  uint64_t s_full[kPfTiles];  // S of the tile's chunk written (and its last product done)
+  uint64_t p_full[kPfTiles];  // P of the tile's chunk written
   uint64_t mma_done;
   uint32_t tmem;
 };
@@ -155,41 +153,39 @@ __device__ __forceinline__ void pf_copy_chunk(const PrefixParams& p, const CUten
   }
 }
 
-// The largest raw score of a thread's row of the chunk (64 columns in s0,
-// s1), over the first `valid` tokens when kMask.  Four independent
-// maxima keep the dependency chain short.
+// The largest raw score among 32 columns of a thread's row (chunk columns
+// c0 .. c0 + 31), over those before `valid` when kMask, folded into `acc`.
+// Four independent maxima keep the dependency chain short.
 template <bool kMask>
-__device__ __forceinline__ float pf_row_max(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
-                                            int32_t valid) {
-  float a[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+__device__ __forceinline__ float pf_max32(const uint32_t (&u)[32], int32_t c0, int32_t valid,
+                                          float acc) {
+  float a[4] = {acc, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    a[0] = fmaxf(a[0], !kMask || i < valid ? __uint_as_float(s0[i]) : -INFINITY);
-    a[1] = fmaxf(a[1], !kMask || i + 1 < valid ? __uint_as_float(s0[i + 1]) : -INFINITY);
-    a[2] = fmaxf(a[2], !kMask || i + 32 < valid ? __uint_as_float(s1[i]) : -INFINITY);
-    a[3] = fmaxf(a[3], !kMask || i + 33 < valid ? __uint_as_float(s1[i + 1]) : -INFINITY);
-  }
+  for (int i = 0; i < 32; ++i)
+    a[i & 3] = fmaxf(a[i & 3], !kMask || c0 + i < valid ? __uint_as_float(u[i]) : -INFINITY);
   return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
 }
 
-// The row's weights 2^(s * sl - m) (neg = -m), rounded to bf16 pairs: w[c]
-// holds tokens 2c (low half) and 2c + 1, the layout of the P.V product's A
-// operand in tensor memory; tokens from `valid` on weigh 0 when kMask.
+// The weights 2^(s * sl - m) (neg = -m) of 32 columns, rounded to bf16
+// pairs: w[c] holds columns 2c (low half) and 2c + 1, the layout of the
+// P.V product's A operand in tensor memory; columns from `valid` on weigh
+// 0 when kMask.  l0 + l1 gains the sum of the rounded weights.
 template <bool kMask>
-__device__ __forceinline__ void pf_row_weights(const uint32_t (&s0)[32], const uint32_t (&s1)[32],
-                                               int32_t valid, float sl, float neg,
-                                               uint32_t (&w)[32]) {
+__device__ __forceinline__ void pf_weights32(const uint32_t (&u)[32], int32_t c0, int32_t valid,
+                                             float sl, float neg, uint32_t (&w)[16], float& l0,
+                                             float& l1) {
 #pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const uint32_t x0 = c < 16 ? s0[2 * c] : s1[2 * c - 32];
-    const uint32_t x1 = c < 16 ? s0[2 * c + 1] : s1[2 * c - 31];
-    float e0 = fast_exp2(fmaf(__uint_as_float(x0), sl, neg));
-    float e1 = fast_exp2(fmaf(__uint_as_float(x1), sl, neg));
+  for (int c = 0; c < 16; ++c) {
+    float e0 = fast_exp2(fmaf(__uint_as_float(u[2 * c]), sl, neg));
+    float e1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl, neg));
     if (kMask) {
-      e0 = 2 * c < valid ? e0 : 0.f;
-      e1 = 2 * c + 1 < valid ? e1 : 0.f;
+      e0 = c0 + 2 * c < valid ? e0 : 0.f;
+      e1 = c0 + 2 * c + 1 < valid ? e1 : 0.f;
     }
     w[c] = pack_bf16x2(e0, e1);
+    const float2 f = unpack_bf16x2(w[c]);
+    l0 += f.x;
+    l1 += f.y;
   }
 }
 
@@ -214,6 +210,11 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   const int32_t c0 = static_cast<int32_t>(static_cast<int64_t>(p.prefix_chunks) * split / p.splits);
   const int32_t c1 = static_cast<int32_t>(static_cast<int64_t>(p.prefix_chunks) * (split + 1) / p.splits);
   const int32_t n = c1 - c0;
+  // The CTAs of one token range (one per 256 query rows) walk its chunks
+  // from different starting points, so that they do not all ask for the
+  // same lines at the same moment; the log-sum-exp fold is order-free.
+  const int32_t rot = n > 0 ? static_cast<int32_t>(static_cast<int64_t>(blockIdx.x) * n / gridDim.x) : 0;
+  auto chunk = [&](int32_t j) -> int32_t { return c0 + (j + rot < n ? j + rot : j + rot - n); };
   // q / partial row of CTA row r (r < R - row0): sequence b, head g*G + j
   auto head_row = [&](uint32_t r) -> int64_t {
     const uint32_t gr = row0 + r, b = gr / G, j = gr - b * G;
@@ -231,9 +232,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     }
     for (int t = 0; t < kPfTiles; ++t) {
       mbar_init(smem_addr(&bars->s_full[t]), 1);
-      mbar_init(smem_addr(&bars->s_empty[t]), 4);
       mbar_init(smem_addr(&bars->p_full[t]), 4);
-      mbar_init(smem_addr(&bars->o_done[t]), 1);
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
     mbar_fence_init();
@@ -246,10 +245,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
   bool ok = true;
   uint32_t tmem = 0;
   if (warp >= 1 && warp < kPfVWarp) {
-    // The tensor memory (warp 1); the 256 query rows (zeros past R, negated
-    // for a negative scale) and the slabs of ones beside the V stages
-    // (softmax warps); then a barrier of warps 1-9.  The producers have
-    // started meanwhile (they write only the V stages' data slabs).
+    // The tensor memory (warp 1) and the 256 query rows (softmax warps;
+    // zeros past R, negated for a negative scale), then a barrier of warps
+    // 1-9.  The producers have started meanwhile.
     if (warp == 1) {
       tmem_alloc(smem_addr(&bars->tmem), kPfTmemCols);
       tmem_relinquish();
@@ -275,14 +273,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
                      "r"(v[i].y ^ flip), "r"(v[i].z ^ flip), "r"(v[i].w ^ flip)
                      : "memory");
       }
-      for (int i = t; i < kPfVStages * L::kSlab / 16; i += kSoft) {
-        const int st = i / (L::kSlab / 16), o = i % (L::kSlab / 16);
-        asm volatile("st.shared.v4.b32 [%0], {%1,%1,%1,%1};" ::"r"(
-                         sv + st * L::kVStage + L::kKV + o * 16),
-                     "r"(kBf16OnePair)
-                     : "memory");
-      }
-      fence_proxy_async_smem();  // the MMA (async proxy) reads Q and the ones
+      fence_proxy_async_smem();  // the MMA (async proxy) reads Q
     }
     tc_fence_before_sync();
     asm volatile("bar.sync 1, %0;" ::"r"(32 * (kPfVWarp - 1)) : "memory");
@@ -296,19 +287,18 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const int S = is_k ? kPfKStages : kPfVStages;
     const CUtensorMap* map = is_k ? &tm_k : &tm_v;
     const uint32_t ring = is_k ? sk : sv;
-    const uint32_t stride = is_k ? L::kKV : L::kVStage;
     uint64_t* full = is_k ? bars->k_full : bars->v_full;
     uint64_t* empty = is_k ? bars->k_empty : bars->v_empty;
     int32_t issued = 0;
-    int32_t e = pf_block_id(p, c0), en = n > 1 ? pf_block_id(p, c0 + 1) : -1;
+    int32_t e = n > 0 ? pf_block_id(p, chunk(0)) : -1, en = n > 1 ? pf_block_id(p, chunk(1)) : -1;
     for (int32_t j = 0; j < n && ok; ++j) {
       const int st = j % S;
       if (lane == 0 && j >= S) ok = mbar_wait(smem_addr(&empty[st]), ((j / S) - 1) & 1);
       if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-      pf_copy_chunk<D>(p, map, g, c0 + j, e, ring + st * stride, smem_addr(&full[st]));
+      pf_copy_chunk<D>(p, map, g, chunk(j), e, ring + st * L::kKV, smem_addr(&full[st]));
       issued = j + 1;
       e = en;  // the next chunk's ids, loaded a chunk ahead
-      en = j + 2 < n ? pf_block_id(p, c0 + j + 2) : -1;
+      en = j + 2 < n ? pf_block_id(p, chunk(j + 2)) : -1;
     }
     // No copy may still target shared memory when the CTA exits: on the
     // normal path the MMAs have consumed every one already.
@@ -319,51 +309,51 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // ---------------------------------------------------- MMA issuer ---
     if (lane == 0) {
       constexpr uint32_t kIdQK = idesc_bf16(kPfRows, kPfChunk, false, false);
-      constexpr uint32_t kIdPV = idesc_bf16(kPfRows, D + 16, false, true);
-      // S_t of chunk j, once the softmax has read S_t of chunk j - 1
-      auto issue_qk = [&](int32_t j) -> bool {
-        const int ks = j % kPfKStages;
-        if (!mbar_wait(smem_addr(&bars->k_full[ks]), (j / kPfKStages) & 1)) return false;
-        const uint32_t kb = sk + ks * L::kKV;
-        for (int t = 0; t < kPfTiles; ++t) {
-          if (j > 0 && !mbar_wait(smem_addr(&bars->s_empty[t]), (j - 1) & 1)) return false;
-          tc_fence_after_sync();
+      constexpr uint32_t kIdPV = idesc_bf16(kPfRows, D, false, true);
+      // S_t = Q_t . K^T of the chunk whose K sits at kb
+      auto qk = [&](int t, uint32_t kb) {
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t off = (k >> 2) * (kPfRows * 128) + (k & 3) * 32;
-            const uint32_t koff = (k >> 2) * L::kSlab + (k & 3) * 32;
-            umma_bf16(tmem + t * kPfTileCols + kPfSCol,
-                      smem_desc_sw128(sq + t * L::kQ + off, 16, 1024),
-                      smem_desc_sw128(kb + koff, 16, 1024), kIdQK, k > 0);
-          }
-          umma_commit(smem_addr(&bars->s_full[t]));
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t off = (k >> 2) * (kPfRows * 128) + (k & 3) * 32;
+          const uint32_t koff = (k >> 2) * L::kSlab + (k & 3) * 32;
+          umma_bf16(tmem + t * kPfTileCols + kPfSCol,
+                    smem_desc_sw128(sq + t * L::kQ + off, 16, 1024),
+                    smem_desc_sw128(kb + koff, 16, 1024), kIdQK, k > 0);
         }
-        umma_commit(smem_addr(&bars->k_empty[ks]));
-        return true;
+        umma_commit(smem_addr(&bars->s_full[t]));
       };
-      // O_t (and l) += P_t . [V | 1] of chunk i, once P_t is written
-      auto issue_pv = [&](int32_t i) -> bool {
-        const int vs = i % kPfVStages;
-        if (!mbar_wait(smem_addr(&bars->v_full[vs]), (i / kPfVStages) & 1)) return false;
-        const uint32_t vb = sv + vs * L::kVStage;
-        for (int t = 0; t < kPfTiles; ++t) {
-          if (!mbar_wait(smem_addr(&bars->p_full[t]), i & 1)) return false;
+      if (n > 0) {
+        ok = mbar_wait(smem_addr(&bars->k_full[0]), 0);
+        if (ok) {
+          tc_fence_after_sync();
+          for (int t = 0; t < kPfTiles; ++t) qk(t, sk);
+          umma_commit(smem_addr(&bars->k_empty[0]));
+        }
+      }
+      for (int32_t j = 0; j < n && ok; ++j) {
+        const int vs = j % kPfVStages, ks = (j + 1) % kPfKStages;
+        const bool more = j + 1 < n;
+        const uint32_t vb = sv + vs * L::kKV, kb = sk + ks * L::kKV;
+        ok = mbar_wait(smem_addr(&bars->v_full[vs]), (j / kPfVStages) & 1);
+        for (int t = 0; t < kPfTiles && ok; ++t) {
+          // P_t of chunk j written (over S_t); then its product and the
+          // scores of chunk j + 1, in that order
+          ok = mbar_wait(smem_addr(&bars->p_full[t]), j & 1);
+          if (ok && more && t == 0)
+            ok = mbar_wait(smem_addr(&bars->k_full[ks]), ((j + 1) / kPfKStages) & 1);
+          if (!ok) break;
           tc_fence_after_sync();
           const uint32_t tt = tmem + t * kPfTileCols;
 #pragma unroll
           for (int k = 0; k < kPfChunk / 16; ++k)
-            umma_bf16_ta(tt + kPfOCol, tt + kPfPCol + k * 8,
+            umma_bf16_ta(tt + kPfOCol, tt + kPfSCol + k * 8,
                          smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV,
-                         i > 0 || k > 0);
-          umma_commit(smem_addr(&bars->o_done[t]));
+                         j > 0 || k > 0);
+          if (more) qk(t, kb);
         }
+        if (!ok) break;
         umma_commit(smem_addr(&bars->v_empty[vs]));
-        return true;
-      };
-      if (n > 0) ok = issue_qk(0);
-      for (int32_t j = 0; j < n && ok; ++j) {
-        if (j + 1 < n) ok = issue_qk(j + 1);
-        if (ok) ok = issue_pv(j);
+        if (more) umma_commit(smem_addr(&bars->k_empty[ks]));
       }
       // every MMA this thread issued has completed before the tensor
       // memory is released
@@ -379,7 +369,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tb =
         tmem + (static_cast<uint32_t>(32 * quarter) << 16) + tile * kPfTileCols;
     const float sl = fabsf(p.scale_log2);
-    float m = -INFINITY;
+    float m = -INFINITY, l0 = 0.f, l1 = 0.f;
     for (int32_t j = 0; j < n; ++j) {
       ok = mbar_wait(smem_addr(&bars->s_full[tile]), j & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -387,43 +377,30 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      uint32_t s0[32], s1[32];
-      tmem_ld32(tb + kPfSCol, s0);
-      tmem_ld32(tb + kPfSCol + 32, s1);
-      tmem_wait_ld();
-      // S is in registers: its columns may take the next chunk's scores
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&bars->s_empty[tile]));
-      const int32_t valid = p.prefix_tokens - (c0 + j) * kPfChunk;  // tokens of the chunk
+      const int32_t valid = p.prefix_tokens - chunk(j) * kPfChunk;  // tokens of the chunk
       const bool part = valid < kPfChunk;  // the prefix's last, partial chunk
-      const float mx = (part ? pf_row_max<true>(s0, s1, valid) : pf_row_max<false>(s0, s1, valid)) * sl;
-      bool resc = false;
-      float alpha = 1.f;
+      // pass 1: the chunk's largest score
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < kPfChunk / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tb + kPfSCol + 32 * c, u);
+        tmem_wait_ld();
+        mx = part ? pf_max32<true>(u, 32 * c, valid, mx) : pf_max32<false>(u, 32 * c, valid, mx);
+      }
+      mx *= sl;
       if (j == 0) {
         m = mx;
       } else if (__any_sync(0xffffffffu, mx > m + 8.f)) {
+        // the running max moves: O and l scale by alpha.  O holds the
+        // products through chunk j - 1, all complete (the scores of chunk
+        // j were issued after them), and the product of chunk j waits for
+        // this warp's P.
         const float mn = fmaxf(m, mx);
-        alpha = fast_exp2(m - mn);
+        const float alpha = fast_exp2(m - mn);
         m = mn;
-        resc = true;
-      }
-      uint32_t w[32];
-      if (part)
-        pf_row_weights<true>(s0, s1, valid, sl, -m, w);
-      else
-        pf_row_weights<false>(s0, s1, valid, sl, -m, w);
-      // P's columns are free, and O holds the product of chunk j - 1, once
-      // that product has completed
-      if (j > 0) {
-        ok = mbar_wait(smem_addr(&bars->o_done[tile]), (j - 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-      }
-      if (resc) {  // the running max moved: O and the row sums scale by alpha
+        l0 *= alpha;
+        l1 *= alpha;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t u[32];
@@ -433,14 +410,21 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           for (int i = 0; i < 32; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
           tmem_st32(tb + kPfOCol + 32 * c, u);
         }
-        uint32_t u[16];
-        tmem_ld16(tb + kPfOCol + D, u);
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(__uint_as_float(u[i]) * alpha);
-        tmem_st16(tb + kPfOCol + D, u);
       }
-      tmem_st32(tb + kPfPCol, w);
+      // pass 2: P over the first half of S, 32 scores (16 columns of P) at
+      // a time; P's columns 16c .. 16c + 15 lie among scores already read
+      const float neg = -m;
+#pragma unroll 1
+      for (int c = 0; c < kPfChunk / 32; ++c) {
+        uint32_t u[32], w[16];
+        tmem_ld32(tb + kPfSCol + 32 * c, u);
+        tmem_wait_ld();
+        if (part)
+          pf_weights32<true>(u, 32 * c, valid, sl, neg, w, l0, l1);
+        else
+          pf_weights32<false>(u, 32 * c, valid, sl, neg, w, l0, l1);
+        tmem_st16(tb + kPfSCol + 16 * c, w);
+      }
       tmem_wait_st();
       tc_fence_before_sync();
       __syncwarp();
@@ -450,13 +434,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     // K and V rings that the other tile's last products may still read)
     ok = mbar_wait(smem_addr(&bars->mma_done), 0) && ok;
     ok = __all_sync(0xffffffffu, ok);
-    // (m, l) of each row into the (free) K ring; l from the row-sum columns
-    tc_fence_after_sync();
-    uint32_t lv[8];
-    tmem_ld8(tb + kPfOCol + D, lv);
-    tmem_wait_ld();
-    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] =
-        make_float2(m, n > 0 ? __uint_as_float(lv[0]) : 0.f);
+    // (m, l) of each row into the (free) K ring
+    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] = make_float2(m, l0 + l1);
   }
   // ---- epilogue, one query tile at a time: its rows' partials (o
   // unnormalised) are staged in the (free) V ring (float rows of D, 16-byte
