@@ -90,10 +90,12 @@ struct PfSmem {
   static constexpr int kOffV = kOffK + kPfKStages * kKV;
   static constexpr int kOffBar = kOffV + kPfVStages * kKV;
   static constexpr int kBytes = kOffBar + 256;
-  // the epilogue stages one tile's partial in the (free) V ring, and the
-  // per-row (m, l) in the (free) K ring
-  static_assert(kPfRows * D * 4 <= kPfVStages * kKV, "epilogue staging");
-  static_assert(kPfTiles * kPfRows * 8 <= kPfKStages * kKV, "epilogue (m, l)");
+  // the epilogue stages tile 0's partial in the (free) V ring, tile 1's in
+  // the (free) K ring and the per-row (m, l) where Q was
+  static_assert(kPfTiles == 2 && kPfRows * D * 4 <= kPfVStages * kKV &&
+                    kPfRows * D * 4 <= kPfKStages * kKV,
+                "epilogue staging");
+  static_assert(kPfTiles * kPfRows * 8 <= kPfTiles * kQ, "epilogue (m, l)");
   static_assert(kPfSCol + kPfChunk <= kPfOCol && kPfOCol + D <= kPfTileCols,
                 "tensor-memory columns");
   static_assert(kBytes <= 227 * 1024, "shared memory");
@@ -431,59 +433,54 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile]));
     }
     // every product of both tiles is complete (the staging below reuses the
-    // K and V rings that the other tile's last products may still read)
+    // rings and Q's room that the other tile's last products may still read)
     ok = mbar_wait(smem_addr(&bars->mma_done), 0) && ok;
     ok = __all_sync(0xffffffffu, ok);
-    // (m, l) of each row into the (free) K ring
-    reinterpret_cast<float2*>(pf_smem + L::kOffK)[tile * kPfRows + r] = make_float2(m, l0 + l1);
+    // (m, l) of each row where Q was
+    reinterpret_cast<float2*>(pf_smem)[tile * kPfRows + r] = make_float2(m, l0 + l1);
   }
-  // ---- epilogue, one query tile at a time: its rows' partials (o
-  // unnormalised) are staged in the (free) V ring (float rows of D, 16-byte
-  // chunk c of row r at chunk c ^ (r % (D/4))), then written to this
-  // split's slot with coalesced stores (softmax warp w rows w, w + 8, ...;
-  // lane l its 16-byte chunk).
+  // ---- epilogue: each tile's rows' partials (o unnormalised) are staged
+  // in shared memory (tile 0 in the V ring, tile 1 in the K ring; float
+  // rows of D, 16-byte chunk c of row r at chunk c ^ (r % (D/4))), then all
+  // 256 rows are written to this split's slot with coalesced stores
+  // (softmax warp w rows w, w + 8, ...; lane l its 16-byte chunk).
   constexpr int kCh = D / 4;
-  const uint32_t stage_addr = sv;
   const int64_t slot = static_cast<int64_t>(split) * p.num_seqs * p.num_q_heads;
   const bool soft = warp >= 2 && warp < kPfVWarp;
-  for (int t = 0; t < kPfTiles; ++t) {
-    if (soft && ((warp - 2) >> 2) == t && ok && n > 0) {
-      const int quarter = warp & 3, r = 32 * quarter + lane;
-      const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + t * kPfTileCols;
-      tc_fence_after_sync();
+  if (soft && ok && n > 0) {
+    const int t = (warp - 2) >> 2, quarter = warp & 3, r = 32 * quarter + lane;
+    const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + t * kPfTileCols;
+    const uint32_t stage_addr = t == 0 ? sv : sk;
+    tc_fence_after_sync();
 #pragma unroll
-      for (int part = 0; part < D / 32; ++part) {
-        uint32_t u[32];
-        tmem_ld32(tb + kPfOCol + part * 32, u);
-        tmem_wait_ld();
+    for (int part = 0; part < D / 32; ++part) {
+      uint32_t u[32];
+      tmem_ld32(tb + kPfOCol + part * 32, u);
+      tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int c = part * 8 + i;
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           stage_addr + (r * D + 4 * (c ^ (r & (kCh - 1)))) * 4),
-                       "r"(u[4 * i]), "r"(u[4 * i + 1]), "r"(u[4 * i + 2]), "r"(u[4 * i + 3])
-                       : "memory");
-        }
-      }
-      if (row0 + t * kPfRows + r < R) {
-        const float2 ml = reinterpret_cast<const float2*>(pf_smem + L::kOffK)[t * kPfRows + r];
-        p.pf_ml[slot + head_row(t * kPfRows + r)] = ml;
+      for (int i = 0; i < 8; ++i) {
+        const int c = part * 8 + i;
+        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                         stage_addr + (r * D + 4 * (c ^ (r & (kCh - 1)))) * 4),
+                     "r"(u[4 * i]), "r"(u[4 * i + 1]), "r"(u[4 * i + 2]), "r"(u[4 * i + 3])
+                     : "memory");
       }
     }
-    if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
-    if (soft && ok && n > 0) {
-      for (int rr = warp - 2; rr < kPfRows && row0 + t * kPfRows + rr < R; rr += kPfSoftWarps)
-        if (lane < kCh) {
-          float4 x;
-          asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                       : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                       : "r"(stage_addr + (rr * D + 4 * (lane ^ (rr & (kCh - 1)))) * 4)
-                       : "memory");
-          reinterpret_cast<float4*>(p.pf_o + (slot + head_row(t * kPfRows + rr)) * D)[lane] = x;
-        }
+    if (row0 + t * kPfRows + r < R)
+      p.pf_ml[slot + head_row(t * kPfRows + r)] =
+          reinterpret_cast<const float2*>(pf_smem)[t * kPfRows + r];
+  }
+  if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
+  if (soft && ok && n > 0 && lane < kCh) {
+    for (int rr = warp - 2; rr < kPfTiles * kPfRows && row0 + rr < R; rr += kPfSoftWarps) {
+      const int t = rr / kPfRows, r = rr % kPfRows;
+      float4 x;
+      asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                   : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                   : "r"((t == 0 ? sv : sk) + (r * D + 4 * (lane ^ (r & (kCh - 1)))) * 4)
+                   : "memory");
+      reinterpret_cast<float4*>(p.pf_o + (slot + head_row(rr)) * D)[lane] = x;
     }
-    // the next tile is staged once every row of this one is out
-    if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
   }
   tc_fence_before_sync();
   __syncthreads();
