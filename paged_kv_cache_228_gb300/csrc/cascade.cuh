@@ -90,8 +90,8 @@ struct PfSmem {
   static constexpr int kOffV = kOffK + kPfKStages * kKV;
   static constexpr int kOffBar = kOffV + kPfVStages * kKV;
   static constexpr int kBytes = kOffBar + 256;
-  // the epilogue stages tile 0's partial in the (free) V ring, tile 1's in
-  // the (free) K ring and the per-row (m, l) where Q was
+  // the epilogue stages tile 0's partial in the (free) K ring, tile 1's in
+  // the (free) V ring and the per-row (m, l) where Q was
   static_assert(kPfTiles == 2 && kPfRows * D * 4 <= kPfVStages * kKV &&
                     kPfRows * D * 4 <= kPfKStages * kKV,
                 "epilogue staging");
@@ -106,6 +106,7 @@ struct PfBars {
   uint64_t v_full[kPfVStages], v_empty[kPfVStages];
   uint64_t s_full[kPfTiles];  // S of the tile's chunk written (and its last product done)
   uint64_t p_full[kPfTiles];  // P of the tile's chunk written
+  uint64_t o_last[kPfTiles];  // the tile's last product (and every MMA before it) done
   uint64_t mma_done;
   uint32_t tmem;
 };
@@ -235,6 +236,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     for (int t = 0; t < kPfTiles; ++t) {
       mbar_init(smem_addr(&bars->s_full[t]), 1);
       mbar_init(smem_addr(&bars->p_full[t]), 4);
+      mbar_init(smem_addr(&bars->o_last[t]), 1);
     }
     mbar_init(smem_addr(&bars->mma_done), 1);
     mbar_fence_init();
@@ -332,6 +334,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
           umma_commit(smem_addr(&bars->k_empty[0]));
         }
       }
+      uint32_t last = 0;  // tiles whose o_last has been committed
       for (int32_t j = 0; j < n && ok; ++j) {
         const int vs = j % kPfVStages, ks = (j + 1) % kPfKStages;
         const bool more = j + 1 < n;
@@ -351,12 +354,20 @@ __global__ void __launch_bounds__(kPfThreads, 1)
             umma_bf16_ta(tt + kPfOCol, tt + kPfSCol + k * 8,
                          smem_desc_sw128(vb + k * 16 * 128, L::kSlab, 1024), kIdPV,
                          j > 0 || k > 0);
-          if (more) qk(t, kb);
+          if (more) {
+            qk(t, kb);
+          } else {
+            umma_commit(smem_addr(&bars->o_last[t]));
+            last |= 1u << t;
+          }
         }
         if (!ok) break;
         umma_commit(smem_addr(&bars->v_empty[vs]));
         if (more) umma_commit(smem_addr(&bars->k_empty[ks]));
       }
+      // a wait that failed still releases the softmax warps
+      for (int t = 0; t < kPfTiles; ++t)
+        if (!(last >> t & 1u)) umma_commit(smem_addr(&bars->o_last[t]));
       // every MMA this thread issued has completed before the tensor
       // memory is released
       umma_commit(smem_addr(&bars->mma_done));
@@ -432,54 +443,60 @@ __global__ void __launch_bounds__(kPfThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_addr(&bars->p_full[tile]));
     }
-    // every product of both tiles is complete (the staging below reuses the
-    // rings and Q's room that the other tile's last products may still read)
-    ok = mbar_wait(smem_addr(&bars->mma_done), 0) && ok;
+    // this tile's last product is complete, and with it every score MMA
+    // (issued before it) and the other tile's products but its last one: the
+    // K ring and Q's room are free, the V ring once the other tile is done
+    ok = mbar_wait(smem_addr(&bars->o_last[tile]), 0) && ok;
     ok = __all_sync(0xffffffffu, ok);
     // (m, l) of each row where Q was
     reinterpret_cast<float2*>(pf_smem)[tile * kPfRows + r] = make_float2(m, l0 + l1);
   }
-  // ---- epilogue: each tile's rows' partials (o unnormalised) are staged
-  // in shared memory (tile 0 in the V ring, tile 1 in the K ring; float
-  // rows of D, 16-byte chunk c of row r at chunk c ^ (r % (D/4))), then all
-  // 256 rows are written to this split's slot with coalesced stores
-  // (softmax warp w rows w, w + 8, ...; lane l its 16-byte chunk).
+  // ---- epilogue, each tile as soon as its last product is done: its
+  // rows' partials (o unnormalised) are staged in shared memory (tile 0 in
+  // the K ring, tile 1 in the V ring; float rows of D, 16-byte chunk c of
+  // row r at chunk c ^ (r % (D/4))), then written to this split's slot with
+  // coalesced stores by the tile's four warps (warp w of the tile rows w,
+  // w + 4, ...; lane l its 16-byte chunk).
   constexpr int kCh = D / 4;
   const int64_t slot = static_cast<int64_t>(split) * p.num_seqs * p.num_q_heads;
-  const bool soft = warp >= 2 && warp < kPfVWarp;
-  if (soft && ok && n > 0) {
+  if (warp >= 2 && warp < kPfVWarp) {
     const int t = (warp - 2) >> 2, quarter = warp & 3, r = 32 * quarter + lane;
-    const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + t * kPfTileCols;
-    const uint32_t stage_addr = t == 0 ? sv : sk;
-    tc_fence_after_sync();
+    const uint32_t stage_addr = t == 0 ? sk : sv;
+    const bool go = ok && n > 0;
+    if (go) {
+      const uint32_t tb = tmem + (static_cast<uint32_t>(32 * quarter) << 16) + t * kPfTileCols;
+      tc_fence_after_sync();
 #pragma unroll
-    for (int part = 0; part < D / 32; ++part) {
-      uint32_t u[32];
-      tmem_ld32(tb + kPfOCol + part * 32, u);
-      tmem_wait_ld();
+      for (int part = 0; part < D / 32; ++part) {
+        uint32_t u[32];
+        tmem_ld32(tb + kPfOCol + part * 32, u);
+        tmem_wait_ld();
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int c = part * 8 + i;
-        asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                         stage_addr + (r * D + 4 * (c ^ (r & (kCh - 1)))) * 4),
-                     "r"(u[4 * i]), "r"(u[4 * i + 1]), "r"(u[4 * i + 2]), "r"(u[4 * i + 3])
-                     : "memory");
+        for (int i = 0; i < 8; ++i) {
+          const int c = part * 8 + i;
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           stage_addr + (r * D + 4 * (c ^ (r & (kCh - 1)))) * 4),
+                       "r"(u[4 * i]), "r"(u[4 * i + 1]), "r"(u[4 * i + 2]), "r"(u[4 * i + 3])
+                       : "memory");
+        }
       }
+      if (row0 + t * kPfRows + r < R)
+        p.pf_ml[slot + head_row(t * kPfRows + r)] =
+            reinterpret_cast<const float2*>(pf_smem)[t * kPfRows + r];
     }
-    if (row0 + t * kPfRows + r < R)
-      p.pf_ml[slot + head_row(t * kPfRows + r)] =
-          reinterpret_cast<const float2*>(pf_smem)[t * kPfRows + r];
-  }
-  if (soft) asm volatile("bar.sync 2, %0;" ::"r"(32 * kPfSoftWarps) : "memory");
-  if (soft && ok && n > 0 && lane < kCh) {
-    for (int rr = warp - 2; rr < kPfTiles * kPfRows && row0 + rr < R; rr += kPfSoftWarps) {
-      const int t = rr / kPfRows, r = rr % kPfRows;
-      float4 x;
-      asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
-                   : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                   : "r"((t == 0 ? sv : sk) + (r * D + 4 * (lane ^ (r & (kCh - 1)))) * 4)
-                   : "memory");
-      reinterpret_cast<float4*>(p.pf_o + (slot + head_row(rr)) * D)[lane] = x;
+    if (t == 0)
+      asm volatile("bar.sync 2, 128;" ::: "memory");
+    else
+      asm volatile("bar.sync 3, 128;" ::: "memory");
+    if (go && lane < kCh) {
+      for (int r2 = quarter; r2 < kPfRows && row0 + t * kPfRows + r2 < R; r2 += 4) {
+        float4 x;
+        asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+                     : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                     : "r"(stage_addr + (r2 * D + 4 * (lane ^ (r2 & (kCh - 1)))) * 4)
+                     : "memory");
+        reinterpret_cast<float4*>(p.pf_o + (slot + head_row(t * kPfRows + r2)) * D)[lane] = x;
+      }
     }
   }
   tc_fence_before_sync();
