@@ -83,7 +83,9 @@ struct DecodeParams {
   int32_t rows_total;  // num_blocks * num_kv_heads * block_size
   float scale_log2;    // softmax scale * log2(e)
   int32_t num_ctas;    // P
-  int32_t seg_cost;    // work split: units charged per segment (a tile is kUnit)
+  int32_t seg_cost;    // work split: units charged per segment (a work unit is kUnit)
+  int32_t tile_log2;   // work unit of the split: 2^tile_log2 16-token tiles (0 but in
+                       // kernels that take a segment in larger chunks)
   int32_t stages;      // ring depth
   // Bounded waits: polls before a math-warp wait gives up (PA_DEVERR_TIMEOUT;
   // the copy warp's waits keep the fixed default bound: a run-time bound
@@ -133,7 +135,7 @@ __device__ __forceinline__ int32_t cdiv16(int32_t n) { return (n + 15) >> 4; }
 
 // Tiles of a sequence of n tokens in this call (its tokens from `skip` on).
 __device__ __forceinline__ int32_t seg_tiles(const DecodeParams& p, int32_t n) {
-  return n > p.skip ? cdiv16(n - p.skip) : 0;
+  return n > p.skip ? (cdiv16(n - p.skip) + (1 << p.tile_log2) - 1) >> p.tile_log2 : 0;
 }
 
 __device__ __forceinline__ int32_t clamp_len(const DecodeParams& p, int32_t n) {

@@ -133,33 +133,42 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int stages) {
 }
 
 // ------------------------------------------------------------ chunking ---
-// A chunk: up to kTcTiles consecutive tiles of one segment in this CTA's
-// range.  Every role walks the same sequence of chunks.
+// The work split runs in whole chunks (tile_log2 = log2 kTcTiles: a
+// segment is ceil(n / 256) work units), so a CTA's range never cuts a chunk
+// and every chunk but a segment's last is full: a chunk costs about the
+// same whatever its number of tokens.  A chunk: the kTcTiles tiles of one
+// work unit of a segment (fewer at the sequence's end).  Every role walks
+// the same sequence of chunks.
 struct TcIter {
-  Cursor c;         // segment and the chunk's first tile
-  int64_t u;        // flat index of that tile
-  int64_t useg;     // flat index of the segment's tile 0
-  int32_t seg_end;  // end of this CTA's part (piece) of the segment
-  int32_t nt;       // tiles in the chunk; 0 past the range
+  Cursor c;         // segment; c.tile, c.T in chunks
+  int64_t u;        // flat index of the chunk
+  int64_t useg;     // flat index of the segment's chunk 0
+  int32_t seg_end;  // end of this CTA's part (piece) of the segment, in chunks
+  int32_t nt;       // 16-token tiles in the chunk; 0 past the range
   bool first;       // the chunk opens the piece
   bool whole;       // the piece is the whole segment
 };
+
+// 16-token tiles of chunk c.tile of the sequence.
+__device__ __forceinline__ int32_t tc_chunk_tiles(const Cursor& c) {
+  return min(kTcTiles, cdiv16(c.n) - c.tile * kTcTiles);
+}
 
 __device__ __forceinline__ void tc_open_piece(TcIter& it, int64_t hi) {
   it.seg_end = static_cast<int32_t>(min(static_cast<int64_t>(it.c.T), it.c.tile + (hi - it.u)));
   it.useg = it.u - it.c.tile;
   it.whole = it.c.tile == 0 && it.seg_end == it.c.T;
   it.first = true;
-  it.nt = min(kTcTiles, it.seg_end - it.c.tile);
+  it.nt = tc_chunk_tiles(it.c);
 }
 
 __device__ __forceinline__ void tc_next(const DecodeParams& p, TcIter& it, int64_t hi) {
   if (it.nt == 0) return;
-  it.u += it.nt;
-  it.c.tile += it.nt;
+  ++it.u;
+  ++it.c.tile;
   if (it.c.tile < it.seg_end) {
     it.first = false;
-    it.nt = min(kTcTiles, it.seg_end - it.c.tile);
+    it.nt = tc_chunk_tiles(it.c);
     return;
   }
   if (it.u >= hi) {
@@ -170,13 +179,11 @@ __device__ __forceinline__ void tc_next(const DecodeParams& p, TcIter& it, int64
   tc_open_piece(it, hi);
 }
 
-__device__ __forceinline__ bool tc_last(const TcIter& it) {
-  return it.c.tile + it.nt == it.seg_end;
-}
+__device__ __forceinline__ bool tc_last(const TcIter& it) { return it.c.tile + 1 == it.seg_end; }
 
 // Tokens of the chunk inside the sequence (>= 1).
 __device__ __forceinline__ int32_t tc_valid(const TcIter& it) {
-  return min(it.nt * kTile, it.c.n - it.c.tile * kTile);
+  return min(it.nt * kTile, it.c.n - it.c.tile * kTcTok);
 }
 
 // --------------------------------------------------------------- copies ---
@@ -187,7 +194,7 @@ __device__ __forceinline__ void tc_fetch_entry(const DecodeParams& p, const TcIt
                                                uint32_t dst) {
   const int lane = threadIdx.x & 31;
   const int32_t t = lane >> lr;
-  const int32_t tok = (it.c.tile + t) * kTile + (lane & ((1 << lr) - 1)) * p.block_size;
+  const int32_t tok = (it.c.tile * kTcTiles + t) * kTile + (lane & ((1 << lr) - 1)) * p.block_size;
   if (it.nt == 0 || t >= it.nt || tok >= it.c.n) {
     asm volatile("st.shared.b32 [%0], %1;" ::"r"(dst), "r"(-2) : "memory");
     return;
@@ -256,7 +263,7 @@ __device__ __forceinline__ void tc_produce(const DecodeParams& p, const CUtensor
     if (has && (mine || part == 0)) {
       int32_t row;
       if (good) {
-        const int32_t tok = (it0.c.tile + (lane >> lr)) * kTile;
+        const int32_t tok = (it0.c.tile * kTcTiles + (lane >> lr)) * kTile;
         row = (e * p.num_kv_heads + it0.c.g) * p.block_size + (lr ? 0 : (tok & (p.block_size - 1)));
       } else {
         if (mine) flag_error(PA_DEVERR_BAD_BLOCK_ID);

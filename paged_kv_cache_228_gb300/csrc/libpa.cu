@@ -249,13 +249,15 @@ pa_status fp4_plan(int dev, int* ctas_per_sm) {
 }
 
 // What the work split charges per (sequence, KV head) segment, in units
-// of kUnit = 8 per tile: the segment's query copy, first table batch and
-// finish.  Two tiles' worth was the best of 8..24 on every kernel shape
-// on the Llama-3.1-8B-shaped layer (~837 tokens a sequence).
+// of kUnit = 8 per work unit: the segment's query copy, first table batch
+// and finish.  Two tiles' worth was the best of 8..24 on every kernel shape
+// on the Llama-3.1-8B-shaped layer (~837 tokens a sequence).  The tcgen05
+// FP8 kernel's work unit is a 256-token chunk; per-CTA timestamps on that
+// layer fit 1.0 us per chunk and 0.7 us per piece of a segment.
 constexpr int32_t kSegCostBf16 = 16;
 constexpr int32_t kSegCostFp8 = 16;
 constexpr int32_t kSegCostFp4 = 16;
-constexpr int32_t kSegCostTc = 128;
+constexpr int32_t kSegCostTc = 6;
 
 // Workspace for P decode CTAs over `segs` segments: P + segs partial
 // slots (a CTA's pieces never collide: piece = cta + segment), then P
@@ -367,6 +369,7 @@ pa_status launch_decode_tc(const DecodeParams& prm_in, const void* q, const void
   DecodeParams prm = prm_in;
   prm.num_ctas = P;
   prm.seg_cost = kSegCostTc;
+  prm.tile_log2 = 4;  // the split in whole 256-token chunks
   prm.stages = plan.stages;
   prm.wait_limit = g_wait_limit.load(std::memory_order_relaxed);
   prm.stall = g_wait_stall.load(std::memory_order_relaxed);
