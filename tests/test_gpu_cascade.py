@@ -5,7 +5,7 @@ nothing of prefixes: it attends over each sequence's whole gathered cache.
 
 Cases: the shared-prefix workload (256 forks of a 2048-token prompt) at
 block sizes 8, 16 and 32 with automatic and fixed partition counts;
-head_dim 64; negative and zero scales; a cascade prefix shorter than the
+head_dim 64; GQA groups of 8, 1 and 3; negative and zero scales; a cascade prefix shorter than the
 shared one (down to a partial last chunk); sequences that
 end exactly at the prefix (prefix partial alone) and one shorter than it
 (zeros, flagged); agreement with pa_decode on the same inputs.
@@ -95,6 +95,24 @@ def test_cascade_negative_and_zero_scale(sign):
     scale = sign * w.scale
     ref = oracle_decode(case, snap, seqs, scale=scale)
     assert_close(_cascade(case, 528, scale=scale), ref, TOL, f"cascade scale {scale}")
+    assert pa.pa_get_device_error() == 0
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 1), (8, 8), (12, 4)])
+def test_cascade_group_sizes(hq, hkv):
+    # GQA groups of 8, 1 (MHA) and 3 (not a power of two) in the prefix
+    # pass's row blocks of 256 (query rows (sequence, head) of one KV head);
+    # 37 sequences leave a partial last block at every group size, and a
+    # 272-token prefix a partial last chunk
+    base = W.shared_prefix(16, num_seqs=37, prefix=272)
+    w = W.Workload(f"cascade_g{hq // hkv}", 37, hq, hkv, 128, 16, seq_lens=base.seq_lens,
+                   pool_blocks=base.pool_blocks, seed=11, shared_prefix=272)
+    case = build_case(w)
+    seqs = list(range(w.num_seqs))
+    snap = snapshot_blocks(case, seqs)
+    pa.pa_cache_write(case.k_new, case.v_new, case.slots_t, case.k_cache, case.v_cache)
+    ref = oracle_decode(case, snap, seqs)
+    assert_close(_cascade(case, 272), ref, TOL, f"cascade G={hq // hkv}")
     assert pa.pa_get_device_error() == 0
 
 
