@@ -156,39 +156,72 @@ __device__ __forceinline__ void pf_copy_chunk(const PrefixParams& p, const CUten
   }
 }
 
+// Three-input maximum, one instruction.
+__device__ __forceinline__ float pf_fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// a * b + c and a + b on pairs of fp32 values, one instruction each, each
+// half rounded as fmaf / an fp32 add would.
+__device__ __forceinline__ float2 pf_fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 pf_add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+
 // The largest raw score among 32 columns of a thread's row (chunk columns
 // c0 .. c0 + 31), over those before `valid` when kMask, folded into `acc`.
-// Four independent maxima keep the dependency chain short.
+// Two independent three-input maxima keep the chain short.
 template <bool kMask>
 __device__ __forceinline__ float pf_max32(const uint32_t (&u)[32], int32_t c0, int32_t valid,
                                           float acc) {
-  float a[4] = {acc, -INFINITY, -INFINITY, -INFINITY};
+  auto v = [&](int i) {
+    return !kMask || c0 + i < valid ? __uint_as_float(u[i]) : -INFINITY;
+  };
+  float a0 = acc, a1 = -INFINITY;
 #pragma unroll
-  for (int i = 0; i < 32; ++i)
-    a[i & 3] = fmaxf(a[i & 3], !kMask || c0 + i < valid ? __uint_as_float(u[i]) : -INFINITY);
-  return fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+  for (int i = 0; i < 32; i += 4) {
+    a0 = pf_fmax3(a0, v(i), v(i + 1));
+    a1 = pf_fmax3(a1, v(i + 2), v(i + 3));
+  }
+  return fmaxf(a0, a1);
 }
 
 // The weights 2^(s * sl - m) (neg = -m) of 32 columns, rounded to bf16
 // pairs: w[c] holds columns 2c (low half) and 2c + 1, the layout of the
 // P.V product's A operand in tensor memory; columns from `valid` on weigh
-// 0 when kMask.  l0 + l1 gains the sum of the rounded weights.
+// 0 when kMask.  l (one sum per half of the pairs) gains the sum of the
+// rounded weights.
 template <bool kMask>
 __device__ __forceinline__ void pf_weights32(const uint32_t (&u)[32], int32_t c0, int32_t valid,
-                                             float sl, float neg, uint32_t (&w)[16], float& l0,
-                                             float& l1) {
+                                             float sl, float neg, uint32_t (&w)[16], float2& l) {
+  const float2 s2 = make_float2(sl, sl), n2 = make_float2(neg, neg);
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
-    float e0 = fast_exp2(fmaf(__uint_as_float(u[2 * c]), sl, neg));
-    float e1 = fast_exp2(fmaf(__uint_as_float(u[2 * c + 1]), sl, neg));
+    const float2 x =
+        pf_fma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), s2, n2);
+    float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
     if (kMask) {
       e0 = c0 + 2 * c < valid ? e0 : 0.f;
       e1 = c0 + 2 * c + 1 < valid ? e1 : 0.f;
     }
     w[c] = pack_bf16x2(e0, e1);
-    const float2 f = unpack_bf16x2(w[c]);
-    l0 += f.x;
-    l1 += f.y;
+    l = pf_add2(l, unpack_bf16x2(w[c]));
   }
 }
 
@@ -382,7 +415,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     const uint32_t tb =
         tmem + (static_cast<uint32_t>(32 * quarter) << 16) + tile * kPfTileCols;
     const float sl = fabsf(p.scale_log2);
-    float m = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float m = -INFINITY;
+    float2 l = make_float2(0.f, 0.f);
     for (int32_t j = 0; j < n; ++j) {
       ok = mbar_wait(smem_addr(&bars->s_full[tile]), j & 1);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -412,8 +446,8 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         const float mn = fmaxf(m, mx);
         const float alpha = fast_exp2(m - mn);
         m = mn;
-        l0 *= alpha;
-        l1 *= alpha;
+        l.x *= alpha;
+        l.y *= alpha;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t u[32];
@@ -433,9 +467,9 @@ __global__ void __launch_bounds__(kPfThreads, 1)
         tmem_ld32(tb + kPfSCol + 32 * c, u);
         tmem_wait_ld();
         if (part)
-          pf_weights32<true>(u, 32 * c, valid, sl, neg, w, l0, l1);
+          pf_weights32<true>(u, 32 * c, valid, sl, neg, w, l);
         else
-          pf_weights32<false>(u, 32 * c, valid, sl, neg, w, l0, l1);
+          pf_weights32<false>(u, 32 * c, valid, sl, neg, w, l);
         tmem_st16(tb + kPfSCol + 16 * c, w);
       }
       tmem_wait_st();
@@ -449,7 +483,7 @@ __global__ void __launch_bounds__(kPfThreads, 1)
     ok = mbar_wait(smem_addr(&bars->o_last[tile]), 0) && ok;
     ok = __all_sync(0xffffffffu, ok);
     // (m, l) of each row where Q was
-    reinterpret_cast<float2*>(pf_smem)[tile * kPfRows + r] = make_float2(m, l0 + l1);
+    reinterpret_cast<float2*>(pf_smem)[tile * kPfRows + r] = make_float2(m, l.x + l.y);
   }
   // ---- epilogue, each tile as soon as its last product is done: its
   // rows' partials (o unnormalised) are staged in shared memory (tile 0 in
