@@ -156,34 +156,6 @@ __device__ __forceinline__ void pf_copy_chunk(const PrefixParams& p, const CUten
   }
 }
 
-// Three-input maximum, one instruction.
-__device__ __forceinline__ float pf_fmax3(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-
-// a * b + c and a + b on pairs of fp32 values, one instruction each, each
-// half rounded as fmaf / an fp32 add would.
-__device__ __forceinline__ float2 pf_fma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
-}
-__device__ __forceinline__ float2 pf_add2(float2 a, float2 b) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
-      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-  return d;
-}
-
 // The largest raw score among 32 columns of a thread's row (chunk columns
 // c0 .. c0 + 31), over those before `valid` when kMask, folded into `acc`.
 // Two independent three-input maxima keep the chain short.
@@ -196,8 +168,8 @@ __device__ __forceinline__ float pf_max32(const uint32_t (&u)[32], int32_t c0, i
   float a0 = acc, a1 = -INFINITY;
 #pragma unroll
   for (int i = 0; i < 32; i += 4) {
-    a0 = pf_fmax3(a0, v(i), v(i + 1));
-    a1 = pf_fmax3(a1, v(i + 2), v(i + 3));
+    a0 = fmax3(a0, v(i), v(i + 1));
+    a1 = fmax3(a1, v(i + 2), v(i + 3));
   }
   return fmaxf(a0, a1);
 }
@@ -214,14 +186,14 @@ __device__ __forceinline__ void pf_weights32(const uint32_t (&u)[32], int32_t c0
 #pragma unroll
   for (int c = 0; c < 16; ++c) {
     const float2 x =
-        pf_fma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), s2, n2);
+        fma2(make_float2(__uint_as_float(u[2 * c]), __uint_as_float(u[2 * c + 1])), s2, n2);
     float e0 = fast_exp2(x.x), e1 = fast_exp2(x.y);
     if (kMask) {
       e0 = c0 + 2 * c < valid ? e0 : 0.f;
       e1 = c0 + 2 * c + 1 < valid ? e1 : 0.f;
     }
     w[c] = pack_bf16x2(e0, e1);
-    l = pf_add2(l, unpack_bf16x2(w[c]));
+    l = add2(l, unpack_bf16x2(w[c]));
   }
 }
 

@@ -615,12 +615,17 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
         const float ks = hdr->sk[st][box];
         vs[h] = valid[h] ? hdr->sv[st][box] : 0.f;
         vsm = fmaxf(vsm, vs[h]);
+        // heads in pairs: s = hi + lo / 16, x = s * k_scale * scale / 2^s
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-          const float s =
-              fmaf(__uint_as_float(sr[h][H + i]), 0.0625f, __uint_as_float(sr[h][i]));
-          x[h][i] = valid[h] ? s * (ks * hm[i]) : -INFINITY;
-          gr |= x[h][i] > mt[i];
+        for (int i = 0; i < H; i += 2) {
+          const float2 sv = fma2(
+              make_float2(__uint_as_float(sr[h][H + i]), __uint_as_float(sr[h][H + i + 1])),
+              make_float2(0.0625f, 0.0625f),
+              make_float2(__uint_as_float(sr[h][i]), __uint_as_float(sr[h][i + 1])));
+          const float2 xv = mul2(sv, mul2(make_float2(ks, ks), make_float2(hm[i], hm[i + 1])));
+          x[h][i] = valid[h] ? xv.x : -INFINITY;
+          x[h][i + 1] = valid[h] ? xv.y : -INFINITY;
+          gr |= x[h][i] > mt[i] || x[h][i + 1] > mt[i + 1];
         }
       }
       const uint32_t wv = __reduce_max_sync(0xffffffffu, __float_as_uint(vsm));  // vs >= 0
@@ -661,10 +666,15 @@ __device__ __forceinline__ void tc_softmax(const DecodeParams& p, uint32_t ring,
         const float r = vs[h] * rinv;
         float pq[H];
 #pragma unroll
-        for (int i = 0; i < H; ++i) {
-          const float pp = fast_exp2(x[h][i] - m[i]);
-          l[i] += pp;
-          pq[i] = pp * r;
+        for (int i = 0; i < H; i += 2) {
+          const float2 d = add2(make_float2(x[h][i], x[h][i + 1]), make_float2(-m[i], -m[i + 1]));
+          const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+          const float2 ls = add2(make_float2(l[i], l[i + 1]), pp);
+          l[i] = ls.x;
+          l[i + 1] = ls.y;
+          const float2 q2 = mul2(pp, make_float2(r, r));
+          pq[i] = q2.x;
+          pq[i + 1] = q2.y;
         }
         uint32_t h0, l0, h1, l1;
         split_e4m3x2(pq[0], pq[1], h0, l0);
