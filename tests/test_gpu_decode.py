@@ -368,12 +368,14 @@ def test_fp8_repeated_decode_is_bit_identical(splits):
 
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_fp8_empty_and_ragged_sequences_poisoned_tails(bs):
-    # lengths around the 16-token tile, the 32-token MMA step and the
-    # 128-token chunk; the codes past each sequence's end are NaN
-    lens = [0, 1, 15, 16, 17, 31, 32, 33, 127, 128, 129, 0, 255, 257, 300, 511]
+    # lengths around the 16-token tile, the 32-token MMA step, the 128-token
+    # half chunk and the 256-token chunk (the tensor-core kernel's work
+    # unit); the codes past each sequence's end are NaN
+    lens = [0, 1, 15, 16, 17, 31, 32, 33, 127, 128, 129, 0, 255, 256, 257, 300, 511, 512,
+            513, 767, 768, 769]
     w = W.Workload("ragged128", len(lens), 32, 8, 128, bs,
-                   seq_lens=[max(1, n) for n in lens], pool_blocks=2 * (512 // bs) * 8,
-                   seed=22)
+                   seq_lens=[max(1, n) for n in lens],
+                   pool_blocks=sum(-(-max(1, n) // bs) for n in lens) + 8, seed=22)
     case = build_case(w)
     case.w.seq_lens = lens
     case.lens_t = torch.tensor(lens, dtype=torch.int32, device="cuda")
